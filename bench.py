@@ -1,0 +1,462 @@
+"""Benchmark of the rolling-KV hot path on B300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+rkv_append (bookkeeping + scatter, one kernel), rkv_rebase (no launch for the
+pre-RoPE layout; the re-rotation kernel for the stored-rotated one) and
+rkv_attend over every layer (one kernel).  Default workload: the 36-layer GQA
+16/2 x 128 decoder shape, one stream, window 4096, full (steady state: one
+pair evicted per step), as BASELINE's metric is quoted on.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...      # the float64 CPU oracle
+
+Timing: K steps bracketed by a barrier + synchronize; each step's kernels are
+timed with CUDA events on the launching stream, and a 256 MiB buffer is
+written between steps (outside the events) so every step starts with a cold
+L2.  ``value`` = K/V bytes read per step / event time per step (whole job:
+all ranks' bytes over the slowest rank).  Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "rolling-KV decode attention µs/step & achieved HBM GB/s (% of B300 peak)"
+L2_FLUSH_BYTES = 256 << 20
+
+WORKLOAD_TEXT = {
+    "qwen3b": "36 layers, GQA 16 query / 2 KV heads, head_dim 128, bf16 K/V, window 4096, "
+              "1 stream, 1 token per step, full window (one eviction per step)",
+    "qwen3b_stored": "as qwen3b, stored-rotated keys: append + re-rotation of all retained "
+                     "keys + attend",
+    "qwen3b_chunk6": "as qwen3b, 6 tokens per step (causal among the 6), 1% of k rows x2",
+    "audio8": "8 layers, MHA 8 heads, head_dim 64, bf16 K/V, window 1024, 1 stream, 1 token "
+              "per step, full window",
+    "batch64": "64 streams, 36 layers, GQA 16/2 x 128, bf16, window 8192 each, fills uniform in "
+               "[1, 8192], origins uniform in [0, 1e6), 1 token per stream per step",
+}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def _workload(name):
+    from rkv_inputs import WORKLOADS
+    if name == "qwen3b_stored":
+        return WORKLOADS["qwen3b"], "stored_rotated"
+    return WORKLOADS[name], "pre_rope"
+
+
+def _kv_bytes_per_step(wl, fills):
+    """Algorithmic K/V bytes the attention reads: every retained pair once."""
+    return sum(fills) * wl.n_layers * wl.n_kv_heads * wl.head_dim * wl.elem_bytes * 2
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rolling_kv_cache_buffer_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since the counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            d = json.load(f)
+        ent = d.get(kernel_key)
+        if ent and ent.get("source_hash") == _kernel_hash():
+            return ent["bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, rank, world):
+    import torch
+
+    from rkv_inputs import initial_states, step_inputs
+    from rolling_kv_cache_buffer_b300 import RollingKV
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl, layout = _workload(args.workload)
+    c = wl.n_new
+    cache = RollingKV(wl.n_streams, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                      wl.capacity, max_chunk=c, kv_dtype=wl.kv_dtype, layout=layout,
+                      rope_theta=wl.rope_theta, attend_impl=args.attend_impl, device=dev)
+    # Steady-state windows: random contents (inputs of the path, not its work).
+    gen = torch.Generator(device=dev).manual_seed(1234 + rank)
+    cache.k_pool.normal_(generator=gen)
+    cache.v_pool.normal_(generator=gen)
+    if wl.random_state:
+        origins, fills = initial_states(wl)
+    else:
+        origins, fills = [123_456] * wl.n_streams, [wl.capacity] * wl.n_streams
+    for s in range(wl.n_streams):
+        cache.set_stream_state(s, origins[s], fills[s])
+    dt = cache.kv_dtype
+
+    # Pre-staged step inputs (a ring cycled by the timed loop).
+    ring = []
+    for t in range(args.ring):
+        q, k, v = step_inputs(wl, 1 + t)
+        ring.append((q.to(dt).to(dev), k.to(dt).to(dev), v.to(dt).to(dev)))
+    out = torch.empty(ring[0][0].shape, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        q, k, v = ring[i % len(ring)]
+        if ev:
+            ev[0].record(stream)
+        cache.append(k, v)
+        cache.rebase()
+        if ev:
+            ev[1].record(stream)
+        cache.attend(q, out)
+        if ev:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize(dev)
+    launches_per_step = 2 + (1 if layout == "stored_rotated" else 0)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()                      # cold L2 for every step (outside the events)
+            step(args.warmup + i, evs[i])
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    attend_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    append_ms = [e[0].elapsed_time(e[1]) for e in evs]
+
+    # Each step attends over the post-append window: fill' = min(W, fill + c).
+    fl = list(fills)
+    for _ in range(args.warmup):
+        fl = [min(wl.capacity, f + c) for f in fl]
+    bytes_per_step = []
+    for i in range(args.steps):
+        fl = [min(wl.capacity, f + c) for f in fl]
+        bytes_per_step.append(_kv_bytes_per_step(wl, fl))
+    # the e2e loop continues from here
+    res_fills = fl
+    total_bytes = sum(bytes_per_step)
+    total_ms = sum(step_ms)
+    assert torch.isfinite(out).all(), "non-finite attention output"
+
+    # e2e: host buffers through the public API, copies inside the timed region.
+    e2e = run_e2e(args, cache, ring, dev, wl, stream)
+
+    res = dict(total_bytes=total_bytes, total_ms=total_ms, steps=args.steps,
+               step_ms=step_ms, attend_ms=attend_ms, append_ms=append_ms, wall_s=wall,
+               clocks=clk.summary(), launches=launches_per_step * args.steps,
+               bytes_per_step=bytes_per_step, e2e=e2e, fills=res_fills)
+    return res
+
+
+def run_e2e(args, cache, ring, dev, wl, stream):
+    import torch
+    host = []
+    for q, k, v in ring[: min(len(ring), 16)]:
+        host.append((q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()))
+    dq = torch.empty_like(ring[0][0])
+    dk = torch.empty_like(ring[0][1])
+    dv = torch.empty_like(ring[0][2])
+    out = torch.empty(dq.shape, dtype=torch.float32, device=dev)
+    hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    steps = max(10, args.steps // 2)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def one(i):
+        q, k, v = host[i % len(host)]
+        dq.copy_(q, non_blocking=True)
+        dk.copy_(k, non_blocking=True)
+        dv.copy_(v, non_blocking=True)
+        cache.append(dk, dv)
+        cache.rebase()
+        cache.attend(dq, out)
+        hout.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize(dev)
+    ev[0].record(stream)
+    for i in range(steps):
+        one(i)
+    ev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev[0].elapsed_time(ev[1]) / steps
+    h2d = sum(t.numel() * t.element_size() for t in host[0])
+    d2h = hout.numel() * hout.element_size()
+    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reported baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleRunner:
+    """The float64 oracle (as it stands) on a bounded sample of the workload:
+    at most two streams and `layers` of the layers, the window seeded to the
+    workload's steady state.  One call of step() runs one whole step of the
+    sample (append + re-rotation for stored-rotated + attend); its time is
+    scaled to the full workload by streams x layers."""
+
+    def __init__(self, wl_name, layers=2):
+        from oracle import rkv_oracle as O
+        from rkv_inputs import initial_states, initial_window
+        self.wl, layout = _workload(wl_name)
+        wl = self.wl
+        self.S = min(wl.n_streams, 2)
+        self.Ls = min(wl.n_layers, layers)
+        self.stored = layout == "stored_rotated"
+        cls = O.StoredRotatedOracle if self.stored else O.RollingCacheOracle
+        self.orc = cls(self.S, self.Ls, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.capacity,
+                       theta=wl.rope_theta)
+        if wl.random_state:
+            origins, fills = initial_states(wl)
+        else:
+            origins, fills = [123_456] * wl.n_streams, [wl.capacity] * wl.n_streams
+        self.fills = fills
+        for s in range(self.S):
+            k, v = initial_window(wl, s, fills[s])
+            self.orc.set_state(s, origins[s], fills[s], k[: self.Ls].double().numpy(),
+                               v[: self.Ls].double().numpy())
+        self.t = 0
+        self.scale = (wl.n_streams / self.S) * (wl.n_layers / self.Ls)
+
+    def step(self):
+        """Runs one sampled step; returns its time scaled to the whole workload."""
+        from rkv_inputs import step_inputs
+        self.t += 1
+        q, k, v = step_inputs(self.wl, self.t)
+        Ls, S = self.Ls, self.S
+        q = q[:Ls, :S].double().numpy()
+        k = k[:Ls, :S].double().numpy()
+        v = v[:Ls, :S].double().numpy()
+        t0 = time.perf_counter()
+        self.orc.append(k, v)
+        if self.stored:
+            self.orc.rebase()
+        self.orc.attend(q)
+        return (time.perf_counter() - t0) * self.scale
+
+    def sample_text(self):
+        return (f"{self.S} of {self.wl.n_streams} stream(s) x {self.Ls} of {self.wl.n_layers} "
+                f"layers per step (float64 numpy), time scaled x{self.scale:g}")
+
+
+def oracle_cores():
+    """Threads the oracle's numpy BLAS runs on (bounded by the usable cores)."""
+    cores = len(os.sched_getaffinity(0))
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        return min(cores, threads)
+    except ImportError:
+        return cores
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="qwen3b", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--attend-impl", default="auto", choices=["auto", "fma", "mma"])
+    ap.add_argument("--ring", type=int, default=64)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    wl, layout = _workload(args.workload)
+    peak, peak_kind = _peaks()
+    tokens_per_step = wl.n_streams * wl.n_new
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        runner = OracleRunner(args.workload)
+        for _ in range(args.warmup):
+            runner.step()
+        secs = [runner.step() for _ in range(args.steps)]
+        sec = sum(secs) / len(secs)
+        bps = _kv_bytes_per_step(wl, [min(wl.capacity, f + wl.n_new) for f in runner.fills])
+        val = bps / sec / 1e9
+        line = {
+            "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "us_per_step": sec * 1e6,
+            "tokens_per_s": tokens_per_step / sec, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}"},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": oracle_cores(),
+                             "kind": "oracle", "sample": runner.sample_text()},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", rank=rank, world_size=world)
+    res = run_gpu(args, rank, world)
+    ms_local = res["total_ms"] / res["steps"]
+    bytes_local = res["total_bytes"] / res["steps"]
+    att_ms = sum(res["attend_ms"]) / res["steps"]
+    e2e_ms_local = res["e2e"]["ms_per_step"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_local, e2e_ms_local, att_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms, att_ms = [float(x) for x in t.tolist()]
+        b = torch.tensor([bytes_local], device="cuda", dtype=torch.float64)
+        dist.all_reduce(b)
+        all_bytes = float(b.item())
+    else:
+        ms, e2e_ms, all_bytes = ms_local, e2e_ms_local, bytes_local
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    value = all_bytes / (ms * 1e-3) / 1e9
+    att_bytes = bytes_local
+    achieved = att_bytes / (att_ms * 1e-3) / 1e9
+    kernel_key = "attend_mma" if args.attend_impl != "fma" and wl.kv_dtype == "bf16" else \
+        "attend_fma"
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "us_per_step": ms * 1e3, "tokens_per_s": world * tokens_per_step / (ms * 1e-3),
+        "pct_of_hbm_peak": 100.0 * value / (peak * world),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
+                   "kv_bytes_per_step": int(bytes_local),
+                   "l2": "256 MiB buffer written between steps, outside the timed events",
+                   "attend_impl": args.attend_impl, "parallelism": f"replicas x{world}",
+                   "step": "append + rebase + attend (all layers)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
+                     "kernel": kernel_key, "traffic": _traffic(kernel_key),
+                     "attend_us": att_ms * 1e3,
+                     "append_us": 1e3 * sum(res["append_ms"]) / res["steps"]},
+        "e2e": {"value": all_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "us_per_step": e2e_ms * 1e3, "h2d_bytes_per_step": res["e2e"]["h2d"],
+                "d2h_bytes_per_step": res["e2e"]["d2h"]},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "wall_s_timed_region": res["wall_s"],
+    }
+    if not args.no_cpu_baseline:
+        runner = OracleRunner(args.workload)
+        runner.step()
+        secs, t0 = [], time.perf_counter()
+        while len(secs) < 200 and (len(secs) < 3 or time.perf_counter() - t0 < args.cpu_budget):
+            secs.append(runner.step())
+        sec = sum(secs) / len(secs)
+        cb = _kv_bytes_per_step(wl, [min(wl.capacity, f + wl.n_new) for f in runner.fills])
+        line["cpu_baseline"] = {
+            "value": cb / sec / 1e9, "unit": "GB/s", "cores": oracle_cores(), "kind": "oracle",
+            "sample": f"{len(secs)} steps of " + runner.sample_text(),
+            "ms_per_step": sec * 1e3}
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+/*
+ * rkv.h -- C ABI of the rolling KV cache with exact RoPE re-basing (B300, sm_103a).
+ *
+ * The operations follow "Audio8 ASR Infinite: What It Actually Takes to Listen
+ * Forever" (its flowchart and the section "Inside the Rolling KV Cache and Exact
+ * RoPE Re-Basing"): a fixed-capacity cache of key/value pairs per stream; when a
+ * new pair does not fit, the oldest pair is evicted, the sliding origin moves
+ * forward and every retained key and the query are placed at position
+ * (p - origin), which preserves every query-key distance exactly.  The rotary
+ * embedding uses theta = 1e6 ("Audio8-ASR-0.1B in audio.cpp", "Architecture")
+ * and split-half pairing ("Audio8-ASR-Infinite-mlx", "Requires a patched
+ * mlx-audio-swift"); the cache is stored in BF16
+ * ("Reza2kn/Audio8-ASR-Infinite-Compressed", "Linux CPU").
+ *
+ * Conventions (all entry points):
+ *  - Every buffer is caller-owned.  The library allocates no device memory;
+ *    buffers must stay valid until rkv_destroy.  Device pointers must be
+ *    16-byte aligned.
+ *  - Work is enqueued on the caller's CUDA stream (passed as an opaque
+ *    pointer, a cudaStream_t; NULL = legacy default stream).  Only
+ *    rkv_get_stream_state waits for the device.
+ *  - Argument errors are returned before anything is enqueued.  A failed
+ *    launch returns RKV_ERR_CUDA.  Inconsistencies that only the device can
+ *    see (a corrupt per-stream state, a query count larger than the window,
+ *    a stored-rotated cache used without its re-base) set a sticky per-stream
+ *    status word; kernels then skip that stream and rkv_get_stream_state
+ *    reports it.
+ *  - One handle is used from one CUDA stream at a time.  Calls on one handle
+ *    that overlap on the GPU race.
+ *
+ * Notation: S streams, L layers, H_q query heads, H_kv KV heads (G = H_q/H_kv
+ * query heads share one KV head: head h reads KV head floor(h/G)), D head_dim,
+ * W capacity (slots per stream, layer and KV head), c tokens per step.
+ * Per stream the state is (origin o, fill n): retained absolute positions are
+ * o .. o+n-1 and position p lives in slot p mod W.
+ */
+#ifndef RKV_H
+#define RKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RKV_ABI_VERSION 1
+
+typedef struct rkv_handle rkv_handle;  /* opaque, host memory owned by the library */
+
+typedef enum {
+  RKV_OK = 0,
+  RKV_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or config field */
+  RKV_ERR_UNSUPPORTED = 2,   /* valid but not built (e.g. head_dim 96)        */
+  RKV_ERR_CAPACITY = 3,      /* more new tokens in one step than the capacity  */
+  RKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed           */
+  RKV_ERR_DEVICE_STATE = 5   /* a stream's device status word is set           */
+} rkv_status;
+
+typedef enum { RKV_BF16 = 0, RKV_F32 = 1 } rkv_dtype;
+
+/* Key storage.  PRE_ROPE keeps keys unrotated and rotates them on the fly at
+ * (p - origin) inside the attention kernels, so re-basing moves no data.
+ * STORED_ROTATED keeps keys rotated at (p - origin) and re-rotates every
+ * retained key by R(-e) after e evictions (rkv_rebase) -- the variant whose
+ * repeated rounding "Audio8 ASR Infinite..." warns about in "Inside the
+ * Rolling KV Cache and Exact RoPE Re-Basing" and "Failure Modes That Only
+ * Appear on Day Three of a Session". */
+typedef enum { RKV_PRE_ROPE = 0, RKV_STORED_ROTATED = 1 } rkv_layout;
+
+/* Rotary pairing: split-half pairs element i with i + D/2 (rotate_half);
+ * interleaved pairs 2i with 2i+1.  Pair i turns by angle r * theta^(-2i/D). */
+typedef enum { RKV_ROPE_SPLIT_HALF = 0, RKV_ROPE_INTERLEAVED = 1 } rkv_rope_style;
+
+/* Attention kernel family: AUTO picks the tensor-core kernels for bf16
+ * caches and the CUDA-core kernel otherwise. */
+typedef enum { RKV_ATTEND_AUTO = 0, RKV_ATTEND_FMA = 1, RKV_ATTEND_MMA = 2 } rkv_attend_impl;
+
+typedef struct {
+  int32_t n_streams;     /* S, 1..1024                                    */
+  int32_t n_layers;      /* L, >= 1                                       */
+  int32_t n_q_heads;     /* H_q, multiple of n_kv_heads                   */
+  int32_t n_kv_heads;    /* H_kv, >= 1                                    */
+  int32_t head_dim;      /* D: 64 or 128                                  */
+  int32_t capacity;      /* W: multiple of 32, 32..65536                  */
+  int32_t max_chunk;     /* largest c passed to rkv_append / rkv_attend   */
+  int32_t kv_dtype;      /* rkv_dtype of the K/V pools and new K/V rows    */
+  int32_t q_dtype;       /* rkv_dtype of the queries                       */
+  int32_t layout;        /* rkv_layout                                     */
+  int32_t rope_style;    /* rkv_rope_style                                 */
+  int32_t attend_impl;   /* rkv_attend_impl                                */
+  double rope_theta;     /* > 1, e.g. 1e6                                  */
+  float softmax_scale;   /* 0 => 1/sqrt(D)                                 */
+  int32_t reserved;      /* must be 0                                      */
+} rkv_config;
+
+typedef struct {
+  void* k_pool;           /* device, [S][L][H_kv][W][D] of kv_dtype           */
+  void* v_pool;           /* device, same shape                               */
+  void* state;            /* device, state_bytes (per-stream origin/fill/...) */
+  void* workspace;        /* device, workspace_bytes (RoPE table, partials)   */
+  size_t workspace_bytes; /* size of workspace, >= rkv_required_bytes value   */
+} rkv_buffers;
+
+/* Sizes of the caller-owned buffers for cfg.  Host only; touches no GPU. */
+rkv_status rkv_required_bytes(const rkv_config* cfg, size_t* kv_pool_bytes_each,
+                              size_t* state_bytes, size_t* workspace_bytes);
+
+/* Validates cfg and bufs, builds the handle and enqueues the initialisation
+ * on `stream`: every stream's state becomes (origin 0, fill 0, status 0) and
+ * the float32 sin/cos table (computed in float64 on the host) is uploaded into
+ * the workspace.  Pool contents are not touched.  *out is set only on RKV_OK. */
+rkv_status rkv_create(const rkv_config* cfg, const rkv_buffers* bufs, void* stream,
+                      rkv_handle** out);
+
+/* Appends n_new (1..max_chunk, <= W) pairs to every stream.
+ * k_new, v_new: device, [L][S][n_new][H_kv][D] of kv_dtype.
+ * Per stream (the flowchart of "Audio8 ASR Infinite...": "evict oldest pair",
+ * "shift sliding origin forward"):
+ *   e = max(0, n + n_new - W); o' = o + e; n' = n + n_new - e;
+ *   new position o + n + j goes to slot (o + n + j) mod W in every layer and
+ *   KV head.  STORED_ROTATED stores bf16/f32(R(p - o') k).
+ * step_log: NULL or device int64 [S][4] receiving (o', n', e, first_slot).
+ * One kernel launch.  In STORED_ROTATED, call rkv_rebase before the next
+ * rkv_append or rkv_attend whenever this step evicted (the device flags a
+ * missing re-base as RKV_ERR_DEVICE_STATE for that stream). */
+rkv_status rkv_append(rkv_handle* h, const void* k_new, const void* v_new, int32_t n_new,
+                      int64_t* step_log, void* stream);
+
+/* Causal attention of the n_q newest tokens of every stream over its window,
+ * for layers layer_begin .. layer_begin+n_layers-1.
+ * q:   device, [n_layers][S][n_q][H_q][D] of q_dtype, before rotation.
+ * out: device float32, same shape.
+ * Query j sits at re-based position n' - n_q + j and sees keys r <= that
+ * position; key r = p - o' is rotated to r (on the fly in PRE_ROPE).
+ * out = sum_r softmax_r(<R(r_q) q, R(r) k_r> * scale) v_r, float32 math,
+ * split across CTAs and merged by log-sum-exp.  An empty window gives 0.
+ * n_q must not exceed the fill (device-checked). */
+rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_begin,
+                      int32_t n_layers, int32_t n_q, void* stream);
+
+/* Re-base.  PRE_ROPE: nothing moves (the origin update of rkv_append is the
+ * whole re-base) and nothing is launched.  STORED_ROTATED: one launch that
+ * re-rotates every retained key older than the last append by R(-e), e = the
+ * pairs that append evicted, in float32, rounded to nearest even. */
+rkv_status rkv_rebase(rkv_handle* h, void* stream);
+
+/* Frees the handle (host memory only). */
+rkv_status rkv_destroy(rkv_handle* h);
+
+/* Sets stream s to (origin, fill) and clears its status, enqueued on `stream`.
+ * The caller must already hold that window's pairs in slots (origin+i) mod W
+ * (keys rotated to i for STORED_ROTATED).  Used to seed workloads and to jump
+ * the origin on an utterance reset.  origin >= 0, 0 <= fill <= W. */
+rkv_status rkv_set_stream_state(rkv_handle* h, int32_t s, int64_t origin, int32_t fill,
+                                void* stream);
+
+/* Copies every stream's (origin, fill, status) to host arrays of length S
+ * (any may be NULL) and waits for `stream`.  For tests and diagnostics. */
+rkv_status rkv_get_stream_state(rkv_handle* h, int64_t* origins, int32_t* fills,
+                                int32_t* status, void* stream);
+
+/* Number of kernel launches the last rkv_append / rkv_attend / rkv_rebase call
+ * on this handle enqueued. */
+int32_t rkv_last_launch_count(const rkv_handle* h);
+
+/* Static description of a status code. */
+const char* rkv_status_string(rkv_status s);
+
+/* RKV_ABI_VERSION of the loaded library. */
+int32_t rkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RKV_H */

@@ -1,0 +1,224 @@
+// rkv_attend_common.cuh -- pieces shared by the attention kernels: the block
+// list of a call, the per-warp block sequence, and the log-sum-exp merge of
+// the partial results of one (stream, layer, KV head) unit.
+//
+// Work layout.  A unit's window is cut into aligned slot blocks of TK slots;
+// the units of all streams (stream-major, then layer, then KV head) are laid
+// end to end and each persistent CTA takes one contiguous, equal share of the
+// blocks.  Inside a CTA every unit segment is split into NWARP contiguous
+// chunks, one per warp; each warp streams its chunk through its own ring of
+// TMA stages and keeps an online-softmax state.  At the end of a segment the
+// warps merge through shared memory; a unit split across CTAs is finished by
+// the CTA that arrives last on the unit's ticket (no CTA waits on another).
+#pragma once
+
+#include "rkv_internal.h"
+
+namespace rkv {
+
+struct UnitRef {
+  int s, l, g;          // stream, layer (within the call), KV head
+  int nb;               // touched blocks per unit of this stream
+  int ustart, uend;     // [ustart, uend): this unit's blocks in the call's list
+  int a;                // origin mod W (slot of the oldest pair)
+  int fill;             // retained pairs
+};
+
+__device__ __forceinline__ int stream_blocks(const AttendParams& p, int s) {
+  const StreamState st = p.st[s];
+  if (!state_ok(st, p.sh.W)) return 0;
+  return touched_blocks(static_cast<int>(st.origin % p.sh.W), st.fill, p.sh.NB);
+}
+
+// pre[s] = first block of stream s in the call's list, pre[S] = total.  Warp 0
+// computes it; the caller synchronises the CTA afterwards.
+__device__ __forceinline__ void build_prefix(const AttendParams& p, int* pre) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const int per_unit = p.L_att * p.sh.Hkv;
+  int carry = 0;
+  if (lane == 0) pre[0] = 0;
+  for (int base = 0; base < p.sh.S; base += 32) {
+    const int s = base + lane;
+    int v = (s < p.sh.S) ? stream_blocks(p, s) * per_unit : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += t;
+    }
+    if (s < p.sh.S) pre[s + 1] = carry + v;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+}
+
+__device__ __forceinline__ UnitRef unit_of(int x, const AttendParams& p, const int* pre) {
+  int lo = 0, hi = p.sh.S;  // pre[lo] <= x < pre[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid;
+  }
+  UnitRef u;
+  u.s = lo;
+  const StreamState st = p.st[lo];
+  u.a = static_cast<int>(st.origin % p.sh.W);
+  u.fill = st.fill;
+  u.nb = touched_blocks(u.a, u.fill, p.sh.NB);
+  const int xs = x - pre[lo];
+  const int ul = xs / u.nb;
+  u.l = ul / p.sh.Hkv;
+  u.g = ul % p.sh.Hkv;
+  u.ustart = pre[lo] + ul * u.nb;
+  u.uend = u.ustart + u.nb;
+  return u;
+}
+
+// Block y of unit u: slot block index and re-based position of its first slot.
+struct BlockGeo {
+  int blk;   // slot block: slots blk*TK .. blk*TK+TK-1
+  int r0;    // (blk*TK - a) mod W; slot blk*TK+d has position r0+d, minus W if >= W
+};
+__device__ __forceinline__ BlockGeo block_geo(int y, const UnitRef& u, int W, int NB) {
+  BlockGeo b;
+  b.blk = touched_block(u.a, y - u.ustart, NB);
+  int r0 = b.blk * TK - u.a;
+  b.r0 = r0 < 0 ? r0 + W : r0;
+  return b;
+}
+
+// The blocks one warp handles, in order: for each unit segment of the CTA's
+// range, the warp's contiguous chunk of it.
+struct WarpSeq {
+  int x, re, w, y, ce;
+  UnitRef u;
+  __device__ __forceinline__ void init(int rb, int re_, int w_) {
+    x = rb; re = re_; w = w_; y = 0; ce = 0;
+  }
+  __device__ __forceinline__ bool next(const AttendParams& p, const int* pre, int& by,
+                                       UnitRef& ur) {
+    while (y >= ce) {
+      if (x >= re) return false;
+      u = unit_of(x, p, pre);
+      const int x1 = min(u.uend, re), n = x1 - x;
+      y = x + (w * n) / NWARP;
+      ce = x + ((w + 1) * n) / NWARP;
+      x = x1;
+    }
+    by = y++;
+    ur = u;
+    return true;
+  }
+};
+
+__device__ __forceinline__ size_t unit_index(const AttendParams& p, const UnitRef& u) {
+  return ((size_t)u.s * p.sh.L + p.layer_begin + u.l) * p.sh.Hkv + u.g;
+}
+// out / q offset of (unit u, query row `row` = j*G + hh).
+__device__ __forceinline__ size_t row_offset(const AttendParams& p, const UnitRef& u, int row) {
+  const int j = row / p.sh.G, hh = row % p.sh.G;
+  const int h = u.g * p.sh.G + hh;
+  return ((((size_t)u.l * p.sh.S + u.s) * p.c + j) * p.sh.Hq + h) * p.sh.D;
+}
+
+// Zero the outputs of units whose stream has an empty window (nothing to
+// attend to).  CTAs stride over the units.
+__device__ __forceinline__ void zero_empty_units(const AttendParams& p) {
+  const int per_stream = p.L_att * p.sh.Hkv;
+  const int units = p.sh.S * per_stream;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int s = u / per_stream;
+    const StreamState st = p.st[s];
+    if (!(state_ok(st, p.sh.W) && st.fill == 0)) continue;
+    UnitRef ur;
+    ur.s = s;
+    ur.l = (u % per_stream) / p.sh.Hkv;
+    ur.g = u % p.sh.Hkv;
+    for (int row = 0; row < p.R; ++row) {
+      float* o = p.out + row_offset(p, ur, row);
+      for (int d = threadIdx.x; d < p.sh.D; d += blockDim.x) o[d] = 0.f;
+    }
+  }
+}
+
+// Segment end.  `mrg` holds NWARP warp partials of `wstride` floats, each
+// [m(R) | l(R) | o(R*D)] with m in log2 units.  All CTA threads call this
+// right after a __syncthreads.  Writes the unit's output when the segment is
+// the whole unit; otherwise stores the CTA partial (slot 0 for the CTA's first
+// segment, slot 1 for its last), takes the unit's ticket and, if it is the
+// last CTA of the unit to arrive, merges every CTA partial of the unit.
+// T = blocks in the call's list, P = CTAs sharing them (every CTA below P has
+// at least one block); `flag` is one int of shared scratch.  The caller
+// synchronises the CTA before reusing `mrg` or `flag`.
+__device__ __forceinline__ void finish_segment(const AttendParams& p, const UnitRef& u, int x0,
+                                               int x1, int rb, int T, int P, const float* mrg,
+                                               int wstride, int* flag) {
+  const int R = p.R, D = p.sh.D;
+  const int nthr = blockDim.x;
+  const bool whole = (x0 == u.ustart) && (x1 == u.uend);
+  float* part = nullptr;
+  if (!whole) {
+    const int kslot = (x0 == rb) ? 0 : 1;
+    part = p.partials + (size_t)(2 * blockIdx.x + kslot) * p.slot_floats;
+  }
+  for (int idx = threadIdx.x; idx < R * D; idx += nthr) {
+    const int row = idx / D, d = idx % D;
+    float M = NEG_BIG;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) M = fmaxf(M, mrg[w * wstride + row]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) {
+      const float sc = exp2f(mrg[w * wstride + row] - M);
+      den += sc * mrg[w * wstride + R + row];
+      num += sc * mrg[w * wstride + 2 * R + row * D + d];
+    }
+    if (whole) {
+      p.out[row_offset(p, u, row) + d] = den > 0.f ? num / den : 0.f;
+    } else {
+      if (d == 0) { part[row] = M; part[R + row] = den; }
+      part[2 * R + row * D + d] = num;
+    }
+  }
+  if (whole) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    *flag = atomicAdd(&p.unit_tickets[unit_index(p, u)], 1);
+  }
+  __syncthreads();
+  const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
+  if (*flag != b1 - b0) return;  // another CTA finishes this unit
+  __threadfence();
+  const int rs0 = range_start(b0, T, P);
+  for (int idx = threadIdx.x; idx < R * D; idx += nthr) {
+    const int row = idx / D, d = idx % D;
+    float M = NEG_BIG;
+    for (int b = b0; b <= b1; ++b) {
+      const int k = (b == b0 && rs0 < u.ustart) ? 1 : 0;
+      const float* pp = p.partials + (size_t)(2 * b + k) * p.slot_floats;
+      M = fmaxf(M, __ldcg(pp + row));
+    }
+    float num = 0.f, den = 0.f;
+    for (int b = b0; b <= b1; ++b) {
+      const int k = (b == b0 && rs0 < u.ustart) ? 1 : 0;
+      const float* pp = p.partials + (size_t)(2 * b + k) * p.slot_floats;
+      const float sc = exp2f(__ldcg(pp + row) - M);
+      den += sc * __ldcg(pp + R + row);
+      num += sc * __ldcg(pp + 2 * R + row * D + d);
+    }
+    p.out[row_offset(p, u, row) + d] = den > 0.f ? num / den : 0.f;
+  }
+  if (threadIdx.x == 0) p.unit_tickets[unit_index(p, u)] = 0;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace rkv

@@ -1,0 +1,88 @@
+// rkv_internal.h -- kernel parameter blocks and launchers shared by the host
+// API (rkv_api.cu) and the kernel files.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "rkv_device.cuh"
+
+namespace rkv {
+
+// Geometry every kernel needs.
+struct Shape {
+  int S, L, Hq, Hkv, G, D, W, NB;  // NB = W / TK
+  int bf16;                        // K/V pools hold bf16 (else f32)
+  int q_bf16;                      // queries are bf16 (else f32)
+  int style;                       // 0 split-half, 1 interleaved
+  int stored_rotated;              // 1: keys kept rotated to (p - origin)
+};
+
+// Workspace carve-up (byte offsets from the workspace base).
+struct WsLayout {
+  size_t table_off;        // float2 [2W][D/2]: (cos, sin)(m * w_i), m in [0, 2W)
+  size_t append_tk_off;    // int [S]  last-block tickets of the append kernel
+  size_t rerot_tk_off;     // int [S]  last-block tickets of the re-rotation kernel
+  size_t unit_tk_off;      // int [S*L*H_kv] tickets of split units (attention merge)
+  size_t part_off;         // float [2 * max_ctas][slot_floats] split partials
+  size_t total;
+  int rmax;                // rows per unit a partial can hold (max_chunk * G)
+  int slot_floats;         // rmax * (D + 2), rounded up to 4
+  int max_ctas;
+};
+
+struct AppendParams {
+  Shape sh;
+  StreamState* st;
+  const void* k_new;
+  const void* v_new;
+  void* k_pool;
+  void* v_pool;
+  long long* log;          // nullable, [S][4]
+  int* tickets;            // [S]
+  const float2* table;
+  int c;                   // pairs appended this step
+  int rows_per_block;
+};
+
+struct RerotParams {
+  Shape sh;
+  StreamState* st;
+  void* k_pool;
+  int* tickets;
+  const float2* table;
+  int rows_per_block;
+};
+
+struct AttendParams {
+  Shape sh;
+  StreamState* st;
+  const void* q;
+  float* out;
+  const float2* table;
+  float* partials;
+  int* unit_tickets;
+  int layer_begin, L_att, c;  // layers of this call, queries per stream
+  int R;                      // rows per unit = c * G
+  int slot_floats;
+  float scale_log2;           // softmax scale * log2(e)
+};
+
+cudaError_t launch_append(const AppendParams& p, int blocks_per_stream, cudaStream_t s);
+cudaError_t launch_rerotate(const RerotParams& p, int blocks_per_stream, cudaStream_t s);
+cudaError_t launch_set_state(StreamState* st, int s_idx, long long origin, int fill,
+                             cudaStream_t s);
+
+// Attention launchers; `grid` = persistent CTAs.  Return cudaErrorNotSupported
+// when the shape has no instantiation.
+cudaError_t launch_attend_fma(const AttendParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                              int grid, cudaStream_t s);
+cudaError_t launch_attend_mma(const AttendParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                              int grid, cudaStream_t s);
+bool attend_mma_supported(const Shape& sh, int c);
+size_t attend_fma_smem(const Shape& sh, int R);
+size_t attend_mma_smem(const Shape& sh, int c);
+
+}  // namespace rkv

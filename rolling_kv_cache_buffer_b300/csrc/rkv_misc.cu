@@ -1,0 +1,225 @@
+// rkv_misc.cu -- bookkeeping + append (K0/K1), stored-rotated re-rotation (K4)
+// and the stream-state setter.
+//
+// Bookkeeping follows the flowchart of "Audio8 ASR Infinite: What It Actually
+// Takes to Listen Forever": a pair that does not fit makes the cache evict the
+// oldest pair and shift the sliding origin forward.  Every block of a stream
+// reads the old state, derives the same new state from it, scatters its rows,
+// and the last block of the stream to finish (atomic ticket) publishes the new
+// state; no block waits on another.
+#include "rkv_internal.h"
+
+namespace rkv {
+
+namespace {
+
+// Four consecutive elements of a row, widened to f32.
+__device__ __forceinline__ void load4(const void* base, size_t i, bool bf16, float (&x)[4]) {
+  if (bf16) {
+    uint2 w = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + i);
+    x[0] = bf_lo(w.x); x[1] = bf_hi(w.x); x[2] = bf_lo(w.y); x[3] = bf_hi(w.y);
+  } else {
+    float4 w = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + i);
+    x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+  }
+}
+__device__ __forceinline__ void store4(void* base, size_t i, bool bf16, const float (&x)[4]) {
+  if (bf16) {
+    uint2 w = make_uint2(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]));
+    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(base) + i) = w;
+  } else {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + i) =
+        make_float4(x[0], x[1], x[2], x[3]);
+  }
+}
+
+// Rotates the 4 pairs held in (a, b) by the table entries cs[0..3]; `sgn` = +1
+// rotates by +angle, -1 by -angle.  Pair (x, y) -> (x cos - y sin, y cos + x sin).
+__device__ __forceinline__ void rotate4(float (&a)[4], float (&b)[4], const float2 (&cs)[4],
+                                        float sgn) {
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    float c = cs[t].x, s = sgn * cs[t].y;
+    float x = a[t], y = b[t];
+    a[t] = x * c - y * s;
+    b[t] = y * c + x * s;
+  }
+}
+
+// Loads the two element groups of 4 pairs starting at pair i.  Split-half:
+// a = dims i..i+3, b = dims i+D/2..i+D/2+3.  Interleaved: a = dims 2i,2i+2,..,
+// b = dims 2i+1,2i+3,.. (8 consecutive elements).
+__device__ __forceinline__ void load_pairs(const void* base, size_t row, int i, int D, int style,
+                                           bool bf16, float (&a)[4], float (&b)[4]) {
+  if (style == 0) {
+    load4(base, row + i, bf16, a);
+    load4(base, row + i + D / 2, bf16, b);
+  } else {
+    float x[4], y[4];
+    load4(base, row + 2 * i, bf16, x);
+    load4(base, row + 2 * i + 4, bf16, y);
+    a[0] = x[0]; b[0] = x[1]; a[1] = x[2]; b[1] = x[3];
+    a[2] = y[0]; b[2] = y[1]; a[3] = y[2]; b[3] = y[3];
+  }
+}
+__device__ __forceinline__ void store_pairs(void* base, size_t row, int i, int D, int style,
+                                            bool bf16, const float (&a)[4], const float (&b)[4]) {
+  if (style == 0) {
+    store4(base, row + i, bf16, a);
+    store4(base, row + i + D / 2, bf16, b);
+  } else {
+    float x[4] = {a[0], b[0], a[1], b[1]};
+    float y[4] = {a[2], b[2], a[3], b[3]};
+    store4(base, row + 2 * i, bf16, x);
+    store4(base, row + 2 * i + 4, bf16, y);
+  }
+}
+
+__device__ __forceinline__ void load_cs4(const float2* table, size_t row_off, int i,
+                                         float2 (&cs)[4]) {
+  const float4* p = reinterpret_cast<const float4*>(table + row_off + i);
+  float4 u = __ldg(p), v = __ldg(p + 1);
+  cs[0] = make_float2(u.x, u.y); cs[1] = make_float2(u.z, u.w);
+  cs[2] = make_float2(v.x, v.y); cs[3] = make_float2(v.z, v.w);
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+// K0 + K1: bookkeeping and scatter of the new rows.  grid = (blocks_per_stream, S)
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+  const Shape& sh = p.sh;
+  const int s = blockIdx.y;
+  const StreamState st = p.st[s];
+  const int c = p.c, W = sh.W, D = sh.D, Hkv = sh.Hkv;
+  const bool ok = state_ok(st, W) && c >= 1 && c <= W &&
+                  !(sh.stored_rotated && st.pending != 0);
+  const int e = max(0, st.fill + c - W);
+  const long long o2 = st.origin + e;
+  const int n2 = st.fill + c - e;
+  const long long first = st.origin + st.fill;
+
+  if (ok) {
+    const int total = sh.L * c * Hkv;                 // rows (l, j, g)
+    const int r0 = blockIdx.x * p.rows_per_block;
+    const int r1 = min(total, r0 + p.rows_per_block);
+    const int quads = D / 8;                          // 4 pairs per thread
+    const bool bf = sh.bf16 != 0;
+    for (int idx = threadIdx.x; idx < (r1 - r0) * quads; idx += blockDim.x) {
+      const int row = r0 + idx / quads;
+      const int i = (idx % quads) * 4;
+      const int g = row % Hkv;
+      const int j = (row / Hkv) % c;
+      const int l = row / (Hkv * c);
+      const long long pos = first + j;
+      const int slot = static_cast<int>(pos % W);
+      const size_t src = ((((size_t)l * sh.S + s) * c + j) * Hkv + g) * D;
+      const size_t dst = ((((size_t)s * sh.L + l) * Hkv + g) * W + slot) * D;
+      float ka[4], kb[4], va[4], vb[4];
+      load_pairs(p.k_new, src, i, D, sh.style, bf, ka, kb);
+      load_pairs(p.v_new, src, i, D, sh.style, bf, va, vb);
+      if (sh.stored_rotated) {  // store R(pos - origin') k
+        float2 cs[4];
+        load_cs4(p.table, (size_t)(pos - o2) * (D / 2), i, cs);
+        rotate4(ka, kb, cs, 1.f);
+      }
+      store_pairs(p.k_pool, dst, i, D, sh.style, bf, ka, kb);
+      store_pairs(p.v_pool, dst, i, D, sh.style, bf, va, vb);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int old = atomicAdd(&p.tickets[s], 1);
+    if (old == static_cast<int>(gridDim.x) - 1) {
+      __threadfence();
+      StreamState ns = st;
+      if (ok) {
+        ns.origin = o2;
+        ns.fill = n2;
+        ns.pending = sh.stored_rotated ? e : 0;
+        ns.last_new = c;
+      } else if (ns.status == 0) {
+        ns.status = STATUS_DEVICE_STATE;
+      }
+      p.st[s] = ns;
+      if (p.log) {
+        long long* lg = p.log + 4 * (size_t)s;
+        lg[0] = ok ? o2 : st.origin;
+        lg[1] = ok ? n2 : st.fill;
+        lg[2] = ok ? e : -1;
+        lg[3] = ok ? first % W : -1;
+      }
+      p.tickets[s] = 0;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// K4: stored-rotated re-base.  Every retained key older than the last append is
+// turned by R(-e), e = pairs that append evicted, in f32 and rounded back to
+// the storage type.  grid = (blocks_per_stream, S).
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) rerotate_kernel(const RerotParams p) {
+  const Shape& sh = p.sh;
+  const int s = blockIdx.y;
+  const StreamState st = p.st[s];
+  const int W = sh.W, D = sh.D, Hkv = sh.Hkv;
+  const bool work = sh.stored_rotated && state_ok(st, W) && st.pending > 0;
+  if (work) {
+    const int nr = st.fill - st.last_new;               // keys that predate the append
+    const int total = sh.L * Hkv * max(nr, 0);
+    const int r0 = blockIdx.x * p.rows_per_block;
+    const int r1 = min(total, r0 + p.rows_per_block);
+    const int quads = D / 8;
+    const bool bf = sh.bf16 != 0;
+    const size_t trow = (size_t)st.pending * (D / 2);
+    for (int idx = threadIdx.x; idx < (r1 - r0) * quads; idx += blockDim.x) {
+      const int row = r0 + idx / quads;
+      const int i = (idx % quads) * 4;
+      const int r = row % nr;
+      const int lg = row / nr;                          // l * Hkv + g
+      const int slot = static_cast<int>((st.origin + r) % W);
+      const size_t base = (((size_t)s * sh.L * Hkv + lg) * W + slot) * D;
+      float a[4], b[4];
+      float2 cs[4];
+      load_pairs(p.k_pool, base, i, D, sh.style, bf, a, b);
+      load_cs4(p.table, trow, i, cs);
+      rotate4(a, b, cs, -1.f);
+      store_pairs(p.k_pool, base, i, D, sh.style, bf, a, b);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int old = atomicAdd(&p.tickets[s], 1);
+    if (old == static_cast<int>(gridDim.x) - 1) {
+      if (work) p.st[s].pending = 0;
+      p.tickets[s] = 0;
+    }
+  }
+}
+
+__global__ void set_state_kernel(StreamState* st, int s, long long origin, int fill) {
+  StreamState ns{};
+  ns.origin = origin;
+  ns.fill = fill;
+  st[s] = ns;
+}
+
+cudaError_t launch_append(const AppendParams& p, int blocks_per_stream, cudaStream_t s) {
+  append_kernel<<<dim3(blocks_per_stream, p.sh.S), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_rerotate(const RerotParams& p, int blocks_per_stream, cudaStream_t s) {
+  rerotate_kernel<<<dim3(blocks_per_stream, p.sh.S), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_set_state(StreamState* st, int s_idx, long long origin, int fill,
+                             cudaStream_t s) {
+  set_state_kernel<<<1, 1, 0, s>>>(st, s_idx, origin, fill);
+  return cudaGetLastError();
+}
+
+}  // namespace rkv
