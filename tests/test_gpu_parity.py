@@ -181,8 +181,11 @@ def test_evicted_slots_never_read(impl):
 @pytest.mark.parametrize("impl", IMPLS)
 def test_origin_shift_invariance(impl):
     """The same window contents at origins 0, 12345, 999999 and 10^12 give the
-    same outputs: bitwise when the origins agree modulo W (same slots), within
-    1e-5 otherwise (different slot blocks change only the summation order)."""
+    same outputs: bitwise when the origins agree modulo W (same slots).
+    Otherwise the slot blocks differ, which changes the summation order (the
+    f32 CUDA-core path stays within 1e-5) and, on the tensor-core path, which
+    rotation goes into the bf16 query operand and which into the bf16 key
+    operand (within 4e-3, inside the oracle tolerance)."""
     wl = WORKLOADS["qwen3b"].replace(n_layers=2, capacity=512)
     k = random_rows((2, 2, 400, 128), 11, torch.bfloat16)
     v = random_rows((2, 2, 400, 128), 12, torch.bfloat16)
@@ -193,8 +196,9 @@ def test_origin_shift_invariance(impl):
         write_window(cache, 0, origin, 400, k, v)
         outs[origin] = cache.attend(q).cpu()
     assert torch.equal(outs[0], outs[512 * 7])
+    tol = 1e-5 if impl == "fma" else 4e-3
     for origin in (12345, 999_999, 10 ** 12):
-        assert (outs[origin] - outs[0]).abs().max() < 1e-5
+        assert (outs[origin] - outs[0]).abs().max() < tol
 
 
 def test_empty_window_gives_zero():
