@@ -145,6 +145,32 @@ rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_be
  * pairs that append evicted, in float32, rounded to nearest even. */
 rkv_status rkv_rebase(rkv_handle* h, void* stream);
 
+/* Size of the library-owned scratch array used by rkv_attend_static_scratch. */
+#define RKV_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+/* rkv_attend without caller-provided scratch.  (The pages have no counterpart:
+ * this is a deployment convenience, not part of the method.)
+ * Same arguments, layouts and result as rkv_attend, on the handle's pools,
+ * state and RoPE table.  The scratch that rkv_attend keeps in the workspace --
+ * split-softmax partials and merge tickets -- lives instead in one static
+ * device array of RKV_STATIC_SCRATCH_BYTES that every GPU loading the library
+ * holds until the process exits, so the call allocates nothing and writes
+ * nothing to the workspace.  Meant for callers that cannot allocate device
+ * memory where they attend (a host framework's fixed memory pool, a plugin
+ * execute callback that forbids allocation, a real-time loop that must not
+ * risk the device synchronisation of cudaMalloc).
+ * Limits: S * L * H_kv <= 16384 and 2 * #SMs * max_chunk * G * (D + 2) * 4
+ * bytes <= RKV_STATIC_SCRATCH_BYTES - 64 KiB; larger calls return
+ * RKV_ERR_UNSUPPORTED before touching the GPU.
+ * The first call on each device takes the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  Each call enqueues a clear of the tickets and one
+ * kernel on `stream`.  All calls, from any handle, share the one array, which
+ * keeps the last call's contents: calls that overlap on the GPU race. */
+rkv_status rkv_attend_static_scratch(rkv_handle* h, const void* q, float* out,
+                                     int32_t layer_begin, int32_t n_layers, int32_t n_q,
+                                     void* stream);
+
 /* Frees the handle (host memory only). */
 rkv_status rkv_destroy(rkv_handle* h);
 

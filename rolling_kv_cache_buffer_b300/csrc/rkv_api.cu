@@ -8,30 +8,14 @@
 #include <new>
 #include <vector>
 
-#include "rkv.h"
-#include "rkv_internal.h"
+#include "rkv_handle.h"
 
 using rkv::Shape;
 using rkv::WsLayout;
 
-struct rkv_handle {
-  rkv_config cfg;
-  Shape sh;
-  WsLayout ws;
-  void* k_pool;
-  void* v_pool;
-  rkv::StreamState* state;
-  uint8_t* workspace;
-  CUtensorMap tmK, tmV;
-  int num_sms;
-  int last_launches;
-  float scale;
-  std::vector<float2> host_table;  // kept alive until destroy
-};
-
 namespace {
 
-constexpr int kMaxCtas = 1024;
+using rkv::kMaxCtas;
 constexpr int kMaxStreams = 1024;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -64,6 +64,7 @@ def load_library():
         "rkv_create": (c_int32, [POINTER(rkv_config), POINTER(rkv_buffers), P, POINTER(P)]),
         "rkv_append": (c_int32, [P, P, P, c_int32, P, P]),
         "rkv_attend": (c_int32, [P, P, P, c_int32, c_int32, c_int32, P]),
+        "rkv_attend_static_scratch": (c_int32, [P, P, P, c_int32, c_int32, c_int32, P]),
         "rkv_rebase": (c_int32, [P, P]),
         "rkv_destroy": (c_int32, [P]),
         "rkv_set_stream_state": (c_int32, [P, c_int32, c_int64, c_int32, P]),
@@ -116,6 +117,13 @@ def rkv_append(h, k_new, v_new, n_new, step_log, stream):
 def rkv_attend(h, q, out, layer_begin, n_layers, n_q, stream):
     _check(load_library().rkv_attend(h, q, out, layer_begin, n_layers, n_q, stream),
            "rkv_attend")
+
+
+def rkv_attend_static_scratch(h, q, out, layer_begin, n_layers, n_q, stream):
+    """rkv_attend with its scratch in the library's static device array (for
+    callers that cannot allocate device memory where they attend)."""
+    _check(load_library().rkv_attend_static_scratch(h, q, out, layer_begin, n_layers, n_q,
+                                                    stream), "rkv_attend_static_scratch")
 
 
 def rkv_rebase(h, stream):
