@@ -10,10 +10,13 @@ pair evicted per step), as BASELINE's metric is quoted on.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...      # the float64 CPU oracle
 
-Timing: K steps bracketed by a barrier + synchronize; each step's kernels are
-timed with CUDA events on the launching stream, and a 256 MiB buffer is
-written between steps (outside the events) so every step starts with a cold
-L2.  ``value`` = K/V bytes read per step / event time per step (whole job:
+Timing: K steps bracketed by a barrier + synchronize; each whole step is timed
+with CUDA events on the launching stream.  Between steps, outside the events,
+a 256 MiB buffer is written and another 256 MiB read, so every step starts on
+a cold L2 that holds no dirty lines, and a short GPU spin gives the host time
+to enqueue the whole step, so host launch latency never shows up between the
+events.  The append/attend split is timed on extra steps with an event
+between the two kernels.  ``value`` = K/V bytes read per step / event time per step (whole job:
 all ranks' bytes over the slowest rank).  Prints one JSON line (rank 0).
 """
 from __future__ import annotations
@@ -33,6 +36,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "rolling-KV decode attention µs/step & achieved HBM GB/s (% of B300 peak)"
 L2_FLUSH_BYTES = 256 << 20
+HOST_SLACK_CYCLES = 400_000      # GPU spin (~0.2 ms) ahead of each timed step
 
 WORKLOAD_TEXT = {
     "qwen3b": "36 layers, GQA 16 query / 2 KV heads, head_dim 128, bf16 K/V, window 4096, "
@@ -178,53 +182,76 @@ def run_gpu(args, rank, world):
         ring.append((q.to(dt).to(dev), k.to(dt).to(dev), v.to(dt).to(dev)))
     out = torch.empty(ring[0][0].shape, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    drain = torch.zeros(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i, ev=None):
+    def cold():
+        """Between steps, outside the events: a GPU spin (the host enqueues the
+        step meanwhile), 256 MiB written (no line of the step's data stays in
+        L2), then another 256 MiB read (the written lines are drained, so the
+        step starts on a cold, clean L2)."""
+        torch.cuda._sleep(HOST_SLACK_CYCLES)
+        flush.zero_()
+        torch.amax(drain)
+
+    def step(i, ev=None, split=False):
         q, k, v = ring[i % len(ring)]
         if ev:
             ev[0].record(stream)
         cache.append(k, v)
         cache.rebase()
-        if ev:
+        if ev and split:
             ev[1].record(stream)
         cache.attend(q, out)
         if ev:
             ev[2].record(stream)
 
+    n_done = 0
     for i in range(args.warmup):
-        flush.zero_()
-        step(i)
+        cold()
+        step(n_done)
+        n_done += 1
     torch.cuda.synchronize(dev)
     launches_per_step = 2 + (1 if layout == "stored_rotated" else 0)
 
+    # Timed region: exactly `steps` whole steps, one event pair around each.
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize(dev)
+    fl = list(fills)
+    for _ in range(n_done):
+        fl = [min(wl.capacity, f + c) for f in fl]
+    bytes_per_step = []
     with ClockSampler(dev.index) as clk:
         t0 = time.perf_counter()
         for i in range(args.steps):
-            flush.zero_()                      # cold L2 for every step (outside the events)
-            step(args.warmup + i, evs[i])
+            cold()
+            step(n_done, evs[i])
+            n_done += 1
+            fl = [min(wl.capacity, f + c) for f in fl]   # each step attends over fill'
+            bytes_per_step.append(_kv_bytes_per_step(wl, fl))
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
     if world > 1:
         dist.barrier()
     step_ms = [e[0].elapsed_time(e[2]) for e in evs]
-    attend_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    append_ms = [e[0].elapsed_time(e[1]) for e in evs]
 
-    # Each step attends over the post-append window: fill' = min(W, fill + c).
-    fl = list(fills)
-    for _ in range(args.warmup):
+    # Kernel split (outside the timed region): an event between append and
+    # attend, which also keeps the attention from overlapping the append.
+    nsplit = min(args.steps, 50)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nsplit)]
+    split_bytes = []
+    for i in range(nsplit):
+        cold()
+        step(n_done, sev[i], split=True)
+        n_done += 1
         fl = [min(wl.capacity, f + c) for f in fl]
-    bytes_per_step = []
-    for i in range(args.steps):
-        fl = [min(wl.capacity, f + c) for f in fl]
-        bytes_per_step.append(_kv_bytes_per_step(wl, fl))
-    # the e2e loop continues from here
+        split_bytes.append(_kv_bytes_per_step(wl, fl))
+    torch.cuda.synchronize(dev)
+    attend_ms = [e[1].elapsed_time(e[2]) for e in sev]
+    append_ms = [e[0].elapsed_time(e[1]) for e in sev]
     res_fills = fl
     total_bytes = sum(bytes_per_step)
     total_ms = sum(step_ms)
@@ -236,6 +263,7 @@ def run_gpu(args, rank, world):
 
     res = dict(total_bytes=total_bytes, total_ms=total_ms, steps=args.steps,
                step_ms=step_ms, attend_ms=attend_ms, append_ms=append_ms, wall_s=wall,
+               split_bytes=split_bytes,
                clocks=clk.summary(), launches=launches_per_step * args.steps,
                bytes_per_step=bytes_per_step, e2e=e2e, fills=res_fills)
     return res
@@ -397,7 +425,8 @@ def main():
     res = run_gpu(args, rank, world)
     ms_local = res["total_ms"] / res["steps"]
     bytes_local = res["total_bytes"] / res["steps"]
-    att_ms = sum(res["attend_ms"]) / res["steps"]
+    att_ms = sum(res["attend_ms"]) / len(res["attend_ms"])
+    att_bytes = sum(res["split_bytes"]) / len(res["split_bytes"])
     e2e_ms_local = res["e2e"]["ms_per_step"]
     if world > 1:
         import torch.distributed as dist
@@ -415,7 +444,6 @@ def main():
         return
 
     value = all_bytes / (ms * 1e-3) / 1e9
-    att_bytes = bytes_local
     achieved = att_bytes / (att_ms * 1e-3) / 1e9
     kernel_key = "attend_mma" if args.attend_impl != "fma" and wl.kv_dtype == "bf16" else \
         "attend_fma"
@@ -428,14 +456,17 @@ def main():
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
                    "kv_bytes_per_step": int(bytes_local),
-                   "l2": "256 MiB buffer written between steps, outside the timed events",
+                   "l2": "between steps, outside the timed events: 256 MiB written, then "
+                         "another 256 MiB read (cold L2, no dirty lines)",
                    "attend_impl": args.attend_impl, "parallelism": f"replicas x{world}",
                    "step": "append + rebase + attend (all layers)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "kernel": kernel_key, "traffic": _traffic(kernel_key),
                      "attend_us": att_ms * 1e3,
-                     "append_us": 1e3 * sum(res["append_ms"]) / res["steps"]},
+                     "append_us": 1e3 * sum(res["append_ms"]) / len(res["append_ms"]),
+                     "timing": "attend and append timed apart on extra steps (an event "
+                               "between them)"},
         "e2e": {"value": all_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "us_per_step": e2e_ms * 1e3, "h2d_bytes_per_step": res["e2e"]["h2d"],
                 "d2h_bytes_per_step": res["e2e"]["d2h"]},

@@ -115,6 +115,24 @@ bool make_pool_map(CUtensorMap* tm, void* pool, const Shape& s) {
   return r == CUDA_SUCCESS;
 }
 
+// 4-D view of a bf16 pool for whole-tile boxes: dims {64 elements, W rows,
+// D/64 row halves, units} with strides {2D bytes, 128 bytes, 2WD bytes}; a box
+// {64, TK, D/64, 1} (the keys of one block) lands in shared memory as D/64
+// pieces of TK rows x 128 bytes one after the other.
+bool make_pool_map4(CUtensorMap* tm, void* pool, const Shape& s) {
+  auto enc = get_encode();
+  if (!enc || !s.bf16) return false;
+  const int nbox = s.D / 64;
+  cuuint64_t dims[4] = {64, (cuuint64_t)s.W, (cuuint64_t)nbox, (cuuint64_t)s.S * s.L * s.Hkv};
+  cuuint64_t strides[3] = {(cuuint64_t)s.D * 2, 128, (cuuint64_t)s.W * s.D * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)rkv::TK, (cuuint32_t)nbox, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pool, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // (cos, sin)(m * w_i), w_i = theta^(-2i/D), for m in [0, 2W): computed in
 // float64 and rounded to float32.
 std::vector<float2> make_table(const Shape& s, double theta) {
@@ -131,9 +149,8 @@ std::vector<float2> make_table(const Shape& s, double theta) {
 }
 
 bool use_mma(const rkv_handle* h, int c) {
-  if (h->cfg.attend_impl == RKV_ATTEND_FMA) return false;
-  const bool ok = rkv::attend_mma_supported(h->sh, c);
-  return ok;
+  if (h->cfg.attend_impl == RKV_ATTEND_FMA || !h->has_map4) return false;
+  return rkv::attend_mma_supported(h->sh, c);
 }
 
 }  // namespace
@@ -201,6 +218,12 @@ rkv_status rkv_create(const rkv_config* cfg, const rkv_buffers* bufs, void* stre
     delete h;
     return RKV_ERR_CUDA;
   }
+  h->has_map4 = h->sh.bf16 && make_pool_map4(&h->tmK4, h->k_pool, h->sh) &&
+                make_pool_map4(&h->tmV4, h->v_pool, h->sh);
+  if (cfg->attend_impl == RKV_ATTEND_MMA && !h->has_map4) {
+    delete h;
+    return RKV_ERR_UNSUPPORTED;
+  }
   h->host_table = make_table(h->sh, cfg->rope_theta);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(h->state, 0, (size_t)h->sh.S * sizeof(rkv::StreamState), s);
@@ -238,14 +261,12 @@ rkv_status rkv_append(rkv_handle* h, const void* k_new, const void* v_new, int32
   p.k_pool = h->k_pool;
   p.v_pool = h->v_pool;
   p.log = reinterpret_cast<long long*>(step_log);
-  p.tickets = reinterpret_cast<int*>(h->workspace + h->ws.append_tk_off);
   p.table = reinterpret_cast<const float2*>(h->workspace + h->ws.table_off);
   p.c = n_new;
-  p.rows_per_block = 256 / (h->sh.D / 8);
-  const int rows = h->sh.L * n_new * h->sh.Hkv;
-  const int bps = (rows + p.rows_per_block - 1) / p.rows_per_block;
+  p.div_hkv = rkv::FastDiv::make(static_cast<uint32_t>(h->sh.Hkv));
+  p.div_c = rkv::FastDiv::make(static_cast<uint32_t>(n_new));
   h->last_launches = 1;
-  return cuda_status(rkv::launch_append(p, bps, static_cast<cudaStream_t>(stream)));
+  return cuda_status(rkv::launch_append(p, static_cast<cudaStream_t>(stream)));
 }
 
 rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_begin,
@@ -270,11 +291,11 @@ rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_be
   p.R = n_q * h->sh.G;
   p.slot_floats = h->ws.slot_floats;
   p.scale_log2 = h->scale * 1.4426950408889634f;
-  const int grid = h->num_sms < kMaxCtas ? h->num_sms : kMaxCtas;
+  const int grid = rkv::attend_grid(h, n_layers);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (use_mma(h, n_q)) {
-    e = rkv::launch_attend_mma(p, h->tmK, h->tmV, grid, s);
+    e = rkv::launch_attend_mma(p, h->tmK4, h->tmV4, grid, s);
   } else {
     if (h->cfg.attend_impl == RKV_ATTEND_MMA) return RKV_ERR_UNSUPPORTED;
     if (p.R > 16) return RKV_ERR_UNSUPPORTED;

@@ -30,11 +30,10 @@ __device__ __forceinline__ int stream_blocks(const AttendParams& p, int s) {
   return touched_blocks(static_cast<int>(st.origin % p.sh.W), st.fill, p.sh.NB);
 }
 
-// pre[s] = first block of stream s in the call's list, pre[S] = total.  Warp 0
-// computes it; the caller synchronises the CTA afterwards.
-__device__ __forceinline__ void build_prefix(const AttendParams& p, int* pre) {
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
+// pre[s] = first block of stream s in the call's list, pre[S] = total.  One
+// warp computes it (lane = its lane index); the caller synchronises the CTA
+// afterwards.
+__device__ __forceinline__ void build_prefix_warp(const AttendParams& p, int* pre, int lane) {
   const int per_unit = p.L_att * p.sh.Hkv;
   int carry = 0;
   if (lane == 0) pre[0] = 0;
@@ -49,6 +48,10 @@ __device__ __forceinline__ void build_prefix(const AttendParams& p, int* pre) {
     if (s < p.sh.S) pre[s + 1] = carry + v;
     carry += __shfl_sync(0xffffffffu, v, 31);
   }
+}
+// Warp 0 of the CTA builds the prefix.
+__device__ __forceinline__ void build_prefix(const AttendParams& p, int* pre) {
+  if (threadIdx.x < 32) build_prefix_warp(p, pre, threadIdx.x);
 }
 
 __device__ __forceinline__ UnitRef unit_of(int x, const AttendParams& p, const int* pre) {
@@ -120,8 +123,9 @@ __device__ __forceinline__ size_t row_offset(const AttendParams& p, const UnitRe
 }
 
 // Zero the outputs of units whose stream has an empty window (nothing to
-// attend to).  CTAs stride over the units.
-__device__ __forceinline__ void zero_empty_units(const AttendParams& p) {
+// attend to).  CTAs stride over the units; threads t0 .. t0+nt-1 of the CTA
+// share a unit's rows.
+__device__ __forceinline__ void zero_empty_units(const AttendParams& p, int t, int nt) {
   const int per_stream = p.L_att * p.sh.Hkv;
   const int units = p.sh.S * per_stream;
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -134,9 +138,12 @@ __device__ __forceinline__ void zero_empty_units(const AttendParams& p) {
     ur.g = u % p.sh.Hkv;
     for (int row = 0; row < p.R; ++row) {
       float* o = p.out + row_offset(p, ur, row);
-      for (int d = threadIdx.x; d < p.sh.D; d += blockDim.x) o[d] = 0.f;
+      for (int d = t; d < p.sh.D; d += nt) o[d] = 0.f;
     }
   }
+}
+__device__ __forceinline__ void zero_empty_units(const AttendParams& p) {
+  zero_empty_units(p, threadIdx.x, blockDim.x);
 }
 
 // Segment end.  `mrg` holds NWARP warp partials of `wstride` floats, each

@@ -7,50 +7,94 @@
 // and every retained key at r = (slot - origin) mod W,
 //   out = sum_r softmax(<R(r_q) q, R(r) k_r> * scale) v_r.
 //
-// The G query heads that share a KV head make S = Q K^T a dense contraction
-// with M = G rows, and O^T = V^T P^T one with N = G columns, so both run on
-// mma.sync m16n8k16 (bf16 operands, f32 accumulation):
-//  * block of TK = 32 slots starting at slot blk*TK, whose first slot sits at
+// Arithmetic.  The G query heads that share a KV head make S = Q K^T a dense
+// contraction with M = G rows, and O^T = V^T P^T one with N = G columns, so
+// both run on mma.sync m16n8k16 (bf16 operands, f32 accumulation):
+//  * a block of TK = 32 slots starts at slot blk*TK, whose first slot sits at
 //    re-based position r0; slot d of the block is at r0 + d, or r0 + d - W
 //    past the ring's end;
 //  * keys are rotated in f32 by R(d) only (d < 32, a shared-memory table) and
 //    rounded to bf16; the block offset goes into the query instead:
-//    rows 0..7 of the A operand hold R(r_q - r0) q and rows 8..15 hold
-//    R(r_q - r0 + W) q, so each key picks the row of its own base
-//    (<R(a) q, R(b) k> depends only on b - a);
+//    rows 0..7 of the A operand hold R(r_q - r0) q and, in the one block of a
+//    unit that holds the ring's end, rows 8..15 hold R(r_q - r0 + W) q, so
+//    each key picks the row of its own base (<R(a) q, R(b) k> depends only on
+//    b - a);
 //  * the S accumulator fragment is exactly the B fragment P^T of the second
 //    product, so probabilities never leave registers.
 // Stored-rotated keys skip the key rotation and use R(r_q) q alone.
-// K/V tiles come by 3-D TMA (128-byte swizzle) into a private 2-stage ring per
-// warp, with the two (cos, sin) rows of the block's query rotations.
+//
+// Pipeline (one persistent CTA per SM).  Warp 0 is the producer: one lane
+// walks the CTA's share of the block list and streams every block's K and V
+// tiles (one 4-D TMA box per tile, 128-byte swizzle) plus the (cos, sin) rows
+// of the block's query rotations into a ring of NS shared-memory stages
+// (full/empty mbarriers).  Warps 1..NCW are consumers: block j of the CTA's share goes to
+// consumer j mod NCW, which keeps an online-softmax state per unit segment.
+// At the end of a segment the consumers merge their states through shared
+// memory (named barrier, shared atomics); a unit split across CTAs is
+// finished by the CTA that arrives last on the unit's ticket, so no CTA waits
+// on another.
+#include <climits>
+#include <type_traits>
+
 #include "rkv_attend_common.cuh"
+
+#ifndef RKV_MMA_NCW
+#define RKV_MMA_NCW 8
+#endif
 
 namespace rkv {
 
 namespace {
 
-constexpr int MMA_NSW = 2;
+constexpr int NCW = RKV_MMA_NCW;              // consumer warps
+constexpr int MMA_THREADS = (NCW + 1) * 32;   // + the producer warp
+constexpr int CONS_THREADS = NCW * 32;
+constexpr int MMA_MAX_STAGES = 16;
+constexpr int SMEM_LIMIT = 227 * 1024;        // opt-in shared memory per CTA
+constexpr int BAR_CONS = 1;                   // named barrier of the consumer warps
+
+constexpr int TKH = TK / 2;     // keys of a block each warp of a pair takes
+constexpr int NPAIR = NCW / 2;  // consumer warp pairs
 
 template <int D, bool ROTK>
 struct MmaCfg {
-  static constexpr int TILE = TK * D * 2;                 // bf16 K (or V) tile
+  static constexpr int HALF = D / 2;
+  static constexpr int TILE = TK * D * 2;                 // bf16 K (or V) block tile
   static constexpr int NBOX = D / 64;                     // 128-byte boxes per row
-  static constexpr int TROW = ROTK ? 2 * D * 4 : 0;       // two float2[D/2] table rows
-  static constexpr int STAGE = ((2 * TILE + TROW + 1023) / 1024) * 1024;
+  static constexpr int TROW = ROTK ? HALF * 8 : 0;        // one (cos, sin) row
+  static constexpr int STAGE = ((2 * TILE + 2 * TROW + 1023) / 1024) * 1024;
   static constexpr int NGRP = D / 8;                      // 8-dim groups
   static constexpr int NKB = D / 16;                      // k-blocks of the QK product
-  static constexpr int FINE = ROTK ? TK * (D / 2) * 8 : 0;  // fine (cos, sin) table
+  static constexpr int HG = NGRP / 2;
+  static constexpr int FINE = ROTK ? TK * HALF * 8 : 0;   // R(d) table, d < TK
+  static constexpr int QSTR = D + 8;                      // padded query row (floats)
+  static constexpr int OSTR = D + 4;                      // padded output row (floats)
+  static constexpr int SLOT = 16 + 8 * OSTR;              // warp partial: m[8] l[8] o[8][OSTR]
+  // Bytes after the stages, without the per-stream prefix.
+  static constexpr int FIXED = FINE + 8 * QSTR * 4 + NCW * SLOT * 4 + 16;
 };
 
+__host__ __device__ constexpr size_t mma_smem_bytes(int stage, int fixed, int ns, int S) {
+  return 1024 + (size_t)ns * stage + (size_t)fixed + (size_t)ns * 16 + (size_t)(S + 1) * 4;
+}
+
+// 16-byte chunk `grp` of key row `row` (0..TK-1) of a block tile: the tile is
+// D/64 boxes of TK rows x 128 bytes, 128-byte swizzled.
 __device__ __forceinline__ uint32_t swz(int row, int grp) {
   const int box = grp >> 3, cq = grp & 7;
   return static_cast<uint32_t>(box * (TK * 128) + row * 128 + ((cq ^ (row & 7)) << 4));
 }
-// Fine table: row d (0..TK-1) holds (cos, sin)(d * w_i) for i < D/2, 16-byte
-// chunks XOR-swizzled by (d & 7) so that 8 rows read together hit all banks.
-__device__ __forceinline__ uint32_t fine_off(int d, int i) {
-  const int q = i >> 1;
-  return static_cast<uint32_t>(((q ^ (d & 7)) << 4) + ((i & 1) << 3));
+// Fine table: row d (0..TK-1) holds the rotation R(d) for every pair; 16-byte
+// chunk k holds pairs 2k and 2k+1.  The chunk sits at position
+// k ^ ((d mod NCH/4) * 4) of its row (NCH = D/4 chunks per row), so the two
+// keys that one 8-lane phase of a 128-bit load reads (rows d, d+1, same k)
+// fall into different halves of the 128-byte bank window.  Split-half chunks
+// are (cos_2k, cos_2k+1, sin_2k, sin_2k+1), interleaved ones
+// (cos_2k, sin_2k, cos_2k+1, sin_2k+1).
+template <int D>
+__device__ __forceinline__ uint32_t fine_chunk(int d, int k) {
+  constexpr int NCH = D / 4;
+  return static_cast<uint32_t>((k ^ ((d & (NCH / 4 - 1)) << 2)) << 4);
 }
 
 __device__ __forceinline__ void rot(float& x, float& y, float c, float s) {
@@ -59,118 +103,217 @@ __device__ __forceinline__ void rot(float& x, float& y, float c, float s) {
   x = a;
 }
 
+// Packed f32 pairs (the sm_100+ f32x2 pipe).
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 f2_make(float a, float b) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(f2 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+  f2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// Two split-half pairs held as bf16x2 words: x = dims (i, i+1), y = their
+// partners (i+D/2, i+D/2+1).  Rotated in f32 by (cos, sin) = (c, s) per pair:
+// x' = x c - y s, y' = y c + x s, then rounded to nearest even.
+__device__ __forceinline__ void rot_pair2(uint32_t& x, uint32_t& y, float4 cs) {
+  const f2 X = f2_make(bf_lo(x), bf_hi(x));
+  const f2 Y = f2_make(bf_lo(y), bf_hi(y));
+  const f2 C = f2_make(cs.x, cs.y), S = f2_make(cs.z, cs.w), NS = f2_make(-cs.z, -cs.w);
+  const f2 Xr = f2_fma(Y, NS, f2_mul(X, C));
+  const f2 Yr = f2_fma(X, S, f2_mul(Y, C));
+  float a, b, c, d;
+  f2_split(Xr, a, b);
+  f2_split(Yr, c, d);
+  x = pack_bf2(a, b);
+  y = pack_bf2(c, d);
+}
+
 }  // namespace
 
 template <int D, bool ROTK, int STYLE>
-__global__ void __launch_bounds__(NWARP * 32, 1)
+__global__ void __launch_bounds__(MMA_THREADS, 1)
     attend_mma_decode(const __grid_constant__ AttendParams p,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
   using C = MmaCfg<D, ROTK>;
-  constexpr int NSW = MMA_NSW, TILE = C::TILE, NGRP = C::NGRP, NKB = C::NKB;
-  constexpr int HALF = D / 2, HG = NGRP / 2;
-  const int W = p.sh.W, NB = p.sh.NB, G = p.sh.G;
+  constexpr int TILE = C::TILE, NGRP = C::NGRP, NKB = C::NKB, HALF = C::HALF, HG = C::HG;
+  constexpr int QSTR = C::QSTR;
+  const int W = p.sh.W, NB = p.sh.NB, G = p.sh.G, NS = p.ns;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
-  uint8_t* stages = smem;                                               // [NWARP][NSW][STAGE]
-  uint8_t* fine = stages + NWARP * NSW * C::STAGE;                      // [TK][D/2] float2
-  uint64_t* bars = reinterpret_cast<uint64_t*>(fine + C::FINE);         // [NWARP][NSW]
-  const int wstride = 8 * (D + 2);
-  float* mrg = reinterpret_cast<float*>(bars + NWARP * NSW);            // [NWARP][wstride]
-  int* flag = reinterpret_cast<int*>(mrg + NWARP * wstride);
-  int* pre = flag + 4;
+  uint8_t* stages = smem;                                          // [NS][STAGE]
+  uint8_t* fine = stages + (size_t)NS * C::STAGE;                  // [TK][D/2] (cos, sin)
+  float* qs = reinterpret_cast<float*>(fine + C::FINE);            // [8][QSTR] raw query
+  float* slots = qs + 8 * QSTR;                                    // [NCW][SLOT] warp partials
+  int* flag = reinterpret_cast<int*>(slots + NCW * C::SLOT);       // ticket, abort, issued
+  uint64_t* full = reinterpret_cast<uint64_t*>(flag + 4);          // [NS]
+  uint64_t* empty = full + NS;                                     // [NS]
+  int* pre = reinterpret_cast<int*>(empty + NS);                   // [S+1]
+  volatile int* abort_flag = flag + 1;
 
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, cq = lane & 3;   // mma fragment coordinates
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Prologue that reads nothing the previous kernel of the stream writes: the
+  // barriers and the R(d) table (written once when the handle was created).
   if (tid == 0) {
-    for (int i = 0; i < NWARP * NSW; ++i) mbar_init(smem_u32(bars + i), 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(full + i), 1);
+      mbar_init(smem_u32(empty + i), 2);   // both warps of the pair that takes the block
+    }
     fence_mbar_init();
+    flag[1] = 0;
+    flag[2] = 0;
   }
   if constexpr (ROTK) {
-    for (int idx = tid; idx < TK * HALF; idx += blockDim.x) {
-      const int d = idx / HALF, i = idx % HALF;
-      *reinterpret_cast<float2*>(fine + d * HALF * 8 + fine_off(d, i)) =
-          __ldg(p.table + (size_t)d * HALF + i);
+    for (int idx = tid - 32; idx >= 0 && idx < TK * HALF / 2; idx += CONS_THREADS) {
+      const int d = idx / (HALF / 2), k = idx % (HALF / 2);
+      const float2 a = __ldg(p.table + (size_t)d * HALF + 2 * k);
+      const float2 c = __ldg(p.table + (size_t)d * HALF + 2 * k + 1);
+      const float4 v = STYLE == 0 ? make_float4(a.x, c.x, a.y, c.y)
+                                  : make_float4(a.x, a.y, c.x, c.y);
+      *reinterpret_cast<float4*>(fine + d * HALF * 8 + fine_chunk<D>(d, k)) = v;
     }
   }
-  build_prefix(p, pre);
+  pdl_wait();   // from here on: stream state, pools, queries, outputs
+  if (warp == 1) build_prefix_warp(p, pre, lane);
   __syncthreads();
-  zero_empty_units(p);
   const int T = pre[p.sh.S];
   const int P = min(static_cast<int>(gridDim.x), T);
   const int b = static_cast<int>(blockIdx.x);
   const int rb = b < P ? range_start(b, T, P) : 0, re = b < P ? range_start(b + 1, T, P) : 0;
 
-  uint8_t* my_st = stages + w * NSW * C::STAGE;
-  uint64_t* my_bars = bars + w * NSW;
-  float* my_m = mrg + w * wstride;
-
-  WarpSeq iss;
-  iss.init(rb, re, w);
-  auto issue = [&](int slot_k) {
-    int by;
-    UnitRef ur;
-    if (!iss.next(p, pre, by, ur)) return;
-    const BlockGeo bg = block_geo(by, ur, W, NB);
-    const int ug = static_cast<int>(unit_index(p, ur));
-    const uint32_t bar = smem_u32(my_bars + slot_k);
-    const uint32_t dst = smem_u32(my_st + slot_k * C::STAGE);
-    mbar_arrive_expect_tx(bar, 2 * TILE + C::TROW);
-#pragma unroll
-    for (int bx = 0; bx < C::NBOX; ++bx) {
-      tma_load_3d(dst + bx * TK * 128, &tmK, bx * 64, bg.blk * TK, ug, bar);
-      tma_load_3d(dst + TILE + bx * TK * 128, &tmV, bx * 64, bg.blk * TK, ug, bar);
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0, round = 0, issued = 0;
+      bool stop = false;
+      for (int x = rb; x < re && !stop;) {
+        // Per unit segment: the unit, then the block geometry advanced per block.
+        const UnitRef u = unit_of(x, p, pre);
+        const int x1 = min(u.uend, re);
+        const int ug = static_cast<int>(unit_index(p, u));
+        int blk = touched_block(u.a, x - u.ustart, NB);
+        int r0 = blk * TK - u.a;
+        if (r0 < 0) r0 += W;
+        for (; x < x1; ++x) {
+          if (*abort_flag) { stop = true; break; }
+          if (round > 0 &&
+              !mbar_wait_or_abort(smem_u32(empty + stage), (round - 1) & 1, abort_flag)) {
+            *abort_flag = 1;
+            p.st[u.s].status = STATUS_DEVICE_STATE;
+            stop = true;
+            break;
+          }
+          const uint32_t bar = smem_u32(full + stage);
+          const uint32_t dst = smem_u32(stages + (size_t)stage * C::STAGE);
+          int mA = 0;
+          bool wraps = false;
+          uint32_t bytes = 2 * TILE;
+          if constexpr (ROTK) {
+            mA = u.fill - 1 - r0;
+            wraps = W - r0 < TK;
+            bytes += wraps ? 2 * C::TROW : C::TROW;
+          }
+          mbar_arrive_expect_tx(bar, bytes);
+          // One box per tile: {64 elements, TK rows, the D/64 row halves, one unit}.
+          tma_load_4d(dst, &tmK, 0, blk * TK, 0, ug, bar);
+          tma_load_4d(dst + TILE, &tmV, 0, blk * TK, 0, ug, bar);
+          if constexpr (ROTK) {
+            bulk_load(dst + 2 * TILE, p.table + (size_t)(mA < 0 ? -mA : mA) * HALF, C::TROW, bar);
+            if (wraps)
+              bulk_load(dst + 2 * TILE + C::TROW, p.table + (size_t)(mA + W) * HALF, C::TROW,
+                        bar);
+          }
+          ++issued;
+          if (++stage == NS) { stage = 0; ++round; }
+          if (++blk == NB) blk = 0;
+          r0 += TK;
+          if (r0 >= W) r0 -= W;
+        }
+      }
+      flag[2] = issued;
     }
-    if constexpr (ROTK) {
-      const int rq = ur.fill - 1;
-      const int mA = rq - bg.r0, mB = mA + W;
-      const float2* ta = p.table + (size_t)(mA < 0 ? -mA : mA) * HALF;
-      const float2* tb = p.table + (size_t)mB * HALF;
-      bulk_load(dst + 2 * TILE, ta, HALF * 8, bar);
-      bulk_load(dst + 2 * TILE + HALF * 8, tb, HALF * 8, bar);
-    }
-  };
-  if (lane == 0)
-    for (int k = 0; k < NSW; ++k) issue(k);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ consumers
+    const int cw = warp - 1, ct = tid - 32;
+    const int g = lane >> 2, cq = lane & 3;   // mma fragment coordinates
+    zero_empty_units(p, ct, CONS_THREADS);
+    // Raw query of a unit into `qs` (rows >= G are zero).
+    auto load_query = [&](const UnitRef& u) {
+      for (int idx = ct; idx < 8 * D; idx += CONS_THREADS) {
+        const int h = idx / D, d = idx % D;
+        qs[h * QSTR + d] = h < G ? load_elem(p.q, row_offset(p, u, h) + d, p.sh.q_bf16) : 0.f;
+      }
+    };
+    if (rb < re) load_query(unit_of(rb, p, pre));
+    named_bar_sync(BAR_CONS, CONS_THREADS);
 
-  // The thread's query elements: head g, dims of its A fragments.
-  //   k-block kb, j in {0,1,2,3}: dim 16kb + (j>>1)*8 + 2cq + (j&1)
-  auto qdim = [&](int kb, int j) { return 16 * kb + (j >> 1) * 8 + 2 * cq + (j & 1); };
+    // Dims of the thread's A-fragment elements: k-block kb, j in {0,1,2,3}:
+    //   dim 16kb + (j>>1)*8 + 2cq + (j&1)
+    auto qdim = [&](int kb, int j) { return 16 * kb + (j >> 1) * 8 + 2 * cq + (j & 1); };
 
-  bool dead = false;
-  int k = 0;
-  for (int x = rb; x < re;) {
-    const UnitRef u = unit_of(x, p, pre);
-    const int x1 = min(u.uend, re), n = x1 - x;
-    const int cb = x + (w * n) / NWARP, ce = x + ((w + 1) * n) / NWARP;
-    const int rq = u.fill - 1;
+    // Warp pair pi takes blocks pi, pi + NPAIR, ...; warp hh of the pair takes
+    // keys 16*hh .. 16*hh+15 of each.
+    const int pi = cw >> 1, hh = cw & 1;
+    int jb = pi, stage = pi, round = 0;   // the pair's next block and its stage (NS >= NPAIR)
+    bool dead = false;
+    for (int x = rb; x < re;) {
+      const UnitRef u = unit_of(x, p, pre);
+      const int x1 = min(u.uend, re);
+      const int rq = u.fill - 1;
+      // The next segment's query: loaded now, stored once this segment is done.
+      const bool has_next = x1 < re;
+      constexpr int QPT = (8 * D + CONS_THREADS - 1) / CONS_THREADS;
+      float nq[QPT];
+      if (has_next) {
+        const UnitRef un = unit_of(x1, p, pre);
+#pragma unroll
+        for (int t = 0; t < QPT; ++t) {
+          const int idx = ct + t * CONS_THREADS, h = idx / D, d = idx % D;
+          nq[t] = (idx < 8 * D && h < G)
+                      ? load_elem(p.q, row_offset(p, un, h) + d, p.sh.q_bf16) : 0.f;
+        }
+      }
 
-    float qf[NKB][4];                // raw query (f32), head g
-    uint32_t qa[NKB][4];             // A fragments of the QK product
-    float o[NKB][4];                 // O^T accumulators: m-tile = 16 dims
-    float m_run = NEG_BIG, l_run = 0.f;
-#pragma unroll
-    for (int kb = 0; kb < NKB; ++kb)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) { o[kb][j] = 0.f; qf[kb][j] = 0.f; qa[kb][j] = 0u; }
-    if (cb < ce && g < G) {
-      const size_t qo = row_offset(p, u, g);
-#pragma unroll
-      for (int kb = 0; kb < NKB; ++kb)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) qf[kb][j] = load_elem(p.q, qo + qdim(kb, j), p.sh.q_bf16);
-    }
-    if constexpr (!ROTK) {
-      // Stored-rotated keys sit at r already: one base, R(r_q) q.
-      if (cb < ce && g < G) {
-        const float2* t = p.table + (size_t)rq * HALF;
-        float qr[NKB][4];
+      // The raw query of head g (dims of the thread's A fragments), from `qs`.
+      auto load_qf = [&](float (&qr)[NKB][4]) {
 #pragma unroll
         for (int kb = 0; kb < NKB; ++kb)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) qr[kb][j] = qf[kb][j];
+          for (int j = 0; j < 4; j += 2) {
+            const float2 v = *reinterpret_cast<const float2*>(qs + g * QSTR + qdim(kb, j));
+            qr[kb][j] = v.x;
+            qr[kb][j + 1] = v.y;
+          }
+      };
+      uint32_t qa[NKB][4];             // A fragments of the QK product
+      float o[NKB][4];                 // O^T accumulators: m-tile = 16 dims
+      float m_run = NEG_BIG, l_run = 0.f;
+#pragma unroll
+      for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          o[kb][j] = 0.f;
+          qa[kb][j] = 0u;
+        }
+      if constexpr (!ROTK) {
+        // Stored-rotated keys sit at r already: one base, R(r_q) q.
+        const float2* t = p.table + (size_t)rq * HALF;
+        float qr[NKB][4];
+        load_qf(qr);
         if constexpr (STYLE == 0) {
 #pragma unroll
           for (int kb = 0; kb < NKB / 2; ++kb)
@@ -192,236 +335,324 @@ __global__ void __launch_bounds__(NWARP * 32, 1)
         for (int kb = 0; kb < NKB; ++kb) {
           qa[kb][0] = pack_bf2(qr[kb][0], qr[kb][1]);
           qa[kb][2] = pack_bf2(qr[kb][2], qr[kb][3]);
-          qa[kb][1] = 0u;
-          qa[kb][3] = 0u;
         }
       }
-    }
 
-    for (int y = cb; y < ce; ++y, ++k) {
-      const int st = k % NSW;
-      if (!dead && !mbar_wait(smem_u32(my_bars + st), (k / NSW) & 1)) {
-        dead = true;
-        if (lane == 0) p.st[u.s].status = STATUS_DEVICE_STATE;
-      }
-      if (!dead) {
-        const uint8_t* kt = my_st + st * C::STAGE;
-        const uint8_t* vt = kt + TILE;
-        const uint32_t kt_s = smem_u32(kt), vt_s = smem_u32(vt);
-        const BlockGeo bg = block_geo(y, u, W, NB);
-        const int r0 = bg.r0;
-        const int wrap_at = W - r0;               // keys d >= wrap_at use base B
-        // ---- query fragments for this block's two bases ----
-        if constexpr (ROTK) {
-          if (g < G) {
-            const float2* ta = reinterpret_cast<const float2*>(kt + 2 * TILE);
-            const float2* tb = ta + HALF;
-            const float sa = (rq - r0) < 0 ? -1.f : 1.f;
-            float qA[NKB][4], qB[NKB][4];
+      int r0 = -1;                     // re-based position of the block's first slot
+      for (; rb + jb < x1; jb += NPAIR) {
+        const int y = rb + jb;
+        if (r0 < 0) {
+          r0 = block_geo(y, u, W, NB).r0;
+        } else {
+          r0 += NPAIR * TK;              // NPAIR blocks further on along the ring
+          while (r0 >= W) r0 -= W;
+        }
+        const int wrap_at = W - r0;      // keys d >= wrap_at sit at r0 + d - W
+        const bool wraps = wrap_at < TK;
+        const bool allvalid = wraps ? (u.fill == W) : (r0 + TK <= u.fill);
+        {
+          const int st_i = stage, st_r = round;
+          // A pair only waits on every NPAIR-th stage, so it may reach one
+          // before the stage's previous block has even landed.  Waiting first
+          // for that block's release makes the full barrier's parity unambiguous.
+          if (!dead && st_r > 0 &&
+              !mbar_wait_or_abort(smem_u32(empty + st_i), (st_r - 1) & 1, abort_flag))
+            dead = true;
+          if (!dead && !mbar_wait_or_abort(smem_u32(full + st_i), st_r & 1, abort_flag))
+            dead = true;
+          dead = __any_sync(0xffffffffu, dead);   // the warp stays converged
+          if (dead && lane == 0 && !*abort_flag) {
+            *abort_flag = 1;
+            p.st[u.s].status = STATUS_DEVICE_STATE;
+          }
+          if (!dead) {
+          const uint8_t* kt = stages + (size_t)st_i * C::STAGE;
+          const uint8_t* vt = kt + TILE;
+          const uint32_t kt_s = smem_u32(kt), vt_s = smem_u32(vt);
+          // ---- query fragments for this block's base(s) ----
+          if constexpr (ROTK) {
+            {
+              const float2* ta = reinterpret_cast<const float2*>(kt + 2 * TILE);
+              const float sa = (rq - r0) < 0 ? -1.f : 1.f;
+              // Rows 0..7 (hi = 0) or 8..15 (hi = 1) of the A operand.
+              auto rotate_q = [&](const float2* tr, float sg, auto hi_c) {
+                constexpr int hi = decltype(hi_c)::value;
+                float qr[NKB][4];
+                load_qf(qr);
+                if constexpr (STYLE == 0) {
+#pragma unroll
+                  for (int kb = 0; kb < NKB / 2; ++kb)
+#pragma unroll
+                    for (int j = 0; j < 4; j += 2) {
+                      const float4 a = *reinterpret_cast<const float4*>(tr + qdim(kb, j));
+                      rot(qr[kb][j], qr[kb + NKB / 2][j], a.x, sg * a.y);
+                      rot(qr[kb][j + 1], qr[kb + NKB / 2][j + 1], a.z, sg * a.w);
+                    }
+                } else {
+#pragma unroll
+                  for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+                    for (int j = 0; j < 4; j += 2) {
+                      const float2 a = tr[qdim(kb, j) >> 1];
+                      rot(qr[kb][j], qr[kb][j + 1], a.x, sg * a.y);
+                    }
+                }
+#pragma unroll
+                for (int kb = 0; kb < NKB; ++kb) {
+                  qa[kb][hi] = pack_bf2(qr[kb][0], qr[kb][1]);
+                  qa[kb][hi + 2] = pack_bf2(qr[kb][2], qr[kb][3]);
+                }
+              };
+              rotate_q(ta, sa, std::integral_constant<int, 0>{});
+              if (wraps) rotate_q(ta + HALF, 1.f, std::integral_constant<int, 1>{});
+            }
+          }
+          // ---- S = Q K^T per 8-key group; select each key's base ----
+          float s[2][2];
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) {
+            uint32_t kf[NGRP];
+            const int krow = hh * TKH + nb * 8 + (lane & 7);
+#pragma unroll
+            for (int g4 = 0; g4 < NGRP; g4 += 4)
+              ldsm_x4(kt_s + swz(krow, g4 + (lane >> 3)), kf[g4], kf[g4 + 1], kf[g4 + 2],
+                      kf[g4 + 3]);
+            if constexpr (ROTK) {
+              const int dk = hh * TKH + nb * 8 + g;   // this thread's key within the block
+              const uint8_t* frow = fine + dk * HALF * 8;
+              if constexpr (STYLE == 0) {
+#pragma unroll
+                for (int gr = 0; gr < HG; ++gr) {
+                  const int k = 4 * gr + cq;      // pairs 8gr + 2cq and 8gr + 2cq + 1
+                  const float4 cs =
+                      *reinterpret_cast<const float4*>(frow + fine_chunk<D>(dk, k));
+                  rot_pair2(kf[gr], kf[gr + HG], cs);
+                }
+              } else {
+#pragma unroll
+                for (int gr = 0; gr < NGRP; ++gr) {
+                  const int i = 4 * gr + cq;      // the pair in word gr
+                  const float2 cs = *reinterpret_cast<const float2*>(
+                      frow + fine_chunk<D>(dk, i >> 1) + ((i & 1) << 3));
+                  float x0 = bf_lo(kf[gr]), x1 = bf_hi(kf[gr]);
+                  rot(x0, x1, cs.x, cs.y);
+                  kf[gr] = pack_bf2(x0, x1);
+                }
+              }
+            }
+            float accs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kb = 0; kb < NKB; ++kb)
+              mma_bf16(accs, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kf[2 * kb],
+                       kf[2 * kb + 1]);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) { qA[kb][j] = qf[kb][j]; qB[kb][j] = qf[kb][j]; }
-            if constexpr (STYLE == 0) {
-#pragma unroll
-              for (int kb = 0; kb < NKB / 2; ++kb)
-#pragma unroll
-                for (int j = 0; j < 4; j += 2) {
-                  const int i = qdim(kb, j);
-                  const float4 a = *reinterpret_cast<const float4*>(ta + i);
-                  const float4 bb = *reinterpret_cast<const float4*>(tb + i);
-                  rot(qA[kb][j], qA[kb + NKB / 2][j], a.x, sa * a.y);
-                  rot(qA[kb][j + 1], qA[kb + NKB / 2][j + 1], a.z, sa * a.w);
-                  rot(qB[kb][j], qB[kb + NKB / 2][j], bb.x, bb.y);
-                  rot(qB[kb][j + 1], qB[kb + NKB / 2][j + 1], bb.z, bb.w);
-                }
-            } else {
-#pragma unroll
-              for (int kb = 0; kb < NKB; ++kb)
-#pragma unroll
-                for (int j = 0; j < 4; j += 2) {
-                  const int i = qdim(kb, j) >> 1;
-                  const float2 a = ta[i], bb = tb[i];
-                  rot(qA[kb][j], qA[kb][j + 1], a.x, sa * a.y);
-                  rot(qB[kb][j], qB[kb][j + 1], bb.x, bb.y);
-                }
-            }
-#pragma unroll
-            for (int kb = 0; kb < NKB; ++kb) {
-              qa[kb][0] = pack_bf2(qA[kb][0], qA[kb][1]);
-              qa[kb][2] = pack_bf2(qA[kb][2], qA[kb][3]);
-              qa[kb][1] = pack_bf2(qB[kb][0], qB[kb][1]);
-              qa[kb][3] = pack_bf2(qB[kb][2], qB[kb][3]);
+            for (int e = 0; e < 2; ++e) {
+              const int d = hh * TKH + nb * 8 + 2 * cq + e;
+              const bool wr = ROTK && d >= wrap_at;
+              const int r = r0 + d - (d >= wrap_at ? W : 0);
+              const bool vis = allvalid || r < u.fill;
+              s[nb][e] = vis ? (wr ? accs[2 + e] : accs[e]) * p.scale_log2 : NEG_BIG;
             }
           }
-        }
-        // ---- S = Q K^T per 8-key group; select each key's base ----
-        float s[4][2];
-        int nvalid = 0;
+          // ---- online softmax for head g (the 4 lanes of quad g) ----
+          float tmax = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+          const float mnew = fmaxf(m_run, tmax);
+          const float alpha = exp2f(m_run - mnew);
+          float pr[2][2];
+          float psum = 0.f;
 #pragma unroll
-        for (int nb = 0; nb < 4; ++nb) {
-          uint32_t kf[NGRP];
-          const int krow = nb * 8 + (lane & 7);
+          for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-          for (int g4 = 0; g4 < NGRP; g4 += 4)
-            ldsm_x4(kt_s + swz(krow, g4 + (lane >> 3)), kf[g4], kf[g4 + 1], kf[g4 + 2],
-                    kf[g4 + 3]);
-          if constexpr (ROTK) {
-            const int dk = nb * 8 + g;          // this thread's key within the block
-            const uint8_t* frow = fine + dk * HALF * 8;
-            if constexpr (STYLE == 0) {
-#pragma unroll
-              for (int gr = 0; gr < HG; ++gr) {
-                const int i = 8 * gr + 2 * cq;
-                const float4 cs = *reinterpret_cast<const float4*>(frow + fine_off(dk, i));
-                float x0 = bf_lo(kf[gr]), x1 = bf_hi(kf[gr]);
-                float y0 = bf_lo(kf[gr + HG]), y1 = bf_hi(kf[gr + HG]);
-                rot(x0, y0, cs.x, cs.y);
-                rot(x1, y1, cs.z, cs.w);
-                kf[gr] = pack_bf2(x0, x1);
-                kf[gr + HG] = pack_bf2(y0, y1);
-              }
-            } else {
-#pragma unroll
-              for (int gr = 0; gr < NGRP; ++gr) {
-                const int i = 4 * gr + cq;
-                const float2 cs = *reinterpret_cast<const float2*>(frow + fine_off(dk, i));
-                float x0 = bf_lo(kf[gr]), x1 = bf_hi(kf[gr]);
-                rot(x0, x1, cs.x, cs.y);
-                kf[gr] = pack_bf2(x0, x1);
-              }
+            for (int e = 0; e < 2; ++e) {
+              pr[nb][e] = s[nb][e] > 0.5f * NEG_BIG ? exp2f(s[nb][e] - mnew) : 0.f;
+              psum += pr[nb][e];
             }
-          }
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int kb = 0; kb < NKB; ++kb)
-            mma_bf16(acc, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kf[2 * kb], kf[2 * kb + 1]);
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int d = nb * 8 + 2 * cq + e;
-            const bool wr = ROTK && d >= wrap_at;
-            int r = r0 + d;
-            if (r >= W) r -= W;
-            const bool vis = (r < u.fill) && (g < G);
-            nvalid += (r < u.fill);
-            s[nb][e] = vis ? (wr ? acc[2 + e] : acc[e]) * p.scale_log2 : NEG_BIG;
-          }
-        }
-        // ---- online softmax for head g (the 4 lanes of quad g) ----
-        float tmax = NEG_BIG;
-#pragma unroll
-        for (int nb = 0; nb < 4; ++nb) tmax = fmaxf(tmax, fmaxf(s[nb][0], s[nb][1]));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-        const float mnew = fmaxf(m_run, tmax);
-        const float alpha = exp2f(m_run - mnew);
-        float pr[4][2];
-        float psum = 0.f;
-#pragma unroll
-        for (int nb = 0; nb < 4; ++nb)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            pr[nb][e] = s[nb][e] > 0.5f * NEG_BIG ? exp2f(s[nb][e] - mnew) : 0.f;
-            psum += pr[nb][e];
-          }
-        l_run = l_run * alpha + psum;
-        m_run = mnew;
-        const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * cq);      // head 2cq
-        const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * cq + 4);  // head 2cq+1
-#pragma unroll
-        for (int mt = 0; mt < NKB; ++mt) {
-          o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
-        }
-        // ---- O^T += V^T P^T ----
-        const bool full = __all_sync(0xffffffffu, nvalid == 8);
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const uint32_t b0 = pack_bf2(pr[2 * kk][0], pr[2 * kk][1]);
-          const uint32_t b1 = pack_bf2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
-          // validity of the keys this thread's V^T elements belong to
-          uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-          if (!full) {
-            auto ok = [&](int d) {
-              int r = r0 + d;
-              if (r >= W) r -= W;
-              return r < u.fill;
-            };
-            const int d0 = 16 * kk + 2 * cq;
-            mlo = (ok(d0) ? 0x0000ffffu : 0u) | (ok(d0 + 1) ? 0xffff0000u : 0u);
-            mhi = (ok(d0 + 8) ? 0x0000ffffu : 0u) | (ok(d0 + 9) ? 0xffff0000u : 0u);
-          }
-          const int vrow = 16 * kk + ((lane >> 4) << 3) + (lane & 7);
+          l_run = l_run * alpha + psum;
+          m_run = mnew;
+          const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * cq);      // head 2cq
+          const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * cq + 4);  // head 2cq+1
 #pragma unroll
           for (int mt = 0; mt < NKB; ++mt) {
-            uint32_t v0, v1, v2, v3;
-            ldsm_x4_t(vt_s + swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
-            mma_bf16(o[mt], v0 & mlo, v1 & mlo, v2 & mhi, v3 & mhi, b0, b1);
+            o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
+          }
+          // ---- O^T += V^T P^T over the 16 keys of this half ----
+          {
+            const uint32_t b0 = pack_bf2(pr[0][0], pr[0][1]);
+            const uint32_t b1 = pack_bf2(pr[1][0], pr[1][1]);
+            // V rows of keys outside the window are zeroed (they may hold anything).
+            uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+            if (!allvalid) {
+              auto ok = [&](int d) { return r0 + d - (d >= wrap_at ? W : 0) < u.fill; };
+              const int d0 = hh * TKH + 2 * cq;
+              mlo = (ok(d0) ? 0x0000ffffu : 0u) | (ok(d0 + 1) ? 0xffff0000u : 0u);
+              mhi = (ok(d0 + 8) ? 0x0000ffffu : 0u) | (ok(d0 + 9) ? 0xffff0000u : 0u);
+            }
+            const int vrow = hh * TKH + ((lane >> 4) << 3) + (lane & 7);
+#pragma unroll
+            for (int mt = 0; mt < NKB; ++mt) {
+              uint32_t v0, v1, v2, v3;
+              ldsm_x4_t(vt_s + swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
+              mma_bf16(o[mt], v0 & mlo, v1 & mlo, v2 & mhi, v3 & mhi, b0, b1);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(empty + st_i));   // this warp's half is done
           }
         }
+        stage += NPAIR;
+        if (stage >= NS) { stage -= NS; ++round; }
       }
-      __syncwarp();
-      if (lane == 0 && !dead) {
-        fence_proxy_async();
-        issue(st);
-      }
-    }
 
-    // ---- segment end: warp partial -> shared (rows = heads), CTA merge ----
-    float lsum = l_run;
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-    const int R = p.R;   // == G for decode
-    if (cq == 0 && g < R) { my_m[g] = m_run; my_m[R + g] = lsum; }
+      // ---- segment end: merge the consumer warps (rows = heads) ----
+      // Each warp leaves (m, l, o) of its blocks in its slot; after one barrier
+      // every thread combines the NCW slots for its output elements.
+      {
+        float lsum = l_run;
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+        float* my = slots + cw * C::SLOT;
+        if (cq == 0) { my[g] = m_run; my[8 + g] = lsum; }
 #pragma unroll
-    for (int mt = 0; mt < NKB; ++mt)
+        for (int mt = 0; mt < NKB; ++mt)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int h = 2 * cq + (j & 1);
-        const int d = 16 * mt + g + ((j >> 1) << 3);
-        if (h < R) my_m[2 * R + h * D + d] = o[mt][j];
+          for (int j = 0; j < 4; ++j) {
+            const int h = 2 * cq + (j & 1);
+            const int d = 16 * mt + g + ((j >> 1) << 3);
+            my[16 + h * C::OSTR + d] = o[mt][j];
+          }
       }
-    __syncthreads();
-    finish_segment(p, u, x, x1, rb, T, P, mrg, wstride, flag);
-    __syncthreads();
-    x = x1;
-  }
-  if (dead && lane == 0) {
-    for (int i = 0; i < NSW; ++i) {
-      const int kk = k + i;
-      mbar_wait(smem_u32(my_bars + kk % NSW), (kk / NSW) & 1);
+      named_bar_sync(BAR_CONS, CONS_THREADS);
+      if (has_next) {
+#pragma unroll
+        for (int t = 0; t < QPT; ++t) {
+          const int idx = ct + t * CONS_THREADS;
+          if (idx < 8 * D) qs[(idx / D) * QSTR + idx % D] = nq[t];
+        }
+      }
+      const int R = p.R;   // == G for decode
+      const bool whole = (x == u.ustart) && (x1 == u.uend);
+      float* part = nullptr;
+      if (!whole) part = p.partials + (size_t)(2 * b + (x == rb ? 0 : 1)) * p.slot_floats;
+      for (int idx = ct; idx < R * D; idx += CONS_THREADS) {
+        const int h = idx / D, d = idx % D;
+        float M = NEG_BIG;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, slots[w * C::SLOT + h]);
+        float L = 0.f, v = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+          const float* sw = slots + w * C::SLOT;
+          const float sc = exp2f(sw[h] - M);
+          L += sc * sw[8 + h];
+          v += sc * sw[16 + h * C::OSTR + d];
+        }
+        if (whole) {
+          p.out[row_offset(p, u, h) + d] = L > 0.f ? v / L : 0.f;
+        } else {
+          if (d == 0) { part[h] = M; part[R + h] = L; }
+          part[2 * R + h * D + d] = v;
+        }
+      }
+      if (!whole) {
+        // Publish this CTA's partial (one release by one thread after the
+        // barrier); the last CTA of the unit to arrive merges them all.
+        named_bar_sync(BAR_CONS, CONS_THREADS);
+        if (ct == 0) {
+          __threadfence();
+          flag[0] = atomicAdd(&p.unit_tickets[unit_index(p, u)], 1);
+          __threadfence();
+        }
+        named_bar_sync(BAR_CONS, CONS_THREADS);
+        const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
+        if (flag[0] == b1 - b0) {
+          const int rs0 = range_start(b0, T, P);
+          for (int idx = ct; idx < R * D; idx += CONS_THREADS) {
+            const int h = idx / D, d = idx % D;
+            float M = NEG_BIG;
+            for (int bb = b0; bb <= b1; ++bb) {
+              const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
+              M = fmaxf(M, __ldcg(p.partials + (size_t)(2 * bb + k) * p.slot_floats + h));
+            }
+            float num = 0.f, den = 0.f;
+            for (int bb = b0; bb <= b1; ++bb) {
+              const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
+              const float* pp = p.partials + (size_t)(2 * bb + k) * p.slot_floats;
+              const float sc = exp2f(__ldcg(pp + h) - M);
+              den += sc * __ldcg(pp + R + h);
+              num += sc * __ldcg(pp + 2 * R + h * D + d);
+            }
+            p.out[row_offset(p, u, h) + d] = den > 0.f ? num / den : 0.f;
+          }
+          if (ct == 0) p.unit_tickets[unit_index(p, u)] = 0;
+        }
+      }
+      named_bar_sync(BAR_CONS, CONS_THREADS);
+      x = x1;
     }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // No CTA exits with a copy still in flight into its shared memory: wait
+    // (bounded) for the last NS stages this CTA issued.
+    const int issued = flag[2];
+    for (int j = max(0, issued - NS); j < issued; ++j)
+      mbar_wait(smem_u32(full + (j % NS)), (j / NS) & 1);
   }
 }
 
 template <int D, bool ROTK>
-static size_t mma_smem_t(int S) {
+static int mma_stages(int S) {
   using C = MmaCfg<D, ROTK>;
-  size_t b = (size_t)NWARP * MMA_NSW * C::STAGE + C::FINE + NWARP * MMA_NSW * 8;
-  b += (size_t)NWARP * 8 * (D + 2) * 4 + (4 + S + 1) * 4;
-  return b + 1024;
+  int ns = MMA_MAX_STAGES;
+  while (ns > NPAIR && mma_smem_bytes(C::STAGE, C::FIXED, ns, S) > (size_t)SMEM_LIMIT) --ns;
+  return ns;
 }
 
 size_t attend_mma_smem(const Shape& sh, int c) {
   (void)c;
   const bool rotk = !sh.stored_rotated;
-  if (sh.D == 128) return rotk ? mma_smem_t<128, true>(sh.S) : mma_smem_t<128, false>(sh.S);
-  return rotk ? mma_smem_t<64, true>(sh.S) : mma_smem_t<64, false>(sh.S);
+  if (sh.D == 128) {
+    if (rotk) return mma_smem_bytes(MmaCfg<128, true>::STAGE, MmaCfg<128, true>::FIXED,
+                                    mma_stages<128, true>(sh.S), sh.S);
+    return mma_smem_bytes(MmaCfg<128, false>::STAGE, MmaCfg<128, false>::FIXED,
+                          mma_stages<128, false>(sh.S), sh.S);
+  }
+  if (rotk) return mma_smem_bytes(MmaCfg<64, true>::STAGE, MmaCfg<64, true>::FIXED,
+                                  mma_stages<64, true>(sh.S), sh.S);
+  return mma_smem_bytes(MmaCfg<64, false>::STAGE, MmaCfg<64, false>::FIXED,
+                        mma_stages<64, false>(sh.S), sh.S);
 }
 
 bool attend_mma_supported(const Shape& sh, int c) {
-  return sh.bf16 && sh.q_bf16 >= 0 && (sh.D == 64 || sh.D == 128) && sh.G <= 8 && c == 1;
+  return sh.bf16 && (sh.D == 64 || sh.D == 128) && sh.G <= 8 && c == 1 &&
+         attend_mma_smem(sh, c) <= (size_t)SMEM_LIMIT;
 }
 
 template <int D, bool ROTK, int STYLE>
-static cudaError_t launch_mma_t(const AttendParams& p, const CUtensorMap& tk,
+static cudaError_t launch_mma_t(const AttendParams& p0, const CUtensorMap& tk,
                                 const CUtensorMap& tv, int grid, cudaStream_t s) {
-  const size_t smem = mma_smem_t<D, ROTK>(p.sh.S);
+  using C = MmaCfg<D, ROTK>;
+  AttendParams p = p0;
+  p.ns = mma_stages<D, ROTK>(p.sh.S);
+  const size_t smem = mma_smem_bytes(C::STAGE, C::FIXED, p.ns, p.sh.S);
   auto kern = attend_mma_decode<D, ROTK, STYLE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, NWARP * 32, smem, s>>>(p, tk, tv);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the prologue overlaps the previous kernel.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(MMA_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, tk, tv);
 }
 
 template <int D>

@@ -59,7 +59,7 @@ extern "C" rkv_status rkv_attend_static_scratch(rkv_handle* h, const void* q, fl
 
   // Sizes first: a call that needs more scratch than the array holds is
   // rejected before anything touches the GPU.
-  const int grid = h->num_sms < rkv::kMaxCtas ? h->num_sms : rkv::kMaxCtas;
+  const int grid = rkv::attend_grid(h, n_layers);
   const size_t tickets = (size_t)h->sh.S * h->sh.L * h->sh.Hkv * sizeof(int);
   const size_t partials = (size_t)2 * grid * h->ws.slot_floats * sizeof(float);
   if (tickets > kTicketBytes || partials > kPartialBytes) return RKV_ERR_UNSUPPORTED;
@@ -86,9 +86,10 @@ extern "C" rkv_status rkv_attend_static_scratch(rkv_handle* h, const void* q, fl
   p.slot_floats = h->ws.slot_floats;
   p.scale_log2 = h->scale * 1.4426950408889634f;
   cudaError_t e;
-  const bool mma = h->cfg.attend_impl != RKV_ATTEND_FMA && rkv::attend_mma_supported(h->sh, n_q);
+  const bool mma = h->cfg.attend_impl != RKV_ATTEND_FMA && h->has_map4 &&
+                   rkv::attend_mma_supported(h->sh, n_q);
   if (mma) {
-    e = rkv::launch_attend_mma(p, h->tmK, h->tmV, grid, s);
+    e = rkv::launch_attend_mma(p, h->tmK4, h->tmV4, grid, s);
   } else {
     if (h->cfg.attend_impl == RKV_ATTEND_MMA) return RKV_ERR_UNSUPPORTED;
     if (p.R > 16) return RKV_ERR_UNSUPPORTED;

@@ -15,7 +15,9 @@ struct rkv_handle {
   void* v_pool;
   rkv::StreamState* state;
   uint8_t* workspace;
-  CUtensorMap tmK, tmV;
+  CUtensorMap tmK, tmV;     // 3-D views [units][W][D], boxes of 128 bytes x TK rows
+  CUtensorMap tmK4, tmV4;   // bf16 pools: 4-D views, one box = a whole TK-row tile
+  bool has_map4;
   int num_sms;
   int last_launches;
   float scale;
@@ -25,4 +27,17 @@ struct rkv_handle {
 namespace rkv {
 // Largest persistent grid of the attention kernels.
 constexpr int kMaxCtas = 1024;
+
+// Persistent grid of an attention call over n_layers layers.  The block list
+// is cut into equal shares, CTA b taking [b*T/P, (b+1)*T/P).  With one stream
+// every unit (layer, KV head) has the same number of blocks, so a grid of
+// U*k CTAs (U units, k = #SMs / U) cuts each unit into exactly k equal parts:
+// no CTA crosses a unit boundary and nothing is merged mid-stream.  Several
+// streams (fills unknown to the host) use one CTA per SM.
+inline int attend_grid(const rkv_handle* h, int n_layers) {
+  const int sms = h->num_sms < kMaxCtas ? h->num_sms : kMaxCtas;
+  const int units = n_layers * h->sh.Hkv;
+  if (h->sh.S == 1 && units <= sms) return units * (sms / units);
+  return sms;
+}
 }  // namespace rkv

@@ -11,6 +11,23 @@
 
 namespace rkv {
 
+// Division by a runtime constant d >= 1 for 0 <= x < 2^31, by multiply-high
+// and shift (round-up reciprocal, the Granlund-Montgomery method).
+struct FastDiv {
+  uint32_t d, m, s;
+  static FastDiv make(uint32_t d_) {
+    FastDiv f;
+    f.d = d_;
+    f.s = 0;
+    while ((1ull << f.s) < d_) ++f.s;
+    f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << f.s) - d_)) / d_ + 1);
+    return f;
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t x) const {
+    return static_cast<uint32_t>((static_cast<uint64_t>(__umulhi(x, m)) + x) >> s);
+  }
+};
+
 // Geometry every kernel needs.
 struct Shape {
   int S, L, Hq, Hkv, G, D, W, NB;  // NB = W / TK
@@ -41,10 +58,9 @@ struct AppendParams {
   void* k_pool;
   void* v_pool;
   long long* log;          // nullable, [S][4]
-  int* tickets;            // [S]
   const float2* table;
   int c;                   // pairs appended this step
-  int rows_per_block;
+  FastDiv div_hkv, div_c;  // H_kv and c
 };
 
 struct RerotParams {
@@ -68,9 +84,10 @@ struct AttendParams {
   int R;                      // rows per unit = c * G
   int slot_floats;
   float scale_log2;           // softmax scale * log2(e)
+  int ns;                     // pipeline stages (set by the launcher)
 };
 
-cudaError_t launch_append(const AppendParams& p, int blocks_per_stream, cudaStream_t s);
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_rerotate(const RerotParams& p, int blocks_per_stream, cudaStream_t s);
 cudaError_t launch_set_state(StreamState* st, int s_idx, long long origin, int fill,
                              cudaStream_t s);

@@ -3,15 +3,15 @@
 //
 // Bookkeeping follows the flowchart of "Audio8 ASR Infinite: What It Actually
 // Takes to Listen Forever": a pair that does not fit makes the cache evict the
-// oldest pair and shift the sliding origin forward.  Every block of a stream
-// reads the old state, derives the same new state from it, scatters its rows,
-// and the last block of the stream to finish (atomic ticket) publishes the new
-// state; no block waits on another.
+// oldest pair and shift the sliding origin forward.
 #include "rkv_internal.h"
 
 namespace rkv {
 
 namespace {
+
+constexpr int APPEND_THREADS = 512;
+constexpr int APPEND_BATCH = 8;   // 16-byte chunks a thread has in flight
 
 // Four consecutive elements of a row, widened to f32.
 __device__ __forceinline__ void load4(const void* base, size_t i, bool bf16, float (&x)[4]) {
@@ -86,11 +86,16 @@ __device__ __forceinline__ void load_cs4(const float2* table, size_t row_off, in
 }  // namespace
 
 // ----------------------------------------------------------------------------
-// K0 + K1: bookkeeping and scatter of the new rows.  grid = (blocks_per_stream, S)
+// K0 + K1: bookkeeping and scatter of the new rows.  One CTA per stream
+// (grid = S): every thread reads the old state and derives the same new state
+// from it, the CTA scatters the stream's rows, and thread 0 publishes the new
+// state once the CTA is done, so the step costs one dependent round trip.
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+__global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendParams p) {
+  pdl_trigger();   // the attention launched next may start its prologue now
+  __shared__ int s_first_slot;
   const Shape& sh = p.sh;
-  const int s = blockIdx.y;
+  const int s = blockIdx.x;
   const StreamState st = p.st[s];
   const int c = p.c, W = sh.W, D = sh.D, Hkv = sh.Hkv;
   const bool ok = state_ok(st, W) && c >= 1 && c <= W &&
@@ -99,59 +104,104 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   const long long o2 = st.origin + e;
   const int n2 = st.fill + c - e;
   const long long first = st.origin + st.fill;
+  const int rows = sh.L * c * Hkv;                    // rows (l, j, g)
+  const bool bf = sh.bf16 != 0;
+  // Row -> (l, j, g) with row = (l * c + j) * Hkv + g.
+  auto split_row = [&](int row, int& l, int& j, int& g) {
+    const int lj = static_cast<int>(p.div_hkv.div(row));
+    g = row - lj * Hkv;
+    l = static_cast<int>(p.div_c.div(lj));
+    j = lj - l * c;
+  };
+  // One thread takes the 64-bit remainder: new pair j goes to slot
+  // first_slot + j (mod W).
+  if (threadIdx.x == 0) s_first_slot = ok ? static_cast<int>(first % W) : 0;
 
-  if (ok) {
-    const int total = sh.L * c * Hkv;                 // rows (l, j, g)
-    const int r0 = blockIdx.x * p.rows_per_block;
-    const int r1 = min(total, r0 + p.rows_per_block);
-    const int quads = D / 8;                          // 4 pairs per thread
-    const bool bf = sh.bf16 != 0;
-    for (int idx = threadIdx.x; idx < (r1 - r0) * quads; idx += blockDim.x) {
-      const int row = r0 + idx / quads;
+  if (ok && !sh.stored_rotated) {
+    // Pre-RoPE: a plain copy of each row in 16-byte chunks.  Each thread loads
+    // up to APPEND_BATCH chunks before storing any, so the loads of a pass
+    // overlap instead of paying one memory round trip each.
+    const int esz = bf ? 2 : 4;
+    const int lch = __ffs(D * esz / 16) - 1;          // log2(16-byte chunks per row)
+    const int total = (2 * rows) << lch;              // K rows, then V rows
+    bool first_pass = true;
+    for (int base = 0; base < total; base += APPEND_BATCH * blockDim.x) {
+      uint4 v[APPEND_BATCH];
+      int rr[APPEND_BATCH];
+#pragma unroll
+      for (int t = 0; t < APPEND_BATCH; ++t) {
+        const int idx = base + t * blockDim.x + threadIdx.x;
+        rr[t] = -1;
+        if (idx >= total) continue;
+        rr[t] = idx;
+        const int kvrow = idx >> lch, q = idx & ((1 << lch) - 1);
+        const int kv = kvrow >= rows;
+        int l, j, g;
+        split_row(kvrow - kv * rows, l, j, g);
+        const size_t src = ((((size_t)l * sh.S + s) * c + j) * Hkv + g) * D;
+        const uint8_t* from = static_cast<const uint8_t*>(kv ? p.v_new : p.k_new) + src * esz;
+        v[t] = __ldg(reinterpret_cast<const uint4*>(from) + q);
+      }
+      if (first_pass) {
+        __syncthreads();   // s_first_slot
+        first_pass = false;
+      }
+      const int first_slot = s_first_slot;
+#pragma unroll
+      for (int t = 0; t < APPEND_BATCH; ++t) {
+        if (rr[t] < 0) continue;
+        const int kvrow = rr[t] >> lch, q = rr[t] & ((1 << lch) - 1);
+        const int kv = kvrow >= rows;
+        int l, j, g;
+        split_row(kvrow - kv * rows, l, j, g);
+        const int slot = first_slot + j < W ? first_slot + j : first_slot + j - W;
+        const size_t dst = ((((size_t)s * sh.L + l) * Hkv + g) * W + slot) * D;
+        uint8_t* to = static_cast<uint8_t*>(kv ? p.v_pool : p.k_pool) + dst * esz;
+        reinterpret_cast<uint4*>(to)[q] = v[t];
+      }
+    }
+  } else if (ok) {
+    // Stored-rotated: keys are stored as R(p - origin') k, four pairs per step.
+    __syncthreads();   // s_first_slot
+    const int first_slot = s_first_slot;
+    const int quads = D / 8;
+    for (int idx = threadIdx.x; idx < rows * quads; idx += blockDim.x) {
+      const int row = idx / quads;
       const int i = (idx % quads) * 4;
-      const int g = row % Hkv;
-      const int j = (row / Hkv) % c;
-      const int l = row / (Hkv * c);
+      int l, j, g;
+      split_row(row, l, j, g);
       const long long pos = first + j;
-      const int slot = static_cast<int>(pos % W);
+      const int slot = first_slot + j < W ? first_slot + j : first_slot + j - W;
       const size_t src = ((((size_t)l * sh.S + s) * c + j) * Hkv + g) * D;
       const size_t dst = ((((size_t)s * sh.L + l) * Hkv + g) * W + slot) * D;
       float ka[4], kb[4], va[4], vb[4];
       load_pairs(p.k_new, src, i, D, sh.style, bf, ka, kb);
       load_pairs(p.v_new, src, i, D, sh.style, bf, va, vb);
-      if (sh.stored_rotated) {  // store R(pos - origin') k
-        float2 cs[4];
-        load_cs4(p.table, (size_t)(pos - o2) * (D / 2), i, cs);
-        rotate4(ka, kb, cs, 1.f);
-      }
+      float2 cs[4];
+      load_cs4(p.table, (size_t)(pos - o2) * (D / 2), i, cs);
+      rotate4(ka, kb, cs, 1.f);
       store_pairs(p.k_pool, dst, i, D, sh.style, bf, ka, kb);
       store_pairs(p.v_pool, dst, i, D, sh.style, bf, va, vb);
     }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const int old = atomicAdd(&p.tickets[s], 1);
-    if (old == static_cast<int>(gridDim.x) - 1) {
-      __threadfence();
-      StreamState ns = st;
-      if (ok) {
-        ns.origin = o2;
-        ns.fill = n2;
-        ns.pending = sh.stored_rotated ? e : 0;
-        ns.last_new = c;
-      } else if (ns.status == 0) {
-        ns.status = STATUS_DEVICE_STATE;
-      }
-      p.st[s] = ns;
-      if (p.log) {
-        long long* lg = p.log + 4 * (size_t)s;
-        lg[0] = ok ? o2 : st.origin;
-        lg[1] = ok ? n2 : st.fill;
-        lg[2] = ok ? e : -1;
-        lg[3] = ok ? first % W : -1;
-      }
-      p.tickets[s] = 0;
+    StreamState ns = st;
+    if (ok) {
+      ns.origin = o2;
+      ns.fill = n2;
+      ns.pending = sh.stored_rotated ? e : 0;
+      ns.last_new = c;
+    } else if (ns.status == 0) {
+      ns.status = STATUS_DEVICE_STATE;
+    }
+    p.st[s] = ns;
+    if (p.log) {
+      long long* lg = p.log + 4 * (size_t)s;
+      lg[0] = ok ? o2 : st.origin;
+      lg[1] = ok ? n2 : st.fill;
+      lg[2] = ok ? e : -1;
+      lg[3] = ok ? s_first_slot : -1;
     }
   }
 }
@@ -208,8 +258,8 @@ __global__ void set_state_kernel(StreamState* st, int s, long long origin, int f
   st[s] = ns;
 }
 
-cudaError_t launch_append(const AppendParams& p, int blocks_per_stream, cudaStream_t s) {
-  append_kernel<<<dim3(blocks_per_stream, p.sh.S), 256, 0, s>>>(p);
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
+  append_kernel<<<p.sh.S, APPEND_THREADS, 0, s>>>(p);
   return cudaGetLastError();
 }
 cudaError_t launch_rerotate(const RerotParams& p, int blocks_per_stream, cudaStream_t s) {
