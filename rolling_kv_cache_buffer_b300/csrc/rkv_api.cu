@@ -328,7 +328,8 @@ rkv_status rkv_set_stream_state(rkv_handle* h, int32_t s, int64_t origin, int32_
   if (!h || s < 0 || s >= h->sh.S || origin < 0 || fill < 0 || fill > h->sh.W)
     return RKV_ERR_INVALID_ARG;
   return cuda_status(
-      rkv::launch_set_state(h->state, s, origin, fill, static_cast<cudaStream_t>(stream)));
+      rkv::launch_set_state(h->state, s, origin, fill, static_cast<int>(origin % h->sh.W),
+                            static_cast<cudaStream_t>(stream)));
 }
 
 rkv_status rkv_get_stream_state(rkv_handle* h, int64_t* origins, int32_t* fills, int32_t* status,

@@ -27,7 +27,7 @@ struct UnitRef {
 __device__ __forceinline__ int stream_blocks(const AttendParams& p, int s) {
   const StreamState st = p.st[s];
   if (!state_ok(st, p.sh.W)) return 0;
-  return touched_blocks(static_cast<int>(st.origin % p.sh.W), st.fill, p.sh.NB);
+  return touched_blocks(st.ring, st.fill, p.sh.NB);
 }
 
 // pre[s] = first block of stream s in the call's list, pre[S] = total.  One
@@ -54,6 +54,57 @@ __device__ __forceinline__ void build_prefix(const AttendParams& p, int* pre) {
   if (threadIdx.x < 32) build_prefix_warp(p, pre, threadIdx.x);
 }
 
+// As build_prefix_warp, and also caches every stream's ring start a = origin
+// mod W (-1 for a stream whose state is not valid) and fill in shared memory,
+// so later unit lookups need no global load.
+__device__ __forceinline__ void build_prefix_cached(const AttendParams& p, int* pre, int* sa,
+                                                    int* sfill, int lane) {
+  const int per_unit = p.L_att * p.sh.Hkv;
+  int carry = 0;
+  if (lane == 0) pre[0] = 0;
+  for (int base = 0; base < p.sh.S; base += 32) {
+    const int s = base + lane;
+    int v = 0;
+    if (s < p.sh.S) {
+      const StreamState st = p.st[s];
+      const bool ok = state_ok(st, p.sh.W);
+      const int a = ok ? st.ring : -1;
+      sa[s] = a;
+      sfill[s] = ok ? st.fill : 0;
+      v = ok ? touched_blocks(a, st.fill, p.sh.NB) * per_unit : 0;
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += t;
+    }
+    if (s < p.sh.S) pre[s + 1] = carry + v;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+}
+
+// The unit holding block x of the call's list, from the cached stream data.
+__device__ __forceinline__ UnitRef unit_of_cached(int x, const AttendParams& p, const int* pre,
+                                                  const int* sa, const int* sfill) {
+  int lo = 0, hi = p.sh.S;  // pre[lo] <= x < pre[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid;
+  }
+  UnitRef u;
+  u.s = lo;
+  u.a = sa[lo];
+  u.fill = sfill[lo];
+  u.nb = touched_blocks(u.a, u.fill, p.sh.NB);
+  const int xs = x - pre[lo];
+  const int ul = xs / u.nb;
+  u.l = ul / p.sh.Hkv;
+  u.g = ul - u.l * p.sh.Hkv;
+  u.ustart = pre[lo] + ul * u.nb;
+  u.uend = u.ustart + u.nb;
+  return u;
+}
+
 __device__ __forceinline__ UnitRef unit_of(int x, const AttendParams& p, const int* pre) {
   int lo = 0, hi = p.sh.S;  // pre[lo] <= x < pre[hi]
   while (hi - lo > 1) {
@@ -63,7 +114,7 @@ __device__ __forceinline__ UnitRef unit_of(int x, const AttendParams& p, const i
   UnitRef u;
   u.s = lo;
   const StreamState st = p.st[lo];
-  u.a = static_cast<int>(st.origin % p.sh.W);
+  u.a = st.ring;
   u.fill = st.fill;
   u.nb = touched_blocks(u.a, u.fill, p.sh.NB);
   const int xs = x - pre[lo];
@@ -144,6 +195,24 @@ __device__ __forceinline__ void zero_empty_units(const AttendParams& p, int t, i
 }
 __device__ __forceinline__ void zero_empty_units(const AttendParams& p) {
   zero_empty_units(p, threadIdx.x, blockDim.x);
+}
+// As zero_empty_units, from the cached stream data.
+__device__ __forceinline__ void zero_empty_units_cached(const AttendParams& p, const int* sa,
+                                                        const int* sfill, int t, int nt) {
+  const int per_stream = p.L_att * p.sh.Hkv;
+  const int units = p.sh.S * per_stream;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int s = u / per_stream;
+    if (!(sa[s] >= 0 && sfill[s] == 0)) continue;
+    UnitRef ur;
+    ur.s = s;
+    ur.l = (u % per_stream) / p.sh.Hkv;
+    ur.g = u % p.sh.Hkv;
+    for (int row = 0; row < p.R; ++row) {
+      float* o = p.out + row_offset(p, ur, row);
+      for (int d = t; d < p.sh.D; d += nt) o[d] = 0.f;
+    }
+  }
 }
 
 // Segment end.  `mrg` holds NWARP warp partials of `wstride` floats, each

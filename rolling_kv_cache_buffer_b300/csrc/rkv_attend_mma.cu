@@ -52,6 +52,7 @@ constexpr int CONS_THREADS = NCW * 32;
 constexpr int MMA_MAX_STAGES = 16;
 constexpr int SMEM_LIMIT = 227 * 1024;        // opt-in shared memory per CTA
 constexpr int BAR_CONS = 1;                   // named barrier of the consumer warps
+constexpr int BAR_PREFIX = 2;                 // the producer warp's block prefix is ready
 
 constexpr int TKH = TK / 2;     // keys of a block each warp of a pair takes
 constexpr int NPAIR = NCW / 2;  // consumer warp pairs
@@ -70,12 +71,14 @@ struct MmaCfg {
   static constexpr int QSTR = D + 8;                      // padded query row (floats)
   static constexpr int OSTR = D + 4;                      // padded output row (floats)
   static constexpr int SLOT = 16 + 8 * OSTR;              // warp partial: m[8] l[8] o[8][OSTR]
-  // Bytes after the stages, without the per-stream prefix.
-  static constexpr int FIXED = FINE + 8 * QSTR * 4 + NCW * SLOT * 4 + 16;
+  // Bytes after the stages (the warp slots of a segment merge alias the
+  // stages), without the per-stream prefix: R(d) table, query rows, flags and
+  // the merge-done barrier.
+  static constexpr int FIXED = FINE + 8 * QSTR * 4 + 16 + 16;
 };
 
 __host__ __device__ constexpr size_t mma_smem_bytes(int stage, int fixed, int ns, int S) {
-  return 1024 + (size_t)ns * stage + (size_t)fixed + (size_t)ns * 16 + (size_t)(S + 1) * 4;
+  return 1024 + (size_t)ns * stage + (size_t)fixed + (size_t)ns * 16 + (size_t)(3 * S + 1) * 4;
 }
 
 // 16-byte chunk `grp` of key row `row` (0..TK-1) of a block tile: the tile is
@@ -155,13 +158,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   uint8_t* stages = smem;                                          // [NS][STAGE]
+  float* slots = reinterpret_cast<float*>(smem);                   // [NCW][SLOT], between segments
   uint8_t* fine = stages + (size_t)NS * C::STAGE;                  // [TK][D/2] (cos, sin)
   float* qs = reinterpret_cast<float*>(fine + C::FINE);            // [8][QSTR] raw query
-  float* slots = qs + 8 * QSTR;                                    // [NCW][SLOT] warp partials
-  int* flag = reinterpret_cast<int*>(slots + NCW * C::SLOT);       // ticket, abort, issued
-  uint64_t* full = reinterpret_cast<uint64_t*>(flag + 4);          // [NS]
+  int* flag = reinterpret_cast<int*>(qs + 8 * QSTR);               // ticket, abort, issued
+  uint64_t* mdone = reinterpret_cast<uint64_t*>(flag + 4);         // segment merged
+  uint64_t* full = mdone + 2;                                      // [NS]
   uint64_t* empty = full + NS;                                     // [NS]
-  int* pre = reinterpret_cast<int*>(empty + NS);                   // [S+1]
+  int* pre = reinterpret_cast<int*>(empty + NS);                   // [S+1] block prefix
+  int* sa = pre + p.sh.S + 1;                                      // [S] origin mod W
+  int* sfill = sa + p.sh.S;                                        // [S] fill
   volatile int* abort_flag = flag + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -172,6 +178,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       mbar_init(smem_u32(full + i), 1);
       mbar_init(smem_u32(empty + i), 2);   // both warps of the pair that takes the block
     }
+    mbar_init(smem_u32(mdone), 1);
     fence_mbar_init();
     flag[1] = 0;
     flag[2] = 0;
@@ -186,9 +193,25 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       *reinterpret_cast<float4*>(fine + d * HALF * 8 + fine_chunk<D>(d, k)) = v;
     }
   }
+  // The queries are not written by the append kernel that may still run: bring
+  // this CTA's share of them into L2 now.
+  {
+    const size_t qbytes = (size_t)p.L_att * p.sh.S * p.c * p.sh.Hq * D * (p.sh.q_bf16 ? 2 : 4);
+    const size_t lines = (qbytes + 127) / 128;
+    const size_t l0 = lines * blockIdx.x / gridDim.x, l1 = lines * (blockIdx.x + 1) / gridDim.x;
+    for (size_t l = l0 + tid; l < l1; l += blockDim.x)
+      prefetch_l2(static_cast<const uint8_t*>(p.q) + l * 128);
+  }
   pdl_wait();   // from here on: stream state, pools, queries, outputs
-  if (warp == 1) build_prefix_warp(p, pre, lane);
-  __syncthreads();
+  // Warp 0 builds the block prefix and starts streaming at once; the
+  // consumers pick the prefix up from the named barrier.
+  if (warp == 0) {
+    build_prefix_cached(p, pre, sa, sfill, lane);
+    __syncwarp();
+    named_bar_arrive(BAR_PREFIX, MMA_THREADS);
+  } else {
+    named_bar_sync(BAR_PREFIX, MMA_THREADS);
+  }
   const int T = pre[p.sh.S];
   const int P = min(static_cast<int>(gridDim.x), T);
   const int b = static_cast<int>(blockIdx.x);
@@ -197,11 +220,17 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      int stage = 0, round = 0, issued = 0;
+      int stage = 0, round = 0, issued = 0, seg = 0;
       bool stop = false;
-      for (int x = rb; x < re && !stop;) {
+      for (int x = rb; x < re && !stop; ++seg) {
         // Per unit segment: the unit, then the block geometry advanced per block.
-        const UnitRef u = unit_of(x, p, pre);
+        const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
+        // The merge of the previous segment uses the stage memory: wait for it.
+        if (seg > 0 && !mbar_wait_or_abort(smem_u32(mdone), (seg - 1) & 1, abort_flag)) {
+          *abort_flag = 1;
+          p.st[u.s].status = STATUS_DEVICE_STATE;
+          break;
+        }
         const int x1 = min(u.uend, re);
         const int ug = static_cast<int>(unit_index(p, u));
         int blk = touched_block(u.a, x - u.ustart, NB);
@@ -250,7 +279,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     // ------------------------------------------------------------------ consumers
     const int cw = warp - 1, ct = tid - 32;
     const int g = lane >> 2, cq = lane & 3;   // mma fragment coordinates
-    zero_empty_units(p, ct, CONS_THREADS);
+    zero_empty_units_cached(p, sa, sfill, ct, CONS_THREADS);
     // Raw query of a unit into `qs` (rows >= G are zero).
     auto load_query = [&](const UnitRef& u) {
       for (int idx = ct; idx < 8 * D; idx += CONS_THREADS) {
@@ -258,7 +287,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         qs[h * QSTR + d] = h < G ? load_elem(p.q, row_offset(p, u, h) + d, p.sh.q_bf16) : 0.f;
       }
     };
-    if (rb < re) load_query(unit_of(rb, p, pre));
+    if (rb < re) load_query(unit_of_cached(rb, p, pre, sa, sfill));
     named_bar_sync(BAR_CONS, CONS_THREADS);
 
     // Dims of the thread's A-fragment elements: k-block kb, j in {0,1,2,3}:
@@ -271,7 +300,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     int jb = pi, stage = pi, round = 0;   // the pair's next block and its stage (NS >= NPAIR)
     bool dead = false;
     for (int x = rb; x < re;) {
-      const UnitRef u = unit_of(x, p, pre);
+      const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
       const int x1 = min(u.uend, re);
       const int rq = u.fill - 1;
       // The next segment's query: loaded now, stored once this segment is done.
@@ -279,7 +308,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       constexpr int QPT = (8 * D + CONS_THREADS - 1) / CONS_THREADS;
       float nq[QPT];
       if (has_next) {
-        const UnitRef un = unit_of(x1, p, pre);
+        const UnitRef un = unit_of_cached(x1, p, pre, sa, sfill);
 #pragma unroll
         for (int t = 0; t < QPT; ++t) {
           const int idx = ct + t * CONS_THREADS, h = idx / D, d = idx % D;
@@ -350,6 +379,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         const int wrap_at = W - r0;      // keys d >= wrap_at sit at r0 + d - W
         const bool wraps = wrap_at < TK;
         const bool allvalid = wraps ? (u.fill == W) : (r0 + TK <= u.fill);
+        const bool plain = allvalid && !wraps;   // every key visible, one base
         {
           const int st_i = stage, st_r = round;
           // A pair only waits on every NPAIR-th stage, so it may reach one
@@ -440,18 +470,30 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 }
               }
             }
-            float accs[4] = {0.f, 0.f, 0.f, 0.f};
+            // Two interleaved accumulation chains (even and odd k-blocks).
+            float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int kb = 0; kb < NKB; ++kb)
-              mma_bf16(accs, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kf[2 * kb],
+            for (int kb = 0; kb < NKB; kb += 2) {
+              mma_bf16(acc0, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kf[2 * kb],
                        kf[2 * kb + 1]);
+              mma_bf16(acc1, qa[kb + 1][0], qa[kb + 1][1], qa[kb + 1][2], qa[kb + 1][3],
+                       kf[2 * kb + 2], kf[2 * kb + 3]);
+            }
+            float accs[4];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int d = hh * TKH + nb * 8 + 2 * cq + e;
-              const bool wr = ROTK && d >= wrap_at;
-              const int r = r0 + d - (d >= wrap_at ? W : 0);
-              const bool vis = allvalid || r < u.fill;
-              s[nb][e] = vis ? (wr ? accs[2 + e] : accs[e]) * p.scale_log2 : NEG_BIG;
+            for (int i = 0; i < 4; ++i) accs[i] = acc0[i] + acc1[i];
+            if (plain) {
+              s[nb][0] = accs[0] * p.scale_log2;
+              s[nb][1] = accs[1] * p.scale_log2;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int d = hh * TKH + nb * 8 + 2 * cq + e;
+                const bool wr = ROTK && d >= wrap_at;
+                const int r = r0 + d - (d >= wrap_at ? W : 0);
+                const bool vis = allvalid || r < u.fill;
+                s[nb][e] = vis ? (wr ? accs[2 + e] : accs[e]) * p.scale_log2 : NEG_BIG;
+              }
             }
           }
           // ---- online softmax for head g (the 4 lanes of quad g) ----
@@ -490,11 +532,20 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
               mhi = (ok(d0 + 8) ? 0x0000ffffu : 0u) | (ok(d0 + 9) ? 0xffff0000u : 0u);
             }
             const int vrow = hh * TKH + ((lane >> 4) << 3) + (lane & 7);
+            if (allvalid) {
 #pragma unroll
-            for (int mt = 0; mt < NKB; ++mt) {
-              uint32_t v0, v1, v2, v3;
-              ldsm_x4_t(vt_s + swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
-              mma_bf16(o[mt], v0 & mlo, v1 & mlo, v2 & mhi, v3 & mhi, b0, b1);
+              for (int mt = 0; mt < NKB; ++mt) {
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_t(vt_s + swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
+                mma_bf16(o[mt], v0, v1, v2, v3, b0, b1);
+              }
+            } else {
+#pragma unroll
+              for (int mt = 0; mt < NKB; ++mt) {
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_t(vt_s + swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
+                mma_bf16(o[mt], v0 & mlo, v1 & mlo, v2 & mhi, v3 & mhi, b0, b1);
+              }
             }
           }
           __syncwarp();
@@ -506,8 +557,11 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       }
 
       // ---- segment end: merge the consumer warps (rows = heads) ----
-      // Each warp leaves (m, l, o) of its blocks in its slot; after one barrier
+      // Once every consumer is done with the stages (the producer issues
+      // nothing more until the merge is over), each warp leaves (m, l, o) of
+      // its blocks in its slot, in the stage memory; after one more barrier
       // every thread combines the NCW slots for its output elements.
+      named_bar_sync(BAR_CONS, CONS_THREADS);
       {
         float lsum = l_run;
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
@@ -588,14 +642,19 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
           if (ct == 0) p.unit_tickets[unit_index(p, u)] = 0;
         }
       }
+      // The slots' generic-proxy accesses come before the producer's next
+      // asynchronous copies into the same memory.
+      fence_proxy_async();
       named_bar_sync(BAR_CONS, CONS_THREADS);
+      if (ct == 0) mbar_arrive(smem_u32(mdone));
       x = x1;
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    // No CTA exits with a copy still in flight into its shared memory: wait
-    // (bounded) for the last NS stages this CTA issued.
+  if (tid == 0 && *abort_flag) {
+    // Normally every issued stage was waited on by its consumers.  After an
+    // abort, no CTA exits with a copy still in flight into its shared memory:
+    // wait (bounded) for the last NS stages this CTA issued.
     const int issued = flag[2];
     for (int j = max(0, issued - NS); j < issued; ++j)
       mbar_wait(smem_u32(full + (j % NS)), (j / NS) & 1);

@@ -22,7 +22,8 @@ struct StreamState {
   int status;     // 0, or an rkv_status code (sticky until rkv_set_stream_state)
   int pending;    // stored-rotated: evictions of the last append not yet re-based
   int last_new;   // pairs inserted by the last append
-  int pad0, pad1;
+  int ring;       // origin mod W (slot of the oldest pair), kept by every state writer
+  int pad1;
 };
 static_assert(sizeof(StreamState) == 32, "state layout");
 
@@ -89,6 +90,15 @@ __device__ __forceinline__ void pdl_trigger() {
 // Named barrier `id` over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Arrival on named barrier `id` without waiting (its writes become visible to
+// the threads that complete the barrier with named_bar_sync).
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Hint: bring the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 // Shared-memory float atomic add (no return value).
 __device__ __forceinline__ void red_add_shared(float* addr, float v) {
@@ -183,7 +193,8 @@ __device__ __forceinline__ int pair_d2(int i, int D, int style) {
 }
 
 __device__ __forceinline__ int state_ok(const StreamState& s, int W) {
-  return s.status == 0 && s.origin >= 0 && s.fill >= 0 && s.fill <= W;
+  return s.status == 0 && s.origin >= 0 && s.fill >= 0 && s.fill <= W && s.ring >= 0 &&
+         s.ring < W;
 }
 
 // ----------------------------------------------------------------------------

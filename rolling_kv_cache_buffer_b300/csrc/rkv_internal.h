@@ -89,7 +89,7 @@ struct AttendParams {
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_rerotate(const RerotParams& p, int blocks_per_stream, cudaStream_t s);
-cudaError_t launch_set_state(StreamState* st, int s_idx, long long origin, int fill,
+cudaError_t launch_set_state(StreamState* st, int s_idx, long long origin, int fill, int ring,
                              cudaStream_t s);
 
 // Attention launchers; `grid` = persistent CTAs.  Return cudaErrorNotSupported

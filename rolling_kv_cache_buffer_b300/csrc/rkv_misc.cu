@@ -93,7 +93,6 @@ __device__ __forceinline__ void load_cs4(const float2* table, size_t row_off, in
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendParams p) {
   pdl_trigger();   // the attention launched next may start its prologue now
-  __shared__ int s_first_slot;
   const Shape& sh = p.sh;
   const int s = blockIdx.x;
   const StreamState st = p.st[s];
@@ -113,9 +112,8 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
     l = static_cast<int>(p.div_c.div(lj));
     j = lj - l * c;
   };
-  // One thread takes the 64-bit remainder: new pair j goes to slot
-  // first_slot + j (mod W).
-  if (threadIdx.x == 0) s_first_slot = ok ? static_cast<int>(first % W) : 0;
+  // New pair j goes to slot first_slot + j (mod W); the state keeps origin mod W.
+  const int first_slot = st.ring + st.fill < W ? st.ring + st.fill : st.ring + st.fill - W;
 
   if (ok && !sh.stored_rotated) {
     // Pre-RoPE: a plain copy of each row in 16-byte chunks.  Each thread loads
@@ -124,7 +122,6 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
     const int esz = bf ? 2 : 4;
     const int lch = __ffs(D * esz / 16) - 1;          // log2(16-byte chunks per row)
     const int total = (2 * rows) << lch;              // K rows, then V rows
-    bool first_pass = true;
     for (int base = 0; base < total; base += APPEND_BATCH * blockDim.x) {
       uint4 v[APPEND_BATCH];
       int rr[APPEND_BATCH];
@@ -142,11 +139,6 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
         const uint8_t* from = static_cast<const uint8_t*>(kv ? p.v_new : p.k_new) + src * esz;
         v[t] = __ldg(reinterpret_cast<const uint4*>(from) + q);
       }
-      if (first_pass) {
-        __syncthreads();   // s_first_slot
-        first_pass = false;
-      }
-      const int first_slot = s_first_slot;
 #pragma unroll
       for (int t = 0; t < APPEND_BATCH; ++t) {
         if (rr[t] < 0) continue;
@@ -162,8 +154,6 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
     }
   } else if (ok) {
     // Stored-rotated: keys are stored as R(p - origin') k, four pairs per step.
-    __syncthreads();   // s_first_slot
-    const int first_slot = s_first_slot;
     const int quads = D / 8;
     for (int idx = threadIdx.x; idx < rows * quads; idx += blockDim.x) {
       const int row = idx / quads;
@@ -190,6 +180,7 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
     if (ok) {
       ns.origin = o2;
       ns.fill = n2;
+      ns.ring = st.ring + e < W ? st.ring + e : st.ring + e - W;
       ns.pending = sh.stored_rotated ? e : 0;
       ns.last_new = c;
     } else if (ns.status == 0) {
@@ -201,7 +192,7 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
       lg[0] = ok ? o2 : st.origin;
       lg[1] = ok ? n2 : st.fill;
       lg[2] = ok ? e : -1;
-      lg[3] = ok ? s_first_slot : -1;
+      lg[3] = ok ? first_slot : -1;
     }
   }
 }
@@ -230,7 +221,7 @@ __global__ void __launch_bounds__(256) rerotate_kernel(const RerotParams p) {
       const int i = (idx % quads) * 4;
       const int r = row % nr;
       const int lg = row / nr;                          // l * Hkv + g
-      const int slot = static_cast<int>((st.origin + r) % W);
+      const int slot = st.ring + r < W ? st.ring + r : st.ring + r - W;
       const size_t base = (((size_t)s * sh.L * Hkv + lg) * W + slot) * D;
       float a[4], b[4];
       float2 cs[4];
@@ -251,10 +242,11 @@ __global__ void __launch_bounds__(256) rerotate_kernel(const RerotParams p) {
   }
 }
 
-__global__ void set_state_kernel(StreamState* st, int s, long long origin, int fill) {
+__global__ void set_state_kernel(StreamState* st, int s, long long origin, int fill, int ring) {
   StreamState ns{};
   ns.origin = origin;
   ns.fill = fill;
+  ns.ring = ring;
   st[s] = ns;
 }
 
@@ -266,9 +258,9 @@ cudaError_t launch_rerotate(const RerotParams& p, int blocks_per_stream, cudaStr
   rerotate_kernel<<<dim3(blocks_per_stream, p.sh.S), 256, 0, s>>>(p);
   return cudaGetLastError();
 }
-cudaError_t launch_set_state(StreamState* st, int s_idx, long long origin, int fill,
+cudaError_t launch_set_state(StreamState* st, int s_idx, long long origin, int fill, int ring,
                              cudaStream_t s) {
-  set_state_kernel<<<1, 1, 0, s>>>(st, s_idx, origin, fill);
+  set_state_kernel<<<1, 1, 0, s>>>(st, s_idx, origin, fill, ring);
   return cudaGetLastError();
 }
 
