@@ -148,11 +148,6 @@ std::vector<float2> make_table(const Shape& s, double theta) {
   return t;
 }
 
-bool use_mma(const rkv_handle* h, int c) {
-  if (h->cfg.attend_impl == RKV_ATTEND_FMA || !h->has_map4) return false;
-  return rkv::attend_mma_supported(h->sh, c);
-}
-
 }  // namespace
 
 extern "C" {
@@ -293,17 +288,9 @@ rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_be
   p.scale_log2 = h->scale * 1.4426950408889634f;
   const int grid = rkv::attend_grid(h, n_layers);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (use_mma(h, n_q)) {
-    e = rkv::launch_attend_mma(p, h->tmK4, h->tmV4, grid, s);
-  } else {
-    if (h->cfg.attend_impl == RKV_ATTEND_MMA) return RKV_ERR_UNSUPPORTED;
-    if (p.R > 16) return RKV_ERR_UNSUPPORTED;
-    e = rkv::launch_attend_fma(p, h->tmK, h->tmV, grid, s);
-  }
-  if (e == cudaErrorNotSupported) return RKV_ERR_UNSUPPORTED;
-  h->last_launches = 1;
-  return cuda_status(e);
+  const rkv_status st = rkv::launch_attend_any(h, p, grid, s);
+  if (st == RKV_OK) h->last_launches = 1;
+  return st;
 }
 
 rkv_status rkv_rebase(rkv_handle* h, void* stream) {

@@ -36,7 +36,7 @@
 #include <climits>
 #include <type_traits>
 
-#include "rkv_attend_common.cuh"
+#include "rkv_attend_pipe.cuh"
 
 #ifndef RKV_MMA_NCW
 #define RKV_MMA_NCW 8
@@ -50,7 +50,6 @@ constexpr int NCW = RKV_MMA_NCW;              // consumer warps
 constexpr int MMA_THREADS = (NCW + 1) * 32;   // + the producer warp
 constexpr int CONS_THREADS = NCW * 32;
 constexpr int MMA_MAX_STAGES = 16;
-constexpr int SMEM_LIMIT = 227 * 1024;        // opt-in shared memory per CTA
 constexpr int BAR_CONS = 1;                   // named barrier of the consumer warps
 constexpr int BAR_PREFIX = 2;                 // the producer warp's block prefix is ready
 
@@ -58,16 +57,11 @@ constexpr int TKH = TK / 2;     // keys of a block each warp of a pair takes
 constexpr int NPAIR = NCW / 2;  // consumer warp pairs
 
 template <int D, bool ROTK>
-struct MmaCfg {
-  static constexpr int HALF = D / 2;
-  static constexpr int TILE = TK * D * 2;                 // bf16 K (or V) block tile
-  static constexpr int NBOX = D / 64;                     // 128-byte boxes per row
-  static constexpr int TROW = ROTK ? HALF * 8 : 0;        // one (cos, sin) row
-  static constexpr int STAGE = ((2 * TILE + 2 * TROW + 1023) / 1024) * 1024;
+struct MmaCfg : PipeCfg<D, ROTK> {
+  using PipeCfg<D, ROTK>::FINE;
   static constexpr int NGRP = D / 8;                      // 8-dim groups
   static constexpr int NKB = D / 16;                      // k-blocks of the QK product
   static constexpr int HG = NGRP / 2;
-  static constexpr int FINE = ROTK ? TK * HALF * 8 : 0;   // R(d) table, d < TK
   static constexpr int QSTR = D + 8;                      // padded query row (floats)
   static constexpr int OSTR = D + 4;                      // padded output row (floats)
   static constexpr int SLOT = 16 + 8 * OSTR;              // warp partial: m[8] l[8] o[8][OSTR]
@@ -79,25 +73,6 @@ struct MmaCfg {
 
 __host__ __device__ constexpr size_t mma_smem_bytes(int stage, int fixed, int ns, int S) {
   return 1024 + (size_t)ns * stage + (size_t)fixed + (size_t)ns * 16 + (size_t)(3 * S + 1) * 4;
-}
-
-// 16-byte chunk `grp` of key row `row` (0..TK-1) of a block tile: the tile is
-// D/64 boxes of TK rows x 128 bytes, 128-byte swizzled.
-__device__ __forceinline__ uint32_t swz(int row, int grp) {
-  const int box = grp >> 3, cq = grp & 7;
-  return static_cast<uint32_t>(box * (TK * 128) + row * 128 + ((cq ^ (row & 7)) << 4));
-}
-// Fine table: row d (0..TK-1) holds the rotation R(d) for every pair; 16-byte
-// chunk k holds pairs 2k and 2k+1.  The chunk sits at position
-// k ^ ((d mod NCH/4) * 4) of its row (NCH = D/4 chunks per row), so the two
-// keys that one 8-lane phase of a 128-bit load reads (rows d, d+1, same k)
-// fall into different halves of the 128-byte bank window.  Split-half chunks
-// are (cos_2k, cos_2k+1, sin_2k, sin_2k+1), interleaved ones
-// (cos_2k, sin_2k, cos_2k+1, sin_2k+1).
-template <int D>
-__device__ __forceinline__ uint32_t fine_chunk(int d, int k) {
-  constexpr int NCH = D / 4;
-  return static_cast<uint32_t>((k ^ ((d & (NCH / 4 - 1)) << 2)) << 4);
 }
 
 __device__ __forceinline__ void rot(float& x, float& y, float c, float s) {
@@ -184,24 +159,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     flag[2] = 0;
   }
   if constexpr (ROTK) {
-    for (int idx = tid - 32; idx >= 0 && idx < TK * HALF / 2; idx += CONS_THREADS) {
-      const int d = idx / (HALF / 2), k = idx % (HALF / 2);
-      const float2 a = __ldg(p.table + (size_t)d * HALF + 2 * k);
-      const float2 c = __ldg(p.table + (size_t)d * HALF + 2 * k + 1);
-      const float4 v = STYLE == 0 ? make_float4(a.x, c.x, a.y, c.y)
-                                  : make_float4(a.x, a.y, c.x, c.y);
-      *reinterpret_cast<float4*>(fine + d * HALF * 8 + fine_chunk<D>(d, k)) = v;
-    }
+    if (warp > 0) load_fine<D, STYLE>(p, fine, tid - 32, CONS_THREADS);
   }
-  // The queries are not written by the append kernel that may still run: bring
-  // this CTA's share of them into L2 now.
-  {
-    const size_t qbytes = (size_t)p.L_att * p.sh.S * p.c * p.sh.Hq * D * (p.sh.q_bf16 ? 2 : 4);
-    const size_t lines = (qbytes + 127) / 128;
-    const size_t l0 = lines * blockIdx.x / gridDim.x, l1 = lines * (blockIdx.x + 1) / gridDim.x;
-    for (size_t l = l0 + tid; l < l1; l += blockDim.x)
-      prefetch_l2(static_cast<const uint8_t*>(p.q) + l * 128);
-  }
+  prefetch_queries(p, D);
   pdl_wait();   // from here on: stream state, pools, queries, outputs
   // Warp 0 builds the block prefix and starts streaming at once; the
   // consumers pick the prefix up from the named barrier.
@@ -219,61 +179,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0, round = 0, issued = 0, seg = 0;
-      bool stop = false;
-      for (int x = rb; x < re && !stop; ++seg) {
-        // Per unit segment: the unit, then the block geometry advanced per block.
-        const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
-        // The merge of the previous segment uses the stage memory: wait for it.
-        if (seg > 0 && !mbar_wait_or_abort(smem_u32(mdone), (seg - 1) & 1, abort_flag)) {
-          *abort_flag = 1;
-          p.st[u.s].status = STATUS_DEVICE_STATE;
-          break;
-        }
-        const int x1 = min(u.uend, re);
-        const int ug = static_cast<int>(unit_index(p, u));
-        int blk = touched_block(u.a, x - u.ustart, NB);
-        int r0 = blk * TK - u.a;
-        if (r0 < 0) r0 += W;
-        for (; x < x1; ++x) {
-          if (*abort_flag) { stop = true; break; }
-          if (round > 0 &&
-              !mbar_wait_or_abort(smem_u32(empty + stage), (round - 1) & 1, abort_flag)) {
-            *abort_flag = 1;
-            p.st[u.s].status = STATUS_DEVICE_STATE;
-            stop = true;
-            break;
-          }
-          const uint32_t bar = smem_u32(full + stage);
-          const uint32_t dst = smem_u32(stages + (size_t)stage * C::STAGE);
-          int mA = 0;
-          bool wraps = false;
-          uint32_t bytes = 2 * TILE;
-          if constexpr (ROTK) {
-            mA = u.fill - 1 - r0;
-            wraps = W - r0 < TK;
-            bytes += wraps ? 2 * C::TROW : C::TROW;
-          }
-          mbar_arrive_expect_tx(bar, bytes);
-          // One box per tile: {64 elements, TK rows, the D/64 row halves, one unit}.
-          tma_load_4d(dst, &tmK, 0, blk * TK, 0, ug, bar);
-          tma_load_4d(dst + TILE, &tmV, 0, blk * TK, 0, ug, bar);
-          if constexpr (ROTK) {
-            bulk_load(dst + 2 * TILE, p.table + (size_t)(mA < 0 ? -mA : mA) * HALF, C::TROW, bar);
-            if (wraps)
-              bulk_load(dst + 2 * TILE + C::TROW, p.table + (size_t)(mA + W) * HALF, C::TROW,
-                        bar);
-          }
-          ++issued;
-          if (++stage == NS) { stage = 0; ++round; }
-          if (++blk == NB) blk = 0;
-          r0 += TK;
-          if (r0 >= W) r0 -= W;
-        }
-      }
-      flag[2] = issued;
-    }
+    if (lane == 0)
+      flag[2] = produce<D, ROTK, QUERY_BASES>(p, &tmK, &tmV, stages, full, empty, mdone, pre, sa,
+                                              sfill, rb, re, abort_flag);
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ consumers
@@ -445,7 +353,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             const int krow = hh * TKH + nb * 8 + (lane & 7);
 #pragma unroll
             for (int g4 = 0; g4 < NGRP; g4 += 4)
-              ldsm_x4(kt_s + swz(krow, g4 + (lane >> 3)), kf[g4], kf[g4 + 1], kf[g4 + 2],
+              ldsm_x4(kt_s + tile_swz(krow, g4 + (lane >> 3)), kf[g4], kf[g4 + 1], kf[g4 + 2],
                       kf[g4 + 3]);
             if constexpr (ROTK) {
               const int dk = hh * TKH + nb * 8 + g;   // this thread's key within the block
@@ -536,14 +444,14 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
 #pragma unroll
               for (int mt = 0; mt < NKB; ++mt) {
                 uint32_t v0, v1, v2, v3;
-                ldsm_x4_t(vt_s + swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
+                ldsm_x4_t(vt_s + tile_swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
                 mma_bf16(o[mt], v0, v1, v2, v3, b0, b1);
               }
             } else {
 #pragma unroll
               for (int mt = 0; mt < NKB; ++mt) {
                 uint32_t v0, v1, v2, v3;
-                ldsm_x4_t(vt_s + swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
+                ldsm_x4_t(vt_s + tile_swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
                 mma_bf16(o[mt], v0 & mlo, v1 & mlo, v2 & mhi, v3 & mhi, b0, b1);
               }
             }

@@ -1,0 +1,151 @@
+// rkv_attend_pipe.cuh -- the streaming side shared by the tensor-core
+// attention kernels: stage geometry, the producer warp and the fine R(d) table.
+//
+// One persistent CTA per SM.  Lane 0 of warp 0 walks the CTA's share of the
+// block list (rkv_attend_common.cuh) and, per block of TK slots, fills one
+// shared-memory stage: the K and V tiles as one 4-D TMA box each (128-byte
+// swizzle) and one or two (cos, sin) rows of the RoPE table.  Stages form a
+// ring with a full barrier (copies landed) and an empty barrier (consumers done)
+// each.  Between unit segments the producer waits for the consumers' merge,
+// which reuses the stage memory.
+#pragma once
+
+#include "rkv_attend_common.cuh"
+
+namespace rkv {
+
+constexpr int SMEM_LIMIT = 227 * 1024;   // opt-in shared memory per CTA
+
+template <int D, bool ROTK>
+struct PipeCfg {
+  static constexpr int HALF = D / 2;
+  static constexpr int TILE = TK * D * 2;                 // bf16 K (or V) block tile
+  static constexpr int TROW = ROTK ? HALF * 8 : 0;        // one (cos, sin) row
+  static constexpr int STAGE = ((2 * TILE + 2 * TROW + 1023) / 1024) * 1024;
+  static constexpr int FINE = ROTK ? TK * HALF * 8 : 0;   // R(d) table, d < TK
+};
+
+// Which table rows a block's stage carries (r0 = re-based position of the
+// block's first slot, fill = the stream's fill):
+//   QUERY_BASES: row |fill-1-r0| (the query's offset from the block; the
+//     consumer flips the sine when negative) and, when the block holds the
+//     ring's end, row fill-1-r0+W;
+//   KEY_BASES: row r0 and, when the block holds the ring's end, row W-r0 (the
+//     consumer flips its sine to get R(r0-W)).
+enum TableRows { QUERY_BASES = 0, KEY_BASES = 1 };
+
+// 16-byte chunk `grp` of key row `row` (0..TK-1) of a block tile: the tile is
+// D/64 boxes of TK rows x 128 bytes, 128-byte swizzled.
+__device__ __forceinline__ uint32_t tile_swz(int row, int grp) {
+  const int box = grp >> 3, cq = grp & 7;
+  return static_cast<uint32_t>(box * (TK * 128) + row * 128 + ((cq ^ (row & 7)) << 4));
+}
+
+// Fine table: row d (0..TK-1) holds the rotation R(d) for every pair; 16-byte
+// chunk k holds pairs 2k and 2k+1.  The chunk sits at position
+// k ^ ((d mod NCH/4) * 4) of its row (NCH = D/4 chunks per row), so the two
+// keys that one 8-lane phase of a 128-bit load reads (rows d, d+1, same k)
+// fall into different halves of the 128-byte bank window.  Split-half chunks
+// are (cos_2k, cos_2k+1, sin_2k, sin_2k+1), interleaved ones
+// (cos_2k, sin_2k, cos_2k+1, sin_2k+1).
+template <int D>
+__device__ __forceinline__ uint32_t fine_chunk(int d, int k) {
+  constexpr int NCH = D / 4;
+  return static_cast<uint32_t>((k ^ ((d & (NCH / 4 - 1)) << 2)) << 4);
+}
+
+// Threads t0, t0+nt, ... fill the fine table from rows 0..TK-1 of the global
+// (cos, sin) table.
+template <int D, int STYLE>
+__device__ __forceinline__ void load_fine(const AttendParams& p, uint8_t* fine, int t0, int nt) {
+  constexpr int HALF = D / 2;
+  for (int idx = t0; idx < TK * HALF / 2; idx += nt) {
+    const int d = idx / (HALF / 2), k = idx % (HALF / 2);
+    const float2 a = __ldg(p.table + (size_t)d * HALF + 2 * k);
+    const float2 c = __ldg(p.table + (size_t)d * HALF + 2 * k + 1);
+    const float4 v = STYLE == 0 ? make_float4(a.x, c.x, a.y, c.y)
+                                : make_float4(a.x, a.y, c.x, c.y);
+    *reinterpret_cast<float4*>(fine + d * HALF * 8 + fine_chunk<D>(d, k)) = v;
+  }
+}
+
+// Threads of the CTA bring its share of the queries into L2 (the queries are
+// not written by the append kernel that may still be running).
+__device__ __forceinline__ void prefetch_queries(const AttendParams& p, int D) {
+  const size_t qbytes = (size_t)p.L_att * p.sh.S * p.c * p.sh.Hq * D * (p.sh.q_bf16 ? 2 : 4);
+  const size_t lines = (qbytes + 127) / 128;
+  const size_t l0 = lines * blockIdx.x / gridDim.x, l1 = lines * (blockIdx.x + 1) / gridDim.x;
+  for (size_t l = l0 + threadIdx.x; l < l1; l += blockDim.x)
+    prefetch_l2(static_cast<const uint8_t*>(p.q) + l * 128);
+}
+
+// The producer loop, run by lane 0 of warp 0 over blocks [rb, re).  Returns
+// the number of stages it filled.  Stops early (status set, *abort raised) if
+// a wait runs out.
+template <int D, bool ROTK, int ROWS>
+__device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap* tmK,
+                                       const CUtensorMap* tmV, uint8_t* stages, uint64_t* full,
+                                       uint64_t* empty, uint64_t* mdone, const int* pre,
+                                       const int* sa, const int* sfill, int rb, int re,
+                                       volatile int* abort_flag) {
+  using C = PipeCfg<D, ROTK>;
+  const int W = p.sh.W, NB = p.sh.NB, NS = p.ns;
+  int stage = 0, round = 0, issued = 0, seg = 0;
+  bool stop = false;
+  for (int x = rb; x < re && !stop; ++seg) {
+    // Per unit segment: the unit, then the block geometry advanced per block.
+    const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
+    // The merge of the previous segment uses the stage memory: wait for it.
+    if (seg > 0 && !mbar_wait_or_abort(smem_u32(mdone), (seg - 1) & 1, abort_flag)) {
+      *abort_flag = 1;
+      p.st[u.s].status = STATUS_DEVICE_STATE;
+      break;
+    }
+    const int x1 = min(u.uend, re);
+    const int ug = static_cast<int>(unit_index(p, u));
+    int blk = touched_block(u.a, x - u.ustart, NB);
+    int r0 = blk * TK - u.a;
+    if (r0 < 0) r0 += W;
+    for (; x < x1; ++x) {
+      if (*abort_flag) { stop = true; break; }
+      if (round > 0 &&
+          !mbar_wait_or_abort(smem_u32(empty + stage), (round - 1) & 1, abort_flag)) {
+        *abort_flag = 1;
+        p.st[u.s].status = STATUS_DEVICE_STATE;
+        stop = true;
+        break;
+      }
+      const uint32_t bar = smem_u32(full + stage);
+      const uint32_t dst = smem_u32(stages + (size_t)stage * C::STAGE);
+      const bool wraps = W - r0 < TK;
+      uint32_t bytes = 2 * C::TILE;
+      if constexpr (ROTK) bytes += wraps ? 2 * C::TROW : C::TROW;
+      mbar_arrive_expect_tx(bar, bytes);
+      // One box per tile: {64 elements, TK rows, the D/64 row halves, one unit}.
+      tma_load_4d(dst, tmK, 0, blk * TK, 0, ug, bar);
+      tma_load_4d(dst + C::TILE, tmV, 0, blk * TK, 0, ug, bar);
+      if constexpr (ROTK) {
+        int rowA, rowB;
+        if constexpr (ROWS == QUERY_BASES) {
+          const int mA = u.fill - 1 - r0;
+          rowA = mA < 0 ? -mA : mA;
+          rowB = mA + W;
+        } else {
+          rowA = r0;
+          rowB = W - r0;
+        }
+        bulk_load(dst + 2 * C::TILE, p.table + (size_t)rowA * C::HALF, C::TROW, bar);
+        if (wraps)
+          bulk_load(dst + 2 * C::TILE + C::TROW, p.table + (size_t)rowB * C::HALF, C::TROW, bar);
+      }
+      ++issued;
+      if (++stage == NS) { stage = 0; ++round; }
+      if (++blk == NB) blk = 0;
+      r0 += TK;
+      if (r0 >= W) r0 -= W;
+    }
+  }
+  return issued;
+}
+
+}  // namespace rkv

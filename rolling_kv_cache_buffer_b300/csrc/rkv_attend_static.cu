@@ -85,17 +85,7 @@ extern "C" rkv_status rkv_attend_static_scratch(rkv_handle* h, const void* q, fl
   p.R = n_q * h->sh.G;
   p.slot_floats = h->ws.slot_floats;
   p.scale_log2 = h->scale * 1.4426950408889634f;
-  cudaError_t e;
-  const bool mma = h->cfg.attend_impl != RKV_ATTEND_FMA && h->has_map4 &&
-                   rkv::attend_mma_supported(h->sh, n_q);
-  if (mma) {
-    e = rkv::launch_attend_mma(p, h->tmK4, h->tmV4, grid, s);
-  } else {
-    if (h->cfg.attend_impl == RKV_ATTEND_MMA) return RKV_ERR_UNSUPPORTED;
-    if (p.R > 16) return RKV_ERR_UNSUPPORTED;
-    e = rkv::launch_attend_fma(p, h->tmK, h->tmV, grid, s);
-  }
-  if (e == cudaErrorNotSupported) return RKV_ERR_UNSUPPORTED;
-  h->last_launches = 2;   // the ticket clear and the attention kernel
-  return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+  const rkv_status ls = rkv::launch_attend_any(h, p, grid, s);
+  if (ls == RKV_OK) h->last_launches = 2;   // the ticket clear and the attention kernel
+  return ls;
 }

@@ -40,4 +40,24 @@ inline int attend_grid(const rkv_handle* h, int n_layers) {
   if (h->sh.S == 1 && units <= sms) return units * (sms / units);
   return sms;
 }
+
+// Picks and launches the attention kernel for p.c queries per stream: the
+// tensor-core kernels for bf16 caches (single query, or a chunk of c*G <= 96
+// rows) unless the handle asks for the CUDA-core kernel, which serves f32
+// caches and c*G <= 16.  RKV_ERR_UNSUPPORTED when no kernel takes the call.
+inline rkv_status launch_attend_any(const rkv_handle* h, const AttendParams& p, int grid,
+                                    cudaStream_t s) {
+  const bool tc = h->cfg.attend_impl != RKV_ATTEND_FMA && h->has_map4;
+  cudaError_t e;
+  if (tc && p.c == 1 && attend_mma_supported(h->sh, 1)) {
+    e = launch_attend_mma(p, h->tmK4, h->tmV4, grid, s);
+  } else if (tc && p.c > 1 && attend_chunk_supported(h->sh, p.c)) {
+    e = launch_attend_chunk(p, h->tmK4, h->tmV4, grid, s);
+  } else {
+    if (h->cfg.attend_impl == RKV_ATTEND_MMA || p.R > 16) return RKV_ERR_UNSUPPORTED;
+    e = launch_attend_fma(p, h->tmK, h->tmV, grid, s);
+  }
+  if (e == cudaErrorNotSupported) return RKV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+}
 }  // namespace rkv

@@ -99,6 +99,10 @@ cudaError_t launch_attend_fma(const AttendParams& p, const CUtensorMap& tk, cons
 cudaError_t launch_attend_mma(const AttendParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                               int grid, cudaStream_t s);
 bool attend_mma_supported(const Shape& sh, int c);
+// Tensor-core chunk attention (c >= 2 queries per stream, c*G <= 96 rows).
+cudaError_t launch_attend_chunk(const AttendParams& p, const CUtensorMap& tk,
+                                const CUtensorMap& tv, int grid, cudaStream_t s);
+bool attend_chunk_supported(const Shape& sh, int c);
 size_t attend_fma_smem(const Shape& sh, int R);
 size_t attend_mma_smem(const Shape& sh, int c);
 

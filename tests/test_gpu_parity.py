@@ -218,7 +218,8 @@ def test_empty_window_gives_zero():
 # ----------------------------------------------------------------------------
 
 @pytest.mark.parametrize("wl_name,c,impl", [("tiny", 5, "fma"), ("audio8", 6, "fma"),
-                                            ("audio8", 6, "auto")])
+                                            ("audio8", 6, "auto"), ("qwen3b", 6, "auto"),
+                                            ("qwen3b", 2, "auto"), ("qwen3b", 12, "auto")])
 def test_chunk_causal(wl_name, c, impl):
     base = WORKLOADS[wl_name]
     wl = base.replace(n_new=c, capacity=min(base.capacity, 64), n_layers=min(base.n_layers, 2))
@@ -231,6 +232,63 @@ def test_chunk_causal(wl_name, c, impl):
         out = cache.attend(dev(q, dt))
         orc.append(k.double().numpy(), v.double().numpy())
         compare(out, orc.attend(q.double().numpy()))
+
+
+def test_qwen3b_chunk6_full_window_sampled_layers():
+    """The 6-token workload (36 layers, GQA 16/2 x 128, W 4096, 1% of k rows
+    doubled): full window at origin 123456, all layers in one launch, layers
+    0, 17 and 35 checked over three evicting steps."""
+    wl = WORKLOADS["qwen3b_chunk6"]
+    layers = [0, 17, 35]
+    cache = make_cache(wl)
+    orc = make_oracle(wl, n_layers=len(layers))
+    _seed_full_window(wl, cache, orc, 0, 123_456, wl.capacity, layers)
+    for t in range(1, 4):
+        q, k, v = step_inputs(wl, t)
+        cache.append(dev(k, torch.bfloat16), dev(v, torch.bfloat16))
+        out = cache.attend(dev(q, torch.bfloat16))
+        orc.append(k[layers].double().numpy(), v[layers].double().numpy())
+        compare(out[layers], orc.attend(q[layers].double().numpy()))
+    o, f, st = cache.get_stream_state()
+    assert (int(o[0]), int(f[0]), int(st[0])) == (123_474, 4096, 0)
+
+
+@pytest.mark.parametrize("layout,style", [("pre_rope", "interleaved"),
+                                          ("stored_rotated", "split_half")])
+def test_chunk_layouts(layout, style):
+    """6-token chunks with the interleaved pairing and with stored-rotated keys,
+    through fill, eviction and the ring's wrap."""
+    wl = WORKLOADS["qwen3b_chunk6"].replace(n_layers=2, capacity=64)
+    cache = make_cache(wl, layout=layout, style=style)
+    cls = O.StoredRotatedOracle if layout == "stored_rotated" else O.RollingCacheOracle
+    orc = make_oracle(wl, cls=cls, style=style)
+    for t in range(1, 26):
+        q, k, v = step_inputs(wl, t)
+        cache.append(dev(k, torch.bfloat16), dev(v, torch.bfloat16))
+        orc.append(k.double().numpy(), v.double().numpy())
+        if layout == "stored_rotated":
+            cache.rebase()
+            orc.rebase()
+        out = cache.attend(dev(q, torch.bfloat16))
+        compare(out, orc.attend(q.double().numpy()))
+
+
+def test_chunk_evicted_slots_never_read():
+    """Chunk attention over windows whose other slots hold NaN: finite outputs,
+    bitwise equal to those of clean pools."""
+    wl = WORKLOADS["qwen3b"].replace(n_streams=4, n_layers=3, capacity=256)
+    cache = make_cache(wl, max_chunk=6)
+    origins, fills = [0, 250, 1000, 77], [6, 37, 200, 256]
+    for s in range(4):
+        k = random_rows((3, 2, fills[s], 128), 300 + s, torch.bfloat16)
+        v = random_rows((3, 2, fills[s], 128), 400 + s, torch.bfloat16)
+        write_window(cache, s, origins[s], fills[s], k, v)
+    q = dev(random_rows((3, 4, 6, 16, 128), 7, torch.bfloat16), torch.bfloat16)
+    clean = cache.attend(q).clone()
+    poison_outside(cache, origins, fills)
+    dirty = cache.attend(q)
+    assert torch.isfinite(dirty).all()
+    assert torch.equal(clean, dirty)
 
 
 # ----------------------------------------------------------------------------
