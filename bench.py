@@ -194,15 +194,23 @@ def run_gpu(args, rank, world):
         flush.zero_()
         torch.amax(drain)
 
+    # The fused decode step (rkv_step: one launch) wherever it applies; the
+    # three calls otherwise and for the append/attend split below.
+    fused = layout == "pre_rope" and wl.kv_dtype == "bf16" and c == 1 and \
+        args.attend_impl != "fma" and not args.no_fused
+
     def step(i, ev=None, split=False):
         q, k, v = ring[i % len(ring)]
         if ev:
             ev[0].record(stream)
-        cache.append(k, v)
-        cache.rebase()
-        if ev and split:
-            ev[1].record(stream)
-        cache.attend(q, out)
+        if fused and not split:
+            cache.step(k, v, q, out)
+        else:
+            cache.append(k, v)
+            cache.rebase()
+            if ev and split:
+                ev[1].record(stream)
+            cache.attend(q, out)
         if ev:
             ev[2].record(stream)
 
@@ -212,7 +220,7 @@ def run_gpu(args, rank, world):
         step(n_done)
         n_done += 1
     torch.cuda.synchronize(dev)
-    launches_per_step = 2 + (1 if layout == "stored_rotated" else 0)
+    launches_per_step = 1 if fused else 2 + (1 if layout == "stored_rotated" else 0)
 
     # Timed region: exactly `steps` whole steps, one event pair around each.
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -258,10 +266,10 @@ def run_gpu(args, rank, world):
     assert torch.isfinite(out).all(), "non-finite attention output"
 
     # e2e: host buffers through the public API, copies inside the timed region.
-    e2e = run_e2e(args, cache, ring, dev, wl, stream) if not args.no_e2e else \
+    e2e = run_e2e(args, cache, ring, dev, wl, stream, fused) if not args.no_e2e else \
         {"ms_per_step": float("nan"), "h2d": 0, "d2h": 0}
 
-    res = dict(total_bytes=total_bytes, total_ms=total_ms, steps=args.steps,
+    res = dict(total_bytes=total_bytes, total_ms=total_ms, steps=args.steps, fused=fused,
                step_ms=step_ms, attend_ms=attend_ms, append_ms=append_ms, wall_s=wall,
                split_bytes=split_bytes,
                clocks=clk.summary(), launches=launches_per_step * args.steps,
@@ -269,7 +277,7 @@ def run_gpu(args, rank, world):
     return res
 
 
-def run_e2e(args, cache, ring, dev, wl, stream):
+def run_e2e(args, cache, ring, dev, wl, stream, fused):
     import torch
     host = []
     for q, k, v in ring[: min(len(ring), 16)]:
@@ -287,9 +295,12 @@ def run_e2e(args, cache, ring, dev, wl, stream):
         dq.copy_(q, non_blocking=True)
         dk.copy_(k, non_blocking=True)
         dv.copy_(v, non_blocking=True)
-        cache.append(dk, dv)
-        cache.rebase()
-        cache.attend(dq, out)
+        if fused:
+            cache.step(dk, dv, dq, out)
+        else:
+            cache.append(dk, dv)
+            cache.rebase()
+            cache.attend(dq, out)
         hout.copy_(out, non_blocking=True)
 
     for i in range(3):
@@ -372,6 +383,22 @@ def oracle_cores():
         return cores
 
 
+def combine_ranks(ms, e2e_ms, att_ms, bytes_local, world, device):
+    """Whole-job numbers from every rank's own: the slowest rank's times (MAX)
+    and the bytes all ranks processed (SUM).  Each rank runs its own streams
+    (independent replicas), so this is the only cross-rank traffic."""
+    if world <= 1:
+        return ms, e2e_ms, att_ms, bytes_local
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms, e2e_ms, att_ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    b = torch.tensor([bytes_local], device=device, dtype=torch.float64)
+    dist.all_reduce(b)
+    ms, e2e_ms, att_ms = [float(x) for x in t.tolist()]
+    return ms, e2e_ms, att_ms, float(b.item())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -383,6 +410,8 @@ def main():
     ap.add_argument("--ring", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="time rkv_append + rkv_rebase + rkv_attend instead of rkv_step")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end loop (short runs under ncu)")
     args = ap.parse_args()
@@ -428,25 +457,28 @@ def main():
     att_ms = sum(res["attend_ms"]) / len(res["attend_ms"])
     att_bytes = sum(res["split_bytes"]) / len(res["split_bytes"])
     e2e_ms_local = res["e2e"]["ms_per_step"]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_local, e2e_ms_local, att_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms, att_ms = [float(x) for x in t.tolist()]
-        b = torch.tensor([bytes_local], device="cuda", dtype=torch.float64)
-        dist.all_reduce(b)
-        all_bytes = float(b.item())
-    else:
-        ms, e2e_ms, all_bytes = ms_local, e2e_ms_local, bytes_local
+    ms, e2e_ms, att_ms, all_bytes = combine_ranks(ms_local, e2e_ms_local, att_ms, bytes_local,
+                                                  world, "cuda")
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
     value = all_bytes / (ms * 1e-3) / 1e9
-    achieved = att_bytes / (att_ms * 1e-3) / 1e9
-    kernel_key = "attend_mma" if args.attend_impl != "fma" and wl.kv_dtype == "bf16" else \
-        "attend_fma"
+    split = {"append_us": 1e3 * sum(res["append_ms"]) / len(res["append_ms"]),
+             "attend_us": att_ms * 1e3,
+             "timing": "rkv_append + rkv_rebase and rkv_attend timed apart on extra steps "
+                       "(an event between them)"}
+    if res["fused"]:
+        # The step is one launch of the fused kernel: its events bracket the kernel.
+        kernel_key = "attend_mma_step"
+        kern_us = ms_local * 1e3
+        achieved = bytes_local / (ms_local * 1e-3) / 1e9
+    else:
+        kernel_key = "attend_mma" if args.attend_impl != "fma" and wl.kv_dtype == "bf16" else \
+            "attend_fma"
+        kern_us = att_ms * 1e3
+        achieved = att_bytes / (att_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -459,14 +491,13 @@ def main():
                    "l2": "between steps, outside the timed events: 256 MiB written, then "
                          "another 256 MiB read (cold L2, no dirty lines)",
                    "attend_impl": args.attend_impl, "parallelism": f"replicas x{world}",
-                   "step": "append + rebase + attend (all layers)"},
+                   "step": ("rkv_step: append + rebase + attend (all layers), one launch"
+                            if res["fused"] else "rkv_append + rkv_rebase + rkv_attend "
+                            "(all layers)")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "kernel": kernel_key, "traffic": _traffic(kernel_key),
-                     "attend_us": att_ms * 1e3,
-                     "append_us": 1e3 * sum(res["append_ms"]) / len(res["append_ms"]),
-                     "timing": "attend and append timed apart on extra steps (an event "
-                               "between them)"},
+                     "kernel_us": kern_us, "split": split},
         "e2e": {"value": all_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "us_per_step": e2e_ms * 1e3, "h2d_bytes_per_step": res["e2e"]["h2d"],
                 "d2h_bytes_per_step": res["e2e"]["d2h"]},

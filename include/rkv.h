@@ -145,6 +145,22 @@ rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_be
  * pairs that append evicted, in float32, rounded to nearest even. */
 rkv_status rkv_rebase(rkv_handle* h, void* stream);
 
+/* One decode step in one kernel launch: rkv_append of one new pair per stream,
+ * the (pre-RoPE, data-free) re-base and rkv_attend over every layer, fused.
+ * k_new, v_new: device, [L][S][1][H_kv][D] of kv_dtype; q: device,
+ * [L][S][1][H_q][D] of q_dtype; out: device float32, same shape as q;
+ * step_log: NULL or device int64 [S][4] as for rkv_append.  Results, pool
+ * contents and stream states equal those of rkv_append(k_new, v_new, 1),
+ * rkv_rebase and rkv_attend(q, out, 0, L, 1) in sequence: the new pair is
+ * written to its slot, and the attention takes it from k_new/v_new (its score
+ * is <q, k_new>, the query and the key sharing a position) together with the
+ * other retained pairs from the pools.  PRE_ROPE bf16 caches served by the
+ * tensor-core kernel only; anything else returns RKV_ERR_UNSUPPORTED before
+ * touching the GPU (use the three calls instead).  The new states are
+ * published by the last CTA of the launch to finish. */
+rkv_status rkv_step(rkv_handle* h, const void* k_new, const void* v_new, const void* q,
+                    float* out, int64_t* step_log, void* stream);
+
 /* Size of the library-owned scratch array used by rkv_attend_static_scratch. */
 #define RKV_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
 

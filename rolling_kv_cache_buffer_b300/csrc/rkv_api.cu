@@ -256,6 +256,7 @@ rkv_status rkv_append(rkv_handle* h, const void* k_new, const void* v_new, int32
   p.k_pool = h->k_pool;
   p.v_pool = h->v_pool;
   p.log = reinterpret_cast<long long*>(step_log);
+  p.tickets = reinterpret_cast<int*>(h->workspace + h->ws.append_tk_off);
   p.table = reinterpret_cast<const float2*>(h->workspace + h->ws.table_off);
   p.c = n_new;
   p.div_hkv = rkv::FastDiv::make(static_cast<uint32_t>(h->sh.Hkv));
@@ -291,6 +292,45 @@ rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_be
   const rkv_status st = rkv::launch_attend_any(h, p, grid, s);
   if (st == RKV_OK) h->last_launches = 1;
   return st;
+}
+
+rkv_status rkv_step(rkv_handle* h, const void* k_new, const void* v_new, const void* q,
+                    float* out, int64_t* step_log, void* stream) {
+  if (!h || !k_new || !v_new || !q || !out) return RKV_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(out) ||
+      (step_log && !aligned16(step_log)))
+    return RKV_ERR_INVALID_ARG;
+  if (h->sh.stored_rotated || !h->sh.bf16 || !h->has_map4 ||
+      h->cfg.attend_impl == RKV_ATTEND_FMA || !rkv::attend_mma_supported(h->sh, 1))
+    return RKV_ERR_UNSUPPORTED;
+  rkv::AttendParams p = {};
+  p.sh = h->sh;
+  p.st = h->state;
+  p.q = q;
+  p.out = out;
+  p.table = reinterpret_cast<const float2*>(h->workspace + h->ws.table_off);
+  p.partials = reinterpret_cast<float*>(h->workspace + h->ws.part_off);
+  p.unit_tickets = reinterpret_cast<int*>(h->workspace + h->ws.unit_tk_off);
+  p.layer_begin = 0;
+  p.L_att = h->sh.L;
+  p.c = 1;
+  p.R = h->sh.G;
+  p.slot_floats = h->ws.slot_floats;
+  p.scale_log2 = h->scale * 1.4426950408889634f;
+  p.fused = 1;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_pool = h->k_pool;
+  p.v_pool = h->v_pool;
+  p.log = reinterpret_cast<long long*>(step_log);
+  p.step_ticket = reinterpret_cast<int*>(h->workspace + h->ws.append_tk_off);
+  const int grid = rkv::attend_grid(h, h->sh.L);
+  const cudaError_t e =
+      rkv::launch_step_mma(p, h->tmK4, h->tmV4, grid, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return RKV_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return RKV_ERR_CUDA;
+  h->last_launches = 1;
+  return RKV_OK;
 }
 
 rkv_status rkv_rebase(rkv_handle* h, void* stream) {

@@ -19,8 +19,9 @@
 // rotated once per unit, R(r_j) q_j.  Stored-rotated keys are used as stored.
 //
 // Work split: the R rows are cut into groups of 16; a team of ceil(R/16)
-// consumer warps takes a block, each warp one row group over all 32 keys of
-// the block.  The producer, the stage ring and the merges are those of the
+// consumer warps takes a block: the team first turns the block's keys in
+// place in shared memory (each key once), then each warp takes one row group
+// over all 32 keys of the block.  The producer, the stage ring and the merges are those of the
 // single-query kernel (rkv_attend_pipe.cuh).
 #include "rkv_attend_pipe.cuh"
 
@@ -34,6 +35,7 @@ constexpr int CCONS = CCW * 32;
 constexpr int CH_MAX_STAGES = 16;
 constexpr int CBAR_CONS = 1;                  // named barrier of the consumer warps
 constexpr int CBAR_PREFIX = 2;                // the producer warp's block prefix is ready
+constexpr int CBAR_TEAM0 = 3;                 // + team: the team's keys are rotated
 constexpr int CH_MAX_ROWS = CCW * 16;
 
 template <int D, bool ROTK>
@@ -103,6 +105,50 @@ __device__ __forceinline__ void rot_pair2_composed(uint32_t& x, uint32_t& y, flo
   f2_split(Yr, e, f);
   x = pack_bf2(a, b);
   y = pack_bf2(e, f);
+}
+
+// Turns key slot d of a block tile in place by R(base + d): the 16-byte chunk
+// m of its first half (dims 8m..8m+7) with its partners (dims D/2+8m..), i.e.
+// split-half pairs 8m..8m+7; or, interleaved, the 4 pairs of chunk m.  `tb` is
+// the base's (cos, sin) row (sine times sg), `frow` the R(d) row of the fine
+// table.
+template <int D, int STYLE>
+__device__ __forceinline__ void rotate_unit(uint8_t* kt, int d, int m, const float2* tb, float sg,
+                                            const uint8_t* frow) {
+  if constexpr (STYLE == 0) {
+    uint4* px = reinterpret_cast<uint4*>(kt + tile_swz(d, m));
+    uint4* py = reinterpret_cast<uint4*>(kt + tile_swz(d, m + D / 16));
+    uint4 x = *px, y = *py;
+    uint32_t* xw = reinterpret_cast<uint32_t*>(&x);
+    uint32_t* yw = reinterpret_cast<uint32_t*>(&y);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int i = 8 * m + 2 * t;          // pairs i, i+1
+      const float4 ds = *reinterpret_cast<const float4*>(frow + fine_chunk<D>(d, i >> 1));
+      const float4 bs = *reinterpret_cast<const float4*>(tb + i);
+      rot_pair2_composed(xw[t], yw[t], bs, sg, ds);
+    }
+    *px = x;
+    *py = y;
+  } else {
+    uint4* pz = reinterpret_cast<uint4*>(kt + tile_swz(d, m));
+    uint4 z = *pz;
+    uint32_t* zw = reinterpret_cast<uint32_t*>(&z);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int i = 4 * m + t;              // the pair in word t
+      const float2 cd = *reinterpret_cast<const float2*>(frow + fine_chunk<D>(d, i >> 1) +
+                                                        ((i & 1) << 3));
+      const float2 cb = tb[i];
+      const float cbs = sg * cb.y;
+      const float cc = cb.x * cd.x - cbs * cd.y;
+      const float ss = cbs * cd.x + cb.x * cd.y;
+      float x0 = bf_lo(zw[t]), x1 = bf_hi(zw[t]);
+      rotc(x0, x1, cc, ss);
+      zw[t] = pack_bf2(x0, x1);
+    }
+    *pz = z;
+  }
 }
 
 }  // namespace
@@ -288,11 +334,32 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
           *abort_flag = 1;
           p.st[u.s].status = STATUS_DEVICE_STATE;
         }
+        if constexpr (ROTK) {
+          // The team turns the block's keys in place, each warp a share of
+          // the (key, chunk) units, then meets at the team barrier.
+          if (!dead) {
+            uint8_t* ktw = stages + (size_t)stage * C::STAGE;
+            const float2* trA = reinterpret_cast<const float2*>(ktw + 2 * TILE);
+            constexpr int UPK = STYLE == 0 ? D / 16 : D / 8;   // units per key
+            for (int un = rg * 32 + lane; un < TK * UPK; un += RG * 32) {
+              const int d = un / UPK, m = un % UPK;
+              const bool useB = d >= wrap_at;                  // past the ring's end
+              rotate_unit<D, STYLE>(ktw, d, m, useB ? trA + HALF : trA, useB ? -1.f : 1.f,
+                                    fine + d * HALF * 8);
+            }
+            // These generic writes come before the next asynchronous copy into
+            // the stage.
+            fence_proxy_async();
+          }
+          if (RG > 1)
+            named_bar_sync(CBAR_TEAM0 + team, RG * 32);
+          else
+            __syncwarp();
+        }
         if (!dead) {
           const uint8_t* kt = stages + (size_t)stage * C::STAGE;
           const uint8_t* vt = kt + TILE;
           const uint32_t kt_s = smem_u32(kt), vt_s = smem_u32(vt);
-          const float2* trA = reinterpret_cast<const float2*>(kt + 2 * TILE);
           // ---- S = Q K^T per 8-key group ----
           float s[4][2][2];   // [key group][row 0/1][key pair element]
 #pragma unroll
@@ -303,37 +370,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             for (int g4 = 0; g4 < NGRP; g4 += 4)
               ldsm_x4(kt_s + tile_swz(krow, g4 + (lane >> 3)), kf[g4], kf[g4 + 1], kf[g4 + 2],
                       kf[g4 + 3]);
-            if constexpr (ROTK) {
-              const int dk = nb * 8 + g;              // this thread's key within the block
-              const bool useB = dk >= wrap_at;        // past the ring's end: base r0 - W
-              const float2* tb = useB ? trA + HALF : trA;
-              const float sg = useB ? -1.f : 1.f;
-              const uint8_t* frow = fine + dk * HALF * 8;
-              if constexpr (STYLE == 0) {
-#pragma unroll
-                for (int gr = 0; gr < HG; ++gr) {
-                  const int i = 8 * gr + 2 * cq;      // pairs i and i+1
-                  const float4 ds =
-                      *reinterpret_cast<const float4*>(frow + fine_chunk<D>(dk, i >> 1));
-                  const float4 bs = *reinterpret_cast<const float4*>(tb + i);
-                  rot_pair2_composed(kf[gr], kf[gr + HG], bs, sg, ds);
-                }
-              } else {
-#pragma unroll
-                for (int gr = 0; gr < NGRP; ++gr) {
-                  const int i = 4 * gr + cq;          // the pair in word gr
-                  const float2 cd = *reinterpret_cast<const float2*>(
-                      frow + fine_chunk<D>(dk, i >> 1) + ((i & 1) << 3));
-                  const float2 cb = tb[i];
-                  const float cbs = sg * cb.y;
-                  const float cc = cb.x * cd.x - cbs * cd.y;
-                  const float ss = cbs * cd.x + cb.x * cd.y;
-                  float x0 = bf_lo(kf[gr]), x1 = bf_hi(kf[gr]);
-                  rotc(x0, x1, cc, ss);
-                  kf[gr] = pack_bf2(x0, x1);
-                }
-              }
-            }
             float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kb = 0; kb < NKB; kb += 2) {

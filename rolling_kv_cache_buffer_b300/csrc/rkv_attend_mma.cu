@@ -68,7 +68,7 @@ struct MmaCfg : PipeCfg<D, ROTK> {
   // Bytes after the stages (the warp slots of a segment merge alias the
   // stages), without the per-stream prefix: R(d) table, query rows, flags and
   // the merge-done barrier.
-  static constexpr int FIXED = FINE + 8 * QSTR * 4 + 16 + 16;
+  static constexpr int FIXED = FINE + 8 * QSTR * 4 + 16 + 16 + 32 + 2 * D * 4;
 };
 
 __host__ __device__ constexpr size_t mma_smem_bytes(int stage, int fixed, int ns, int S) {
@@ -119,7 +119,89 @@ __device__ __forceinline__ void rot_pair2(uint32_t& x, uint32_t& y, float4 cs) {
 
 }  // namespace
 
-template <int D, bool ROTK, int STYLE>
+// Fused decode step: what rkv_append of one pair would leave in a stream's
+// state, from the state the step starts from (the bookkeeping of the append
+// kernel: e = max(0, n + 1 - W), o' = o + e, n' = n + 1 - e).
+struct StepState {
+  bool ok;
+  int e, n2, ring2;   // evictions, fill and origin mod W after the append
+  int new_slot;       // slot of the new pair
+};
+__device__ __forceinline__ StepState step_state(const StreamState& st, int W) {
+  StepState r;
+  r.ok = state_ok(st, W);
+  r.e = max(0, st.fill + 1 - W);
+  r.n2 = st.fill + 1 - r.e;
+  r.ring2 = st.ring + r.e < W ? st.ring + r.e : st.ring + r.e - W;
+  r.new_slot = st.ring + st.fill < W ? st.ring + st.fill : st.ring + st.fill - W;
+  return r;
+}
+
+// Block prefix of a fused step: every stream's window after the append minus
+// its new pair (the kernels read the new pair from the step's inputs, not from
+// the pool), i.e. ring start ring', n' - 1 pairs; the query sits at n' - 1.
+__device__ __forceinline__ void build_prefix_step(const AttendParams& p, int* pre, int* sa,
+                                                  int* sfill, int lane) {
+  const int per_unit = p.L_att * p.sh.Hkv;
+  int carry = 0;
+  if (lane == 0) pre[0] = 0;
+  for (int base = 0; base < p.sh.S; base += 32) {
+    const int s = base + lane;
+    int v = 0;
+    if (s < p.sh.S) {
+      const StepState ss = step_state(p.st[s], p.sh.W);
+      sa[s] = ss.ok ? ss.ring2 : -1;
+      sfill[s] = ss.ok ? ss.n2 - 1 : 0;
+      v = ss.ok ? touched_blocks(ss.ring2, ss.n2 - 1, p.sh.NB) * per_unit : 0;
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += t;
+    }
+    if (s < p.sh.S) pre[s + 1] = carry + v;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+}
+
+// Fused step, every unit once (CTAs stride over the units, threads t of nt
+// share a unit): the new pair goes into its slot in the pools (this step's
+// attention takes it from the inputs and never reads that slot), and a unit
+// whose window holds only the new pair gets v_new as its output.
+template <int D>
+__device__ __forceinline__ void step_prepass(const AttendParams& p, int w, int nw, int lane) {
+  const int per_stream = p.L_att * p.sh.Hkv;
+  const int units = p.sh.S * per_stream;
+  const int esz = p.sh.bf16 ? 2 : 4;
+  const int t = lane, nt = 32;   // one warp per unit
+  for (int u = blockIdx.x + gridDim.x * w; u < units; u += gridDim.x * nw) {
+    const int s = u / per_stream;
+    const StepState ss = step_state(p.st[s], p.sh.W);
+    if (!ss.ok) continue;
+    const int l = (u % per_stream) / p.sh.Hkv, g = u % p.sh.Hkv;
+    const size_t src = (((size_t)l * p.sh.S + s) * p.sh.Hkv + g) * D;
+    const size_t dst = ((((size_t)s * p.sh.L + l) * p.sh.Hkv + g) * p.sh.W + ss.new_slot) * D;
+    const int chunks = D * esz / 16;
+    for (int i = t; i < 2 * chunks; i += nt) {
+      const int kv = i >= chunks, q = i - kv * chunks;
+      const uint4* from = reinterpret_cast<const uint4*>(
+          static_cast<const uint8_t*>(kv ? p.v_new : p.k_new) + src * esz) + q;
+      uint4* to = reinterpret_cast<uint4*>(
+          static_cast<uint8_t*>(kv ? p.v_pool : p.k_pool) + dst * esz) + q;
+      *to = *from;
+    }
+    if (ss.n2 == 1) {   // only the new pair: softmax over one key gives v_new
+      UnitRef ur;
+      ur.s = s; ur.l = l; ur.g = g;
+      for (int i = t; i < p.sh.G * D; i += nt) {
+        const int h = i / D, d = i % D;
+        p.out[row_offset(p, ur, h) + d] = load_elem(p.v_new, src + d, p.sh.bf16);
+      }
+    }
+  }
+}
+
+template <int D, bool ROTK, int STYLE, bool FUSED>
 __global__ void __launch_bounds__(MMA_THREADS, 1)
     attend_mma_decode(const __grid_constant__ AttendParams p,
                       const __grid_constant__ CUtensorMap tmK,
@@ -138,7 +220,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   float* qs = reinterpret_cast<float*>(fine + C::FINE);            // [8][QSTR] raw query
   int* flag = reinterpret_cast<int*>(qs + 8 * QSTR);               // ticket, abort, issued
   uint64_t* mdone = reinterpret_cast<uint64_t*>(flag + 4);         // segment merged
-  uint64_t* full = mdone + 2;                                      // [NS]
+  float* mx = reinterpret_cast<float*>(mdone + 2);                 // [8] new-key scores
+  float* kvn = mx + 8;                                             // [2][D] new pair (fused)
+  uint64_t* full = reinterpret_cast<uint64_t*>(kvn + 2 * D);       // [NS]
   uint64_t* empty = full + NS;                                     // [NS]
   int* pre = reinterpret_cast<int*>(empty + NS);                   // [S+1] block prefix
   int* sa = pre + p.sh.S + 1;                                      // [S] origin mod W
@@ -162,11 +246,24 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     if (warp > 0) load_fine<D, STYLE>(p, fine, tid - 32, CONS_THREADS);
   }
   prefetch_queries(p, D);
+  if constexpr (FUSED) {
+    // The step's new pairs (not written by any earlier kernel of the step).
+    const size_t nbytes = (size_t)p.L_att * p.sh.S * p.sh.Hkv * D * (p.sh.bf16 ? 2 : 4);
+    const size_t lines = (nbytes + 127) / 128;
+    const size_t l0 = lines * blockIdx.x / gridDim.x, l1 = lines * (blockIdx.x + 1) / gridDim.x;
+    for (size_t l = l0 + tid; l < l1; l += blockDim.x) {
+      prefetch_l2(static_cast<const uint8_t*>(p.k_new) + l * 128);
+      prefetch_l2(static_cast<const uint8_t*>(p.v_new) + l * 128);
+    }
+  }
   pdl_wait();   // from here on: stream state, pools, queries, outputs
   // Warp 0 builds the block prefix and starts streaming at once; the
   // consumers pick the prefix up from the named barrier.
   if (warp == 0) {
-    build_prefix_cached(p, pre, sa, sfill, lane);
+    if constexpr (FUSED)
+      build_prefix_step(p, pre, sa, sfill, lane);
+    else
+      build_prefix_cached(p, pre, sa, sfill, lane);
     __syncwarp();
     named_bar_arrive(BAR_PREFIX, MMA_THREADS);
   } else {
@@ -181,13 +278,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     // ------------------------------------------------------------------ producer
     if (lane == 0)
       flag[2] = produce<D, ROTK, QUERY_BASES>(p, &tmK, &tmV, stages, full, empty, mdone, pre, sa,
-                                              sfill, rb, re, abort_flag);
+                                              sfill, rb, re, abort_flag, FUSED ? 1 : 0);
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ consumers
     const int cw = warp - 1, ct = tid - 32;
     const int g = lane >> 2, cq = lane & 3;   // mma fragment coordinates
-    zero_empty_units_cached(p, sa, sfill, ct, CONS_THREADS);
+    if constexpr (FUSED)
+      step_prepass<D>(p, cw, NCW, lane);
+    else
+      zero_empty_units_cached(p, sa, sfill, ct, CONS_THREADS);
     // Raw query of a unit into `qs` (rows >= G are zero).
     auto load_query = [&](const UnitRef& u) {
       for (int idx = ct; idx < 8 * D; idx += CONS_THREADS) {
@@ -195,7 +295,17 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         qs[h * QSTR + d] = h < G ? load_elem(p.q, row_offset(p, u, h) + d, p.sh.q_bf16) : 0.f;
       }
     };
-    if (rb < re) load_query(unit_of_cached(rb, p, pre, sa, sfill));
+    // Fused step: the unit's new pair, for the merge that adds it.
+    auto load_new = [&](const UnitRef& u) {
+      const size_t r = (((size_t)u.l * p.sh.S + u.s) * p.sh.Hkv + u.g) * D;
+      for (int idx = ct; idx < 2 * D; idx += CONS_THREADS)
+        kvn[idx] = load_elem(idx < D ? p.k_new : p.v_new, r + (idx % D), p.sh.bf16);
+    };
+    if (rb < re) {
+      const UnitRef u0 = unit_of_cached(rb, p, pre, sa, sfill);
+      load_query(u0);
+      if constexpr (FUSED) load_new(u0);
+    }
     named_bar_sync(BAR_CONS, CONS_THREADS);
 
     // Dims of the thread's A-fragment elements: k-block kb, j in {0,1,2,3}:
@@ -210,7 +320,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     for (int x = rb; x < re;) {
       const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
       const int x1 = min(u.uend, re);
-      const int rq = u.fill - 1;
+      const int rq = u.fill - 1 + (FUSED ? 1 : 0);   // the query's re-based position
       // The next segment's query: loaded now, stored once this segment is done.
       const bool has_next = x1 < re;
       constexpr int QPT = (8 * D + CONS_THREADS - 1) / CONS_THREADS;
@@ -476,6 +586,16 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
         float* my = slots + cw * C::SLOT;
         if (cq == 0) { my[g] = m_run; my[8 + g] = lsum; }
+        if constexpr (FUSED) {
+          // The new pair sits at the query's own position: its score is <q, k_new>
+          // (the rotations cancel).  Warp h scores head h.
+          if (x1 == u.uend && cw < G) {
+            float dot = 0.f;
+            for (int d = lane; d < D; d += 32) dot += qs[cw * QSTR + d] * kvn[d];
+            dot = warp_sum(dot);
+            if (lane == 0) mx[cw] = dot * p.scale_log2;
+          }
+        }
 #pragma unroll
         for (int mt = 0; mt < NKB; ++mt)
 #pragma unroll
@@ -497,12 +617,18 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       const bool whole = (x == u.ustart) && (x1 == u.uend);
       float* part = nullptr;
       if (!whole) part = p.partials + (size_t)(2 * b + (x == rb ? 0 : 1)) * p.slot_floats;
+      const bool add_new = FUSED && x1 == u.uend;   // this CTA adds the new pair
       for (int idx = ct; idx < R * D; idx += CONS_THREADS) {
         const int h = idx / D, d = idx % D;
-        float M = NEG_BIG;
+        float M = add_new ? mx[h] : NEG_BIG;
 #pragma unroll
         for (int w = 0; w < NCW; ++w) M = fmaxf(M, slots[w * C::SLOT + h]);
         float L = 0.f, v = 0.f;
+        if (add_new) {
+          const float sc = exp2f(mx[h] - M);
+          L = sc;
+          v = sc * kvn[D + d];
+        }
 #pragma unroll
         for (int w = 0; w < NCW; ++w) {
           const float* sw = slots + w * C::SLOT;
@@ -555,10 +681,52 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       fence_proxy_async();
       named_bar_sync(BAR_CONS, CONS_THREADS);
       if (ct == 0) mbar_arrive(smem_u32(mdone));
+      if constexpr (FUSED) {
+        if (has_next) load_new(unit_of_cached(x1, p, pre, sa, sfill));
+      }
       x = x1;
     }
   }
   __syncthreads();
+  if constexpr (FUSED) {
+    // Every CTA read the old states before it got here; the last CTA of the
+    // step to arrive publishes the new ones (the append's bookkeeping), one
+    // stream per lane of warp 0.
+    if (warp == 0) {
+      int last = 0;
+      if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(p.step_ticket, 1) == static_cast<int>(gridDim.x) - 1;
+        if (last) __threadfence();
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        for (int s2 = lane; s2 < p.sh.S; s2 += 32) {
+          const StreamState st = p.st[s2];
+          const StepState ss = step_state(st, W);
+          StreamState ns = st;
+          if (ss.ok) {
+            ns.origin = st.origin + ss.e;
+            ns.fill = ss.n2;
+            ns.ring = ss.ring2;
+            ns.pending = 0;
+            ns.last_new = 1;
+          } else if (ns.status == 0) {
+            ns.status = STATUS_DEVICE_STATE;
+          }
+          p.st[s2] = ns;
+          if (p.log) {
+            long long* lg = p.log + 4 * (size_t)s2;
+            lg[0] = ss.ok ? ns.origin : st.origin;
+            lg[1] = ss.ok ? ns.fill : st.fill;
+            lg[2] = ss.ok ? ss.e : -1;
+            lg[3] = ss.ok ? ss.new_slot : -1;
+          }
+        }
+        if (lane == 0) *p.step_ticket = 0;
+      }
+    }
+  }
   if (tid == 0 && *abort_flag) {
     // Normally every issued stage was waited on by its consumers.  After an
     // abort, no CTA exits with a copy still in flight into its shared memory:
@@ -597,14 +765,14 @@ bool attend_mma_supported(const Shape& sh, int c) {
          attend_mma_smem(sh, c) <= (size_t)SMEM_LIMIT;
 }
 
-template <int D, bool ROTK, int STYLE>
+template <int D, bool ROTK, int STYLE, bool FUSED = false>
 static cudaError_t launch_mma_t(const AttendParams& p0, const CUtensorMap& tk,
                                 const CUtensorMap& tv, int grid, cudaStream_t s) {
   using C = MmaCfg<D, ROTK>;
   AttendParams p = p0;
   p.ns = mma_stages<D, ROTK>(p.sh.S);
   const size_t smem = mma_smem_bytes(C::STAGE, C::FIXED, p.ns, p.sh.S);
-  auto kern = attend_mma_decode<D, ROTK, STYLE>;
+  auto kern = attend_mma_decode<D, ROTK, STYLE, FUSED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -638,6 +806,17 @@ cudaError_t launch_attend_mma(const AttendParams& p, const CUtensorMap& tk, cons
   if (!attend_mma_supported(p.sh, p.c)) return cudaErrorNotSupported;
   if (p.sh.D == 128) return launch_mma_d<128>(p, tk, tv, grid, s);
   return launch_mma_d<64>(p, tk, tv, grid, s);
+}
+
+cudaError_t launch_step_mma(const AttendParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                            int grid, cudaStream_t s) {
+  if (!attend_mma_supported(p.sh, 1) || p.sh.stored_rotated || p.c != 1)
+    return cudaErrorNotSupported;
+  if (p.sh.D == 128)
+    return p.sh.style == 0 ? launch_mma_t<128, true, 0, true>(p, tk, tv, grid, s)
+                           : launch_mma_t<128, true, 1, true>(p, tk, tv, grid, s);
+  return p.sh.style == 0 ? launch_mma_t<64, true, 0, true>(p, tk, tv, grid, s)
+                         : launch_mma_t<64, true, 1, true>(p, tk, tv, grid, s);
 }
 
 }  // namespace rkv

@@ -82,12 +82,14 @@ __device__ __forceinline__ void prefetch_queries(const AttendParams& p, int D) {
 // The producer loop, run by lane 0 of warp 0 over blocks [rb, re).  Returns
 // the number of stages it filled.  Stops early (status set, *abort raised) if
 // a wait runs out.
+// rq_off: the query sits at fill - 1 + rq_off (1 in a fused step, where the
+// cached fill counts the window's pairs other than the new one).
 template <int D, bool ROTK, int ROWS>
 __device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap* tmK,
                                        const CUtensorMap* tmV, uint8_t* stages, uint64_t* full,
                                        uint64_t* empty, uint64_t* mdone, const int* pre,
                                        const int* sa, const int* sfill, int rb, int re,
-                                       volatile int* abort_flag) {
+                                       volatile int* abort_flag, int rq_off = 0) {
   using C = PipeCfg<D, ROTK>;
   const int W = p.sh.W, NB = p.sh.NB, NS = p.ns;
   int stage = 0, round = 0, issued = 0, seg = 0;
@@ -127,7 +129,7 @@ __device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap*
       if constexpr (ROTK) {
         int rowA, rowB;
         if constexpr (ROWS == QUERY_BASES) {
-          const int mA = u.fill - 1 - r0;
+          const int mA = u.fill - 1 + rq_off - r0;
           rowA = mA < 0 ? -mA : mA;
           rowB = mA + W;
         } else {

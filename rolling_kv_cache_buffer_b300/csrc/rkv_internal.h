@@ -58,6 +58,7 @@ struct AppendParams {
   void* k_pool;
   void* v_pool;
   long long* log;          // nullable, [S][4]
+  int* tickets;            // [S] last-part tickets
   const float2* table;
   int c;                   // pairs appended this step
   FastDiv div_hkv, div_c;  // H_kv and c
@@ -85,6 +86,14 @@ struct AttendParams {
   int slot_floats;
   float scale_log2;           // softmax scale * log2(e)
   int ns;                     // pipeline stages (set by the launcher)
+  // Fused decode step (rkv_step): the kernel also appends one pair per stream.
+  int fused;                  // 0: attention only
+  const void* k_new;          // [L][S][1][H_kv][D] of the cache type
+  const void* v_new;
+  void* k_pool;               // the pools the new pair goes into
+  void* v_pool;
+  long long* log;             // nullable, [S][4]
+  int* step_ticket;           // one int: CTAs done with the step
 };
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
@@ -98,6 +107,9 @@ cudaError_t launch_attend_fma(const AttendParams& p, const CUtensorMap& tk, cons
                               int grid, cudaStream_t s);
 cudaError_t launch_attend_mma(const AttendParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                               int grid, cudaStream_t s);
+// Fused decode step (append of one pair + pre-RoPE re-base + attention).
+cudaError_t launch_step_mma(const AttendParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                            int grid, cudaStream_t s);
 bool attend_mma_supported(const Shape& sh, int c);
 // Tensor-core chunk attention (c >= 2 queries per stream, c*G <= 96 rows).
 cudaError_t launch_attend_chunk(const AttendParams& p, const CUtensorMap& tk,

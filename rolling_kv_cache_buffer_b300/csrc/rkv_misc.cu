@@ -86,15 +86,18 @@ __device__ __forceinline__ void load_cs4(const float2* table, size_t row_off, in
 }  // namespace
 
 // ----------------------------------------------------------------------------
-// K0 + K1: bookkeeping and scatter of the new rows.  One CTA per stream
-// (grid = S): every thread reads the old state and derives the same new state
-// from it, the CTA scatters the stream's rows, and thread 0 publishes the new
-// state once the CTA is done, so the step costs one dependent round trip.
+// K0 + K1: bookkeeping and scatter of the new rows.  grid = (parts, S): every
+// thread reads the old state and derives the same new state from it, the
+// parts of a stream scatter its rows, and the new state is published once the
+// stream's rows are written: by the CTA itself when a stream has one part,
+// else by the part that arrives last on the stream's ticket (no CTA waits on
+// another).
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendParams p) {
   pdl_trigger();   // the attention launched next may start its prologue now
   const Shape& sh = p.sh;
-  const int s = blockIdx.x;
+  const int s = blockIdx.y;
+  const int part = blockIdx.x, parts = gridDim.x;
   const StreamState st = p.st[s];
   const int c = p.c, W = sh.W, D = sh.D, Hkv = sh.Hkv;
   const bool ok = state_ok(st, W) && c >= 1 && c <= W &&
@@ -121,8 +124,10 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
     // overlap instead of paying one memory round trip each.
     const int esz = bf ? 2 : 4;
     const int lch = __ffs(D * esz / 16) - 1;          // log2(16-byte chunks per row)
-    const int total = (2 * rows) << lch;              // K rows, then V rows
-    for (int base = 0; base < total; base += APPEND_BATCH * blockDim.x) {
+    const int all = (2 * rows) << lch;                // K rows, then V rows
+    const int lo = static_cast<int>((long long)all * part / parts);
+    const int total = static_cast<int>((long long)all * (part + 1) / parts);
+    for (int base = lo; base < total; base += APPEND_BATCH * blockDim.x) {
       uint4 v[APPEND_BATCH];
       int rr[APPEND_BATCH];
 #pragma unroll
@@ -155,7 +160,9 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
   } else if (ok) {
     // Stored-rotated: keys are stored as R(p - origin') k, four pairs per step.
     const int quads = D / 8;
-    for (int idx = threadIdx.x; idx < rows * quads; idx += blockDim.x) {
+    const int lo = static_cast<int>((long long)rows * quads * part / parts);
+    const int hi = static_cast<int>((long long)rows * quads * (part + 1) / parts);
+    for (int idx = lo + threadIdx.x; idx < hi; idx += blockDim.x) {
       const int row = idx / quads;
       const int i = (idx % quads) * 4;
       int l, j, g;
@@ -175,7 +182,16 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  bool publish = threadIdx.x == 0;
+  if (publish && parts > 1) {
+    __threadfence();
+    publish = atomicAdd(&p.tickets[s], 1) == parts - 1;
+    if (publish) {
+      __threadfence();
+      p.tickets[s] = 0;
+    }
+  }
+  if (publish) {
     StreamState ns = st;
     if (ok) {
       ns.origin = o2;
@@ -251,7 +267,12 @@ __global__ void set_state_kernel(StreamState* st, int s, long long origin, int f
 }
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
-  append_kernel<<<p.sh.S, APPEND_THREADS, 0, s>>>(p);
+  // One CTA per stream unless a stream's rows need several batched passes.
+  const int esz = p.sh.bf16 ? 2 : 4;
+  const long long items = 2LL * p.sh.L * p.c * p.sh.Hkv * (p.sh.D * esz / 16);
+  long long parts = (items + APPEND_THREADS * APPEND_BATCH - 1) / (APPEND_THREADS * APPEND_BATCH);
+  parts = parts < 1 ? 1 : (parts > 64 ? 64 : parts);
+  append_kernel<<<dim3((unsigned)parts, p.sh.S), APPEND_THREADS, 0, s>>>(p);
   return cudaGetLastError();
 }
 cudaError_t launch_rerotate(const RerotParams& p, int blocks_per_stream, cudaStream_t s) {

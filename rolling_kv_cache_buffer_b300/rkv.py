@@ -66,6 +66,7 @@ def load_library():
         "rkv_attend": (c_int32, [P, P, P, c_int32, c_int32, c_int32, P]),
         "rkv_attend_static_scratch": (c_int32, [P, P, P, c_int32, c_int32, c_int32, P]),
         "rkv_rebase": (c_int32, [P, P]),
+        "rkv_step": (c_int32, [P, P, P, P, P, P, P]),
         "rkv_destroy": (c_int32, [P]),
         "rkv_set_stream_state": (c_int32, [P, c_int32, c_int64, c_int32, P]),
         "rkv_get_stream_state": (c_int32, [P, P, P, P, P]),
@@ -128,6 +129,11 @@ def rkv_attend_static_scratch(h, q, out, layer_begin, n_layers, n_q, stream):
 
 def rkv_rebase(h, stream):
     _check(load_library().rkv_rebase(h, stream), "rkv_rebase")
+
+
+def rkv_step(h, k_new, v_new, q, out, step_log, stream):
+    """Fused decode step: append one pair per stream, re-base, attend all layers."""
+    _check(load_library().rkv_step(h, k_new, v_new, q, out, step_log, stream), "rkv_step")
 
 
 def rkv_destroy(h):
@@ -225,6 +231,24 @@ class RollingKV:
 
     def rebase(self):
         rkv_rebase(self.handle, self._stream())
+
+    def step(self, k_new, v_new, q, out=None, step_log=None):
+        """append(k_new, v_new) + rebase() + attend(q) for one token per stream,
+        all layers, in one kernel launch (pre-RoPE bf16 caches)."""
+        shp = (self.L, self.S, 1, self.Hkv, self.D)
+        self._need(k_new, shp, self.kv_dtype, "k_new")
+        self._need(v_new, shp, self.kv_dtype, "v_new")
+        self._need(q, (self.L, self.S, 1, self.Hq, self.D), self.q_dtype, "q")
+        if out is None:
+            out = self.torch.empty(q.shape, dtype=self.torch.float32, device=self.device)
+        self._need(out, tuple(q.shape), self.torch.float32, "out")
+        lp = 0
+        if step_log is not None:
+            self._need(step_log, (self.S, 4), self.torch.int64, "step_log")
+            lp = step_log.data_ptr()
+        rkv_step(self.handle, k_new.data_ptr(), v_new.data_ptr(), q.data_ptr(), out.data_ptr(),
+                 lp, self._stream())
+        return out
 
     def set_stream_state(self, s, origin, fill):
         rkv_set_stream_state(self.handle, s, origin, fill, self._stream())

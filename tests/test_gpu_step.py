@@ -1,0 +1,98 @@
+"""rkv_step (append + re-base + attend in one launch) against the float64
+oracle and against the three separate calls (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import rkv_oracle as O
+from rkv_inputs import WORKLOADS, initial_states, initial_window, random_rows, step_inputs
+from tests.gpu_util import compare, dev, make_cache, make_oracle, write_window
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("wl_name,style", [("qwen3b", "split_half"), ("qwen3b", "interleaved"),
+                                           ("audio8", "split_half")])
+def test_step_from_empty_through_wrap(wl_name, style):
+    """From an empty cache through the fill, the first eviction and two wraps
+    of the ring: logs bit-exact, outputs within tolerance of the oracle, and
+    pools bitwise equal to those of rkv_append + rkv_attend."""
+    wl = WORKLOADS[wl_name].replace(n_layers=2, capacity=64)
+    fused = make_cache(wl, style=style)
+    split = make_cache(wl, style=style)
+    orc = make_oracle(wl, style=style)
+    log = torch.zeros((1, 4), dtype=torch.int64, device="cuda")
+    o, n = 0, 0
+    for t in range(1, 140):
+        q, k, v = step_inputs(wl, t)
+        qd, kd, vd = dev(q, torch.bfloat16), dev(k, torch.bfloat16), dev(v, torch.bfloat16)
+        out = fused.step(kd, vd, qd, step_log=log)
+        split.append(kd, vd)
+        orc.append(k.double().numpy(), v.double().numpy())
+        bk = O.bookkeep(o, n, 1, wl.capacity)
+        o, n = bk.origin, bk.fill
+        assert tuple(log[0].tolist()) == bk.log(), f"step {t}"
+        if t <= 3 or t % 9 == 0 or t in (63, 64, 65, 128, 129):
+            compare(out, orc.attend(q.double().numpy()))
+            # The fused kernel scores the new pair in f32 from the inputs, the
+            # separate path from bf16 tensor-core operands: both sit within the
+            # oracle tolerance, and within half of it of each other.
+            ref = split.attend(qd)
+            compare(out, ref.double().cpu().numpy(), 1e-2, 1e-3)
+    assert torch.equal(fused.k_pool, split.k_pool) and torch.equal(fused.v_pool, split.v_pool)
+    fo, ff, fs = fused.get_stream_state()
+    so, sf, ss = split.get_stream_state()
+    assert (fo.tolist(), ff.tolist(), fs.tolist()) == (so.tolist(), sf.tolist(), ss.tolist())
+
+
+def test_step_qwen3b_full_window_sampled_layers():
+    """The benchmarked call: 36 layers, GQA 16/2 x 128, W 4096, full window at
+    origin 123456; layers 0, 17 and 35 checked over three steps."""
+    wl = WORKLOADS["qwen3b"]
+    layers = [0, 17, 35]
+    cache = make_cache(wl)
+    orc = make_oracle(wl, n_layers=len(layers))
+    k, v = initial_window(wl, 0, wl.capacity)
+    write_window(cache, 0, 123_456, wl.capacity, k, v)
+    orc.set_state(0, 123_456, wl.capacity, k[layers].double().numpy(),
+                  v[layers].double().numpy())
+    for t in range(1, 4):
+        q, k, v = step_inputs(wl, t)
+        out = cache.step(dev(k, torch.bfloat16), dev(v, torch.bfloat16), dev(q, torch.bfloat16))
+        orc.append(k[layers].double().numpy(), v[layers].double().numpy())
+        compare(out[layers], orc.attend(q[layers].double().numpy()))
+    o, f, st = cache.get_stream_state()
+    assert (int(o[0]), int(f[0]), int(st[0])) == (123_459, 4096, 0)
+
+
+def test_step_many_streams():
+    """Eight streams with fills 0, 1, 5, 31, 32, 33, 200, 256 (W 256) and
+    scattered origins: every stream's outputs against the oracle."""
+    wl = WORKLOADS["qwen3b"].replace(n_streams=8, n_layers=2, capacity=256)
+    fills = [0, 1, 5, 31, 32, 33, 200, 256]
+    origins = [0, 7, 250, 1000, 77, 12345, 999_999, 256 * 9 + 3]
+    cache = make_cache(wl)
+    orcs = []
+    for s in range(8):
+        k = random_rows((2, 2, fills[s], 128), 500 + s, torch.bfloat16)
+        v = random_rows((2, 2, fills[s], 128), 600 + s, torch.bfloat16)
+        write_window(cache, s, origins[s], fills[s], k, v)
+        orc = make_oracle(wl, n_streams=1)
+        orc.set_state(0, origins[s], fills[s], k.double().numpy(), v.double().numpy())
+        orcs.append(orc)
+    for t in range(1, 4):
+        q, k, v = step_inputs(wl, t)
+        out = cache.step(dev(k, torch.bfloat16), dev(v, torch.bfloat16), dev(q, torch.bfloat16))
+        for s in range(8):
+            orcs[s].append(k[:, s:s + 1].double().numpy(), v[:, s:s + 1].double().numpy())
+            compare(out[:, s:s + 1], orcs[s].attend(q[:, s:s + 1].double().numpy()))
+
+
+def test_step_unsupported_layouts_are_refused():
+    wl = WORKLOADS["qwen3b"].replace(n_layers=1, capacity=64)
+    cache = make_cache(wl, layout="stored_rotated")
+    q, k, v = step_inputs(wl, 1)
+    from rolling_kv_cache_buffer_b300.rkv import RKV_ERR_UNSUPPORTED, RkvError
+    with pytest.raises(RkvError) as e:
+        cache.step(dev(k, torch.bfloat16), dev(v, torch.bfloat16), dev(q, torch.bfloat16))
+    assert e.value.status == RKV_ERR_UNSUPPORTED
