@@ -185,6 +185,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Prologue: nothing here reads what the previous kernel of the stream writes.
   if (tid == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(full + i), 1);
       mbar_init(smem_u32(empty + i), RG);   // every warp of the team that takes the block
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     if (warp > 0) load_fine<D, STYLE>(p, fine, tid - 32, CCONS);
   }
   prefetch_queries(p, D);
+  prefetch_states(p);
   pdl_wait();   // from here on: stream state, pools, queries, outputs
   if (warp == 0) {
     build_prefix_cached(p, pre, sa, sfill, lane);
@@ -222,7 +225,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     const int g = lane >> 2, cq = lane & 3;   // mma fragment coordinates
     const int team = cw / RG, rg = cw % RG;
     const bool active = team < NTEAM;
-    zero_empty_units_cached(p, sa, sfill, ct, CCONS);
     // Raw queries of a unit into `qs` (rows >= R are zero).
     auto load_query = [&](const UnitRef& u) {
       for (int idx = ct; idx < R16 * D; idx += CCONS) {
@@ -232,6 +234,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       }
     };
     if (rb < re) load_query(unit_of_cached(rb, p, pre, sa, sfill));
+    zero_empty_units_cached(p, sa, sfill, ct, CCONS);
     named_bar_sync(CBAR_CONS, CCONS);
 
     // Dims of the thread's A-fragment elements: k-block kb, j in {0,1,2,3}:

@@ -27,12 +27,16 @@
 // walks the CTA's share of the block list and streams every block's K and V
 // tiles (one 4-D TMA box per tile, 128-byte swizzle) plus the (cos, sin) rows
 // of the block's query rotations into a ring of NS shared-memory stages
-// (full/empty mbarriers).  Warps 1..NCW are consumers: block j of the CTA's share goes to
-// consumer j mod NCW, which keeps an online-softmax state per unit segment.
-// At the end of a segment the consumers merge their states through shared
-// memory (named barrier, shared atomics); a unit split across CTAs is
-// finished by the CTA that arrives last on the unit's ticket, so no CTA waits
-// on another.
+// (full/empty mbarriers).  Warps 1..NCW are consumers in NCW/2 pairs: block j
+// of the CTA's share goes to pair j mod (NCW/2), each warp of the pair takes
+// 16 of the block's 32 keys and keeps an online-softmax state per unit
+// segment.  At the end of a segment every warp writes its state to a slot
+// that aliases the stage memory and the consumers combine the slots; the
+// producer waits for that merge before it reuses the stages.  A unit split
+// across CTAs is finished either by the CTA that arrives last on the unit's
+// ticket (global partials), or, when the grid is exactly two CTAs per unit,
+// by rank 0 of a 2-CTA cluster, into whose shared memory rank 1 writes its
+// partial.  No CTA ever waits on a CTA that may not be resident.
 #include <climits>
 #include <type_traits>
 
@@ -55,6 +59,7 @@ constexpr int BAR_PREFIX = 2;                 // the producer warp's block prefi
 
 constexpr int TKH = TK / 2;     // keys of a block each warp of a pair takes
 constexpr int NPAIR = NCW / 2;  // consumer warp pairs
+static_assert(NCW % 2 == 0 && NCW <= 8, "consumer warps come in pairs; the merge covers 8 heads");
 
 template <int D, bool ROTK>
 struct MmaCfg : PipeCfg<D, ROTK> {
@@ -63,17 +68,25 @@ struct MmaCfg : PipeCfg<D, ROTK> {
   static constexpr int NKB = D / 16;                      // k-blocks of the QK product
   static constexpr int HG = NGRP / 2;
   static constexpr int QSTR = D + 8;                      // padded query row (floats)
-  static constexpr int OSTR = D + 4;                      // padded output row (floats)
-  static constexpr int SLOT = 16 + 8 * OSTR;              // warp partial: m[8] l[8] o[8][OSTR]
+  static constexpr int FR = 4 * NKB;                      // O^T fragment floats per lane
+  // Warp partial: m[8], l[8], then the O^T fragment element-major: element i
+  // of lane t at 16 + 32 i + t (every access pattern below is conflict-free).
+  static constexpr int SLOT = 16 + 32 * FR;
   // Bytes after the stages (the warp slots of a segment merge alias the
   // stages), without the per-stream prefix: R(d) table, query rows, flags and
   // the merge-done barrier.
-  static constexpr int FIXED = FINE + 8 * QSTR * 4 + 16 + 16 + 32 + 2 * D * 4;
+  static constexpr int FIXED = FINE + 8 * QSTR * 4 + 10 * D * 4 + 16 + 16 + 32 + 2 * D * 4;
 };
 
-__host__ __device__ constexpr size_t mma_smem_bytes(int stage, int fixed, int ns, int S) {
-  return 1024 + (size_t)ns * stage + (size_t)fixed + (size_t)ns * 16 + (size_t)(3 * S + 1) * 4;
+// `rx`: bytes of the cluster receive area (0 without cluster merge).
+__host__ __device__ constexpr size_t mma_smem_bytes(int stage, int fixed, int ns, int S,
+                                                    int rx = 0) {
+  return 1024 + (size_t)ns * stage + (size_t)fixed + (size_t)ns * 16 + (size_t)(3 * S + 1) * 4 +
+         (rx ? 16 + 16 + (size_t)rx : 0);
 }
+// Cluster merge: rank 0 receives rank 1's NCW warp partials.
+template <int D>
+constexpr int rx_floats() { return NCW * (16 + 32 * (D / 4)); }
 
 __device__ __forceinline__ void rot(float& x, float& y, float c, float s) {
   const float a = x * c - y * s;
@@ -164,23 +177,29 @@ __device__ __forceinline__ void build_prefix_step(const AttendParams& p, int* pr
   }
 }
 
-// Fused step, every unit once (CTAs stride over the units, threads t of nt
-// share a unit): the new pair goes into its slot in the pools (this step's
-// attention takes it from the inputs and never reads that slot), and a unit
-// whose window holds only the new pair gets v_new as its output.
+// Fused step, every unit once (CTAs stride over the units, one warp per
+// unit): the new pair goes into its slot in the pools (this step's attention
+// takes it from the inputs and never reads that slot), and a unit whose window
+// holds only the new pair gets v_new as its output.  Reads the post-append
+// geometry from the CTA's cache (sa = ring start after the append, or -1 for
+// a bad state; sfill = fill after the append minus the new pair), so the new
+// pair's slot is (sa + sfill) mod W.
 template <int D>
-__device__ __forceinline__ void step_prepass(const AttendParams& p, int w, int nw, int lane) {
+__device__ __forceinline__ void step_prepass(const AttendParams& p, const int* sa,
+                                             const int* sfill, int w, int nw, int lane) {
   const int per_stream = p.L_att * p.sh.Hkv;
   const int units = p.sh.S * per_stream;
   const int esz = p.sh.bf16 ? 2 : 4;
   const int t = lane, nt = 32;   // one warp per unit
   for (int u = blockIdx.x + gridDim.x * w; u < units; u += gridDim.x * nw) {
     const int s = u / per_stream;
-    const StepState ss = step_state(p.st[s], p.sh.W);
-    if (!ss.ok) continue;
+    const int a = sa[s];
+    if (a < 0) continue;
+    int new_slot = a + sfill[s];
+    if (new_slot >= p.sh.W) new_slot -= p.sh.W;
     const int l = (u % per_stream) / p.sh.Hkv, g = u % p.sh.Hkv;
     const size_t src = (((size_t)l * p.sh.S + s) * p.sh.Hkv + g) * D;
-    const size_t dst = ((((size_t)s * p.sh.L + l) * p.sh.Hkv + g) * p.sh.W + ss.new_slot) * D;
+    const size_t dst = ((((size_t)s * p.sh.L + l) * p.sh.Hkv + g) * p.sh.W + new_slot) * D;
     const int chunks = D * esz / 16;
     for (int i = t; i < 2 * chunks; i += nt) {
       const int kv = i >= chunks, q = i - kv * chunks;
@@ -190,7 +209,7 @@ __device__ __forceinline__ void step_prepass(const AttendParams& p, int w, int n
           static_cast<uint8_t*>(kv ? p.v_pool : p.k_pool) + dst * esz) + q;
       *to = *from;
     }
-    if (ss.n2 == 1) {   // only the new pair: softmax over one key gives v_new
+    if (sfill[s] == 0) {   // only the new pair: softmax over one key gives v_new
       UnitRef ur;
       ur.s = s; ur.l = l; ur.g = g;
       for (int i = t; i < p.sh.G * D; i += nt) {
@@ -201,7 +220,7 @@ __device__ __forceinline__ void step_prepass(const AttendParams& p, int w, int n
   }
 }
 
-template <int D, bool ROTK, int STYLE, bool FUSED>
+template <int D, bool ROTK, int STYLE, bool FUSED, bool CL>
 __global__ void __launch_bounds__(MMA_THREADS, 1)
     attend_mma_decode(const __grid_constant__ AttendParams p,
                       const __grid_constant__ CUtensorMap tmK,
@@ -218,7 +237,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   float* slots = reinterpret_cast<float*>(smem);                   // [NCW][SLOT], between segments
   uint8_t* fine = stages + (size_t)NS * C::STAGE;                  // [TK][D/2] (cos, sin)
   float* qs = reinterpret_cast<float*>(fine + C::FINE);            // [8][QSTR] raw query
-  int* flag = reinterpret_cast<int*>(qs + 8 * QSTR);               // ticket, abort, issued
+  uint8_t* qraw = reinterpret_cast<uint8_t*>(qs + 8 * QSTR);       // [8][D] query, as stored
+  uint8_t* nraw = qraw + 8 * D * 4;                                // [2][D] new pair, as stored
+  int* flag = reinterpret_cast<int*>(nraw + 2 * D * 4);            // ticket, abort, issued
   uint64_t* mdone = reinterpret_cast<uint64_t*>(flag + 4);         // segment merged
   float* mx = reinterpret_cast<float*>(mdone + 2);                 // [8] new-key scores
   float* kvn = mx + 8;                                             // [2][D] new pair (fused)
@@ -227,17 +248,28 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   int* pre = reinterpret_cast<int*>(empty + NS);                   // [S+1] block prefix
   int* sa = pre + p.sh.S + 1;                                      // [S] origin mod W
   int* sfill = sa + p.sh.S;                                        // [S] fill
+  // Cluster merge (CL): the pair of CTAs that shares a unit meets here.
+  uint64_t* rx_bar = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(sfill + p.sh.S) + 15) & ~uintptr_t(15));
+  float* rslots = reinterpret_cast<float*>(rx_bar + 2);            // [NCW][SLOT] rank 1's slots
   volatile int* abort_flag = flag + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Prologue that reads nothing the previous kernel of the stream writes: the
   // barriers and the R(d) table (written once when the handle was created).
   if (tid == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(full + i), 1);
       mbar_init(smem_u32(empty + i), 2);   // both warps of the pair that takes the block
     }
     mbar_init(smem_u32(mdone), 1);
+    if constexpr (CL) {
+      // Completes once rank 1's partials (rx_floats() floats) have landed.
+      mbar_init(smem_u32(rx_bar), 1);
+      mbar_arrive_expect_tx(smem_u32(rx_bar), rx_floats<D>() * 4);
+    }
     fence_mbar_init();
     flag[1] = 0;
     flag[2] = 0;
@@ -246,6 +278,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     if (warp > 0) load_fine<D, STYLE>(p, fine, tid - 32, CONS_THREADS);
   }
   prefetch_queries(p, D);
+  // Cluster merge: the partner's barrier must exist before this CTA touches
+  // it; every thread arrives here and waits once it has work under way.
+  if constexpr (CL) cluster_arrive_relaxed();
   if constexpr (FUSED) {
     // The step's new pairs (not written by any earlier kernel of the step).
     const size_t nbytes = (size_t)p.L_att * p.sh.S * p.sh.Hkv * D * (p.sh.bf16 ? 2 : 4);
@@ -256,6 +291,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       prefetch_l2(static_cast<const uint8_t*>(p.v_new) + l * 128);
     }
   }
+  prefetch_states(p);
   pdl_wait();   // from here on: stream state, pools, queries, outputs
   // Warp 0 builds the block prefix and starts streaming at once; the
   // consumers pick the prefix up from the named barrier.
@@ -280,33 +316,75 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       flag[2] = produce<D, ROTK, QUERY_BASES>(p, &tmK, &tmV, stages, full, empty, mdone, pre, sa,
                                               sfill, rb, re, abort_flag, FUSED ? 1 : 0);
     __syncwarp();
+    if constexpr (CL) cluster_wait();
   } else {
     // ------------------------------------------------------------------ consumers
     const int cw = warp - 1, ct = tid - 32;
     const int g = lane >> 2, cq = lane & 3;   // mma fragment coordinates
-    if constexpr (FUSED)
-      step_prepass<D>(p, cw, NCW, lane);
-    else
-      zero_empty_units_cached(p, sa, sfill, ct, CONS_THREADS);
-    // Raw query of a unit into `qs` (rows >= G are zero).
-    auto load_query = [&](const UnitRef& u) {
-      for (int idx = ct; idx < 8 * D; idx += CONS_THREADS) {
-        const int h = idx / D, d = idx % D;
-        qs[h * QSTR + d] = h < G ? load_elem(p.q, row_offset(p, u, h) + d, p.sh.q_bf16) : 0.f;
+    // A unit's query rows (and, in a fused step, its new pair) reach shared
+    // memory in two steps: `stage_unit` issues 16-byte asynchronous copies of the
+    // rows as stored, `unstage_*` converts the chunks this thread copied to
+    // f32 (`qs` rows >= G stay zero; `kvn` = [k_new | v_new]).
+    const int qesz = p.sh.q_bf16 ? 2 : 4, kesz = p.sh.bf16 ? 2 : 4;
+    const int qcpr = D * qesz / 16, kcpr = D * kesz / 16;   // 16-byte chunks per row
+    auto stage_unit = [&](const UnitRef& un) {
+      for (int i = ct; i < G * qcpr; i += CONS_THREADS) {
+        const int h = i / qcpr, c = i - h * qcpr;
+        cp_async16(smem_u32(qraw + (size_t)i * 16),
+                   static_cast<const uint8_t*>(p.q) + row_offset(p, un, h) * qesz + c * 16);
+      }
+      if constexpr (FUSED) {
+        const size_t r = (((size_t)un.l * p.sh.S + un.s) * p.sh.Hkv + un.g) * D;
+        for (int i = ct; i < 2 * kcpr; i += CONS_THREADS) {
+          const int kv = i >= kcpr, c = i - kv * kcpr;
+          cp_async16(smem_u32(nraw + (size_t)i * 16),
+                     static_cast<const uint8_t*>(kv ? p.v_new : p.k_new) + r * kesz + c * 16);
+        }
+      }
+      cp_async_commit();
+    };
+    auto widen = [](const uint8_t* src, float* dst, bool bf) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src);
+      if (bf) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          dst[2 * k] = bf_lo(w[k]);
+          dst[2 * k + 1] = bf_hi(w[k]);
+        }
+      } else {
+        dst[0] = __uint_as_float(v.x);
+        dst[1] = __uint_as_float(v.y);
+        dst[2] = __uint_as_float(v.z);
+        dst[3] = __uint_as_float(v.w);
       }
     };
-    // Fused step: the unit's new pair, for the merge that adds it.
-    auto load_new = [&](const UnitRef& u) {
-      const size_t r = (((size_t)u.l * p.sh.S + u.s) * p.sh.Hkv + u.g) * D;
-      for (int idx = ct; idx < 2 * D; idx += CONS_THREADS)
-        kvn[idx] = load_elem(idx < D ? p.k_new : p.v_new, r + (idx % D), p.sh.bf16);
+    auto unstage_q = [&]() {   // waits for this thread's copies
+      cp_async_wait_all();
+      for (int i = ct; i < G * qcpr; i += CONS_THREADS) {
+        const int h = i / qcpr, c = i - h * qcpr;
+        widen(qraw + (size_t)i * 16, qs + h * QSTR + c * (16 / qesz), p.sh.q_bf16);
+      }
     };
+    auto unstage_new = [&]() {   // after unstage_q
+      for (int i = ct; i < 2 * kcpr; i += CONS_THREADS) {
+        const int kv = i >= kcpr, c = i - kv * kcpr;
+        widen(nraw + (size_t)i * 16, kvn + kv * D + c * (16 / kesz), p.sh.bf16);
+      }
+    };
+    for (int i = ct; i < (8 - G) * D; i += CONS_THREADS)
+      qs[(G + i / D) * QSTR + i % D] = 0.f;
+    if (rb < re) stage_unit(unit_of_cached(rb, p, pre, sa, sfill));
+    if constexpr (FUSED)
+      step_prepass<D>(p, sa, sfill, cw, NCW, lane);
+    else
+      zero_empty_units_cached(p, sa, sfill, ct, CONS_THREADS);
     if (rb < re) {
-      const UnitRef u0 = unit_of_cached(rb, p, pre, sa, sfill);
-      load_query(u0);
-      if constexpr (FUSED) load_new(u0);
+      unstage_q();
+      if constexpr (FUSED) unstage_new();
     }
     named_bar_sync(BAR_CONS, CONS_THREADS);
+    if constexpr (CL) cluster_wait();   // long after both CTAs arrived
 
     // Dims of the thread's A-fragment elements: k-block kb, j in {0,1,2,3}:
     //   dim 16kb + (j>>1)*8 + 2cq + (j&1)
@@ -321,19 +399,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
       const int x1 = min(u.uend, re);
       const int rq = u.fill - 1 + (FUSED ? 1 : 0);   // the query's re-based position
-      // The next segment's query: loaded now, stored once this segment is done.
+      // The next segment's query (and new pair): copied now, converted once
+      // this segment is done with `qs` (and `kvn`).
       const bool has_next = x1 < re;
-      constexpr int QPT = (8 * D + CONS_THREADS - 1) / CONS_THREADS;
-      float nq[QPT];
-      if (has_next) {
-        const UnitRef un = unit_of_cached(x1, p, pre, sa, sfill);
-#pragma unroll
-        for (int t = 0; t < QPT; ++t) {
-          const int idx = ct + t * CONS_THREADS, h = idx / D, d = idx % D;
-          nq[t] = (idx < 8 * D && h < G)
-                      ? load_elem(p.q, row_offset(p, un, h) + d, p.sh.q_bf16) : 0.f;
-        }
-      }
+      if (has_next) stage_unit(unit_of_cached(x1, p, pre, sa, sfill));
 
       // The raw query of head g (dims of the thread's A fragments), from `qs`.
       auto load_qf = [&](float (&qr)[NKB][4]) {
@@ -574,76 +643,106 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         if (stage >= NS) { stage -= NS; ++round; }
       }
 
-      // ---- segment end: merge the consumer warps (rows = heads) ----
+      // ---- segment end: merge the consumer warps ----
       // Once every consumer is done with the stages (the producer issues
-      // nothing more until the merge is over), each warp leaves (m, l, o) of
-      // its blocks in its slot, in the stage memory; after one more barrier
-      // every thread combines the NCW slots for its output elements.
+      // nothing more until the merge is over), each warp leaves (m, l, O^T)
+      // of its blocks in its slot, in the stage memory; after one more barrier
+      // every thread combines the slots for its output elements.  In a
+      // 2-CTA cluster that splits the unit, rank 1 writes its slots straight
+      // into rank 0's receive area (asynchronous stores that complete bytes on
+      // rank 0's barrier) and is done; rank 0 combines all 2*NCW slots.
       named_bar_sync(BAR_CONS, CONS_THREADS);
+      const bool whole = (x == u.ustart) && (x1 == u.uend);
+      const bool ship = CL && !whole && x != u.ustart;      // rank 1: slots go to rank 0
+      const bool receive = CL && !whole && x == u.ustart;   // rank 0: waits for them
+      // The CTA that finishes the unit adds the fused step's new pair.
+      const bool add_new = FUSED && (CL ? x == u.ustart : x1 == u.uend);
       {
         float lsum = l_run;
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-        float* my = slots + cw * C::SLOT;
-        if (cq == 0) { my[g] = m_run; my[8 + g] = lsum; }
         if constexpr (FUSED) {
           // The new pair sits at the query's own position: its score is <q, k_new>
           // (the rotations cancel).  Warp h scores head h.
-          if (x1 == u.uend && cw < G) {
+          if (add_new && cw < G) {
             float dot = 0.f;
             for (int d = lane; d < D; d += 32) dot += qs[cw * QSTR + d] * kvn[d];
             dot = warp_sum(dot);
             if (lane == 0) mx[cw] = dot * p.scale_log2;
           }
         }
-#pragma unroll
-        for (int mt = 0; mt < NKB; ++mt)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int h = 2 * cq + (j & 1);
-            const int d = 16 * mt + g + ((j >> 1) << 3);
-            my[16 + h * C::OSTR + d] = o[mt][j];
+        if (ship) {
+          const uint32_t peer = cluster_rank() ^ 1u;
+          const uint32_t dst = map_to_rank(smem_u32(rslots + cw * C::SLOT), peer);
+          const uint32_t bar = map_to_rank(smem_u32(rx_bar), peer);
+          if (cq == 0) {
+            st_async_f32(dst + 4u * g, m_run, bar);
+            st_async_f32(dst + 4u * (8 + g), lsum, bar);
           }
+#pragma unroll
+          for (int i = 0; i < C::FR; ++i)
+            st_async_f32(dst + 4u * (16 + 32 * i + lane), o[i >> 2][i & 3], bar);
+        } else {
+          float* my = slots + cw * C::SLOT;
+          if (cq == 0) { my[g] = m_run; my[8 + g] = lsum; }
+#pragma unroll
+          for (int i = 0; i < C::FR; ++i) my[16 + 32 * i + lane] = o[i >> 2][i & 3];
+        }
       }
       named_bar_sync(BAR_CONS, CONS_THREADS);
-      if (has_next) {
-#pragma unroll
-        for (int t = 0; t < QPT; ++t) {
-          const int idx = ct + t * CONS_THREADS;
-          if (idx < 8 * D) qs[(idx / D) * QSTR + idx % D] = nq[t];
-        }
-      }
+      if (has_next) unstage_q();
       const int R = p.R;   // == G for decode
-      const bool whole = (x == u.ustart) && (x1 == u.uend);
-      float* part = nullptr;
-      if (!whole) part = p.partials + (size_t)(2 * b + (x == rb ? 0 : 1)) * p.slot_floats;
-      const bool add_new = FUSED && x1 == u.uend;   // this CTA adds the new pair
-      for (int idx = ct; idx < R * D; idx += CONS_THREADS) {
-        const int h = idx / D, d = idx % D;
-        float M = add_new ? mx[h] : NEG_BIG;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) M = fmaxf(M, slots[w * C::SLOT + h]);
-        float L = 0.f, v = 0.f;
-        if (add_new) {
-          const float sc = exp2f(mx[h] - M);
-          L = sc;
-          v = sc * kvn[D + d];
-        }
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) {
-          const float* sw = slots + w * C::SLOT;
-          const float sc = exp2f(sw[h] - M);
-          L += sc * sw[8 + h];
-          v += sc * sw[16 + h * C::OSTR + d];
-        }
-        if (whole) {
-          p.out[row_offset(p, u, h) + d] = L > 0.f ? v / L : 0.f;
-        } else {
-          if (d == 0) { part[h] = M; part[R + h] = L; }
-          part[2 * R + h * D + d] = v;
+      bool got = true;
+      if (receive) {
+        got = false;
+        for (uint32_t i = 0; i < WAIT_LIMIT && !got; ++i)
+          got = mbar_try_wait_cluster(smem_u32(rx_bar), 0);
+        if (!got && ct == 0) {
+          *abort_flag = 1;
+          p.st[u.s].status = STATUS_DEVICE_STATE;
         }
       }
-      if (!whole) {
+      if (!ship && got) {
+        // Thread ct takes fragment element i of lane lf for i = ct/32, ct/32 +
+        // NCW, ...: head h = 2(lf & 3) + (i & 1) is the same for all of them.
+        const int lf = ct & 31, i0 = ct >> 5;
+        const int h = 2 * (lf & 3) + (i0 & 1);
+        const int nsl = receive ? 2 * NCW : NCW;
+        auto slot = [&](int w) { return w < NCW ? slots + w * C::SLOT : rslots + (w - NCW) * C::SLOT; };
+        float M = add_new ? mx[h] : NEG_BIG;
+        for (int w = 0; w < nsl; ++w) M = fmaxf(M, slot(w)[h]);
+        float sc[2 * NCW];
+        float L = 0.f;
+#pragma unroll
+        for (int w = 0; w < 2 * NCW; ++w) {
+          sc[w] = 0.f;
+          if (w < nsl) {
+            sc[w] = exp2f(slot(w)[h] - M);
+            L += sc[w] * slot(w)[8 + h];
+          }
+        }
+        const float scn = add_new ? exp2f(mx[h] - M) : 0.f;
+        L += scn;
+        float* part = nullptr;
+        if (!whole && !CL) {
+          part = p.partials + (size_t)(2 * b + (x == rb ? 0 : 1)) * p.slot_floats;
+          if (lf < 4 && i0 < 2 && h < R) { part[h] = M; part[R + h] = L; }
+        }
+        for (int i = i0; i < C::FR; i += NCW) {
+          const int d = 16 * (i >> 2) + (lf >> 2) + (((i >> 1) & 1) << 3);
+          float v = scn * (add_new ? kvn[D + d] : 0.f);
+#pragma unroll
+          for (int w = 0; w < 2 * NCW; ++w)
+            if (w < nsl) v += sc[w] * slot(w)[16 + 32 * i + lf];
+          if (h < R) {
+            if (whole || receive)
+              p.out[row_offset(p, u, h) + d] = L > 0.f ? v / L : 0.f;
+            else
+              part[2 * R + h * D + d] = v;
+          }
+        }
+      }
+      if (!whole && !CL) {
         // Publish this CTA's partial (one release by one thread after the
         // barrier); the last CTA of the unit to arrive merges them all.
         named_bar_sync(BAR_CONS, CONS_THREADS);
@@ -682,7 +781,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       named_bar_sync(BAR_CONS, CONS_THREADS);
       if (ct == 0) mbar_arrive(smem_u32(mdone));
       if constexpr (FUSED) {
-        if (has_next) load_new(unit_of_cached(x1, p, pre, sa, sfill));
+        if (has_next) unstage_new();
       }
       x = x1;
     }
@@ -727,6 +826,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       }
     }
   }
+  if constexpr (CL) cluster_sync_all();   // neither CTA leaves while the other may reach it
   if (tid == 0 && *abort_flag) {
     // Normally every issued stage was waited on by its consumers.  After an
     // abort, no CTA exits with a copy still in flight into its shared memory:
@@ -765,14 +865,25 @@ bool attend_mma_supported(const Shape& sh, int c) {
          attend_mma_smem(sh, c) <= (size_t)SMEM_LIMIT;
 }
 
-template <int D, bool ROTK, int STYLE, bool FUSED = false>
-static cudaError_t launch_mma_t(const AttendParams& p0, const CUtensorMap& tk,
+// The pair of CTAs that shares a unit merges through distributed shared
+// memory when every unit is cut into exactly two CTAs (one stream, grid = 2U).
+inline bool use_cluster_merge(const AttendParams& p, int grid) {
+  return p.sh.S == 1 && grid == 2 * p.L_att * p.sh.Hkv;
+}
+
+template <int D, bool ROTK, int STYLE, bool FUSED, bool CL>
+static cudaError_t launch_mma_k(const AttendParams& p0, const CUtensorMap& tk,
                                 const CUtensorMap& tv, int grid, cudaStream_t s) {
   using C = MmaCfg<D, ROTK>;
   AttendParams p = p0;
-  p.ns = mma_stages<D, ROTK>(p.sh.S);
-  const size_t smem = mma_smem_bytes(C::STAGE, C::FIXED, p.ns, p.sh.S);
-  auto kern = attend_mma_decode<D, ROTK, STYLE, FUSED>;
+  const int rx = CL ? rx_floats<D>() * 4 : 0;
+  int ns = MMA_MAX_STAGES;
+  while (ns > NPAIR && mma_smem_bytes(C::STAGE, C::FIXED, ns, p.sh.S, rx) > (size_t)SMEM_LIMIT)
+    --ns;
+  p.ns = ns;
+  const size_t smem = mma_smem_bytes(C::STAGE, C::FIXED, p.ns, p.sh.S, rx);
+  if (smem > (size_t)SMEM_LIMIT) return cudaErrorNotSupported;
+  auto kern = attend_mma_decode<D, ROTK, STYLE, FUSED, CL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -782,12 +893,23 @@ static cudaError_t launch_mma_t(const AttendParams& p0, const CUtensorMap& tk,
   cfg.blockDim = dim3(MMA_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = CL ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, p, tk, tv);
+}
+
+template <int D, bool ROTK, int STYLE, bool FUSED = false>
+static cudaError_t launch_mma_t(const AttendParams& p, const CUtensorMap& tk,
+                                const CUtensorMap& tv, int grid, cudaStream_t s) {
+  if (use_cluster_merge(p, grid)) return launch_mma_k<D, ROTK, STYLE, FUSED, true>(p, tk, tv, grid, s);
+  return launch_mma_k<D, ROTK, STYLE, FUSED, false>(p, tk, tv, grid, s);
 }
 
 template <int D>

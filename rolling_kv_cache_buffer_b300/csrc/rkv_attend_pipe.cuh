@@ -79,6 +79,15 @@ __device__ __forceinline__ void prefetch_queries(const AttendParams& p, int D) {
     prefetch_l2(static_cast<const uint8_t*>(p.q) + l * 128);
 }
 
+// Threads of the CTA bring the stream states into L2.  A prefetch reads
+// nothing into the SM, so it may run before the previous kernel that writes
+// the states has finished.
+__device__ __forceinline__ void prefetch_states(const AttendParams& p) {
+  const int lines = (p.sh.S * (int)sizeof(StreamState) + 127) / 128;
+  for (int i = threadIdx.x; i < lines; i += blockDim.x)
+    prefetch_l2(reinterpret_cast<const uint8_t*>(p.st) + (size_t)i * 128);
+}
+
 // The producer loop, run by lane 0 of warp 0 over blocks [rb, re).  Returns
 // the number of stages it filled.  Stops early (status set, *abort raised) if
 // a wait runs out.
