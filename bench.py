@@ -475,8 +475,8 @@ def main():
         kern_us = ms_local * 1e3
         achieved = bytes_local / (ms_local * 1e-3) / 1e9
     else:
-        kernel_key = "attend_mma" if args.attend_impl != "fma" and wl.kv_dtype == "bf16" else \
-            "attend_fma"
+        kernel_key = "attend_fma" if args.attend_impl == "fma" or wl.kv_dtype != "bf16" else \
+            ("attend_mma_chunk" if wl.n_new > 1 else "attend_mma")
         kern_us = att_ms * 1e3
         achieved = att_bytes / (att_ms * 1e-3) / 1e9
     line = {
