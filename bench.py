@@ -191,8 +191,9 @@ def run_gpu(args, rank, world):
         L2), then another 256 MiB read (the written lines are drained, so the
         step starts on a cold, clean L2)."""
         torch.cuda._sleep(HOST_SLACK_CYCLES)
-        flush.zero_()
-        torch.amax(drain)
+        if not args.warm_l2:
+            flush.zero_()
+            torch.amax(drain)
 
     # The fused decode step (rkv_step: one launch) wherever it applies; the
     # three calls otherwise and for the append/attend split below.
@@ -414,6 +415,8 @@ def main():
                     help="time rkv_append + rkv_rebase + rkv_attend instead of rkv_step")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end loop (short runs under ncu)")
+    ap.add_argument("--warm-l2", action="store_true",
+                    help="no L2 flush between steps (reported alongside; the default is cold)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", 0))
@@ -488,8 +491,10 @@ def main():
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
                    "kv_bytes_per_step": int(bytes_local),
-                   "l2": "between steps, outside the timed events: 256 MiB written, then "
-                         "another 256 MiB read (cold L2, no dirty lines)",
+                   "l2": ("warm: no flush between steps (inputs smaller than L2 may stay "
+                          "resident)" if args.warm_l2 else
+                          "between steps, outside the timed events: 256 MiB written, then "
+                          "another 256 MiB read (cold L2, no dirty lines)"),
                    "attend_impl": args.attend_impl, "parallelism": f"replicas x{world}",
                    "step": ("rkv_step: append + rebase + attend (all layers), one launch"
                             if res["fused"] else "rkv_append + rkv_rebase + rkv_attend "
