@@ -43,6 +43,9 @@ WORKLOAD_TEXT = {
               "1 stream, 1 token per step, full window (one eviction per step)",
     "qwen3b_stored": "as qwen3b, stored-rotated keys: append + re-rotation of all retained "
                      "keys + attend",
+    "qwen3b_epoch": "as qwen3b, stored-rotated keys re-based once every 4096 evictions "
+                    "(rebase_epoch = W): append + re-base (a no-op until the lag reaches "
+                    "W) + attend",
     "qwen3b_chunk6": "as qwen3b, 6 tokens per step (causal among the 6), 1% of k rows x2",
     "audio8": "8 layers, MHA 8 heads, head_dim 64, bf16 K/V, window 1024, 1 stream, 1 token "
               "per step, full window",
@@ -61,10 +64,13 @@ def _peaks():
 
 
 def _workload(name):
+    """(workload, key layout, re-basing epoch)."""
     from rkv_inputs import WORKLOADS
     if name == "qwen3b_stored":
-        return WORKLOADS["qwen3b"], "stored_rotated"
-    return WORKLOADS[name], "pre_rope"
+        return WORKLOADS["qwen3b"], "stored_rotated", 0
+    if name == "qwen3b_epoch":
+        return WORKLOADS["qwen3b"], "stored_rotated", WORKLOADS["qwen3b"].capacity
+    return WORKLOADS[name], "pre_rope", 0
 
 
 def _kv_bytes_per_step(wl, fills):
@@ -158,11 +164,12 @@ def run_gpu(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    wl, layout = _workload(args.workload)
+    wl, layout, epoch = _workload(args.workload)
     c = wl.n_new
     cache = RollingKV(wl.n_streams, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
                       wl.capacity, max_chunk=c, kv_dtype=wl.kv_dtype, layout=layout,
-                      rope_theta=wl.rope_theta, attend_impl=args.attend_impl, device=dev)
+                      rope_theta=wl.rope_theta, attend_impl=args.attend_impl, device=dev,
+                      rebase_epoch=epoch)
     # Steady-state windows: random contents (inputs of the path, not its work).
     gen = torch.Generator(device=dev).manual_seed(1234 + rank)
     cache.k_pool.normal_(generator=gen)
@@ -200,11 +207,36 @@ def run_gpu(args, rank, world):
     fused = layout == "pre_rope" and wl.kv_dtype == "bf16" and c == 1 and \
         args.attend_impl != "fma" and not args.no_fused
 
+    per_layer = fused and (args.per_layer or args.graph)
+    graphs = {}
+
+    def layer_calls(q, k, v):
+        for l in range(wl.n_layers):
+            cache.step_layers(l, k[l:l + 1], v[l:l + 1], q[l:l + 1], out[l:l + 1],
+                              last=(l == wl.n_layers - 1))
+
+    def graph_of(i):
+        """The per-layer calls of ring entry i, captured once in a CUDA graph."""
+        if i not in graphs:
+            q, k, v = ring[i]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                layer_calls(q, k, v)
+            graphs[i] = g
+        return graphs[i]
+
     def step(i, ev=None, split=False):
         q, k, v = ring[i % len(ring)]
+        if args.graph and fused and not split:
+            g = graph_of(i % len(ring))      # captured outside the events
         if ev:
             ev[0].record(stream)
-        if fused and not split:
+        if per_layer and not split:
+            if args.graph:
+                g.replay()
+            else:
+                layer_calls(q, k, v)
+        elif fused and not split:
             cache.step(k, v, q, out)
         else:
             cache.append(k, v)
@@ -215,13 +247,17 @@ def run_gpu(args, rank, world):
         if ev:
             ev[2].record(stream)
 
+    if args.graph and fused:
+        for i in range(len(ring)):
+            graph_of(i)
     n_done = 0
     for i in range(args.warmup):
         cold()
         step(n_done)
         n_done += 1
     torch.cuda.synchronize(dev)
-    launches_per_step = 1 if fused else 2 + (1 if layout == "stored_rotated" else 0)
+    launches_per_step = (wl.n_layers if per_layer else 1) if fused else \
+        2 + (1 if layout == "stored_rotated" else 0)
 
     # Timed region: exactly `steps` whole steps, one event pair around each.
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -332,14 +368,19 @@ class OracleRunner:
     def __init__(self, wl_name, layers=2):
         from oracle import rkv_oracle as O
         from rkv_inputs import initial_states, initial_window
-        self.wl, layout = _workload(wl_name)
+        self.wl, layout, epoch = _workload(wl_name)
         wl = self.wl
         self.S = min(wl.n_streams, 2)
         self.Ls = min(wl.n_layers, layers)
         self.stored = layout == "stored_rotated"
-        cls = O.StoredRotatedOracle if self.stored else O.RollingCacheOracle
-        self.orc = cls(self.S, self.Ls, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.capacity,
-                       theta=wl.rope_theta)
+        if self.stored and epoch:
+            self.orc = O.EpochRotatedOracle(self.S, self.Ls, wl.n_q_heads, wl.n_kv_heads,
+                                            wl.head_dim, wl.capacity, theta=wl.rope_theta,
+                                            epoch=epoch)
+        else:
+            cls = O.StoredRotatedOracle if self.stored else O.RollingCacheOracle
+            self.orc = cls(self.S, self.Ls, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                           wl.capacity, theta=wl.rope_theta)
         if wl.random_state:
             origins, fills = initial_states(wl)
         else:
@@ -415,13 +456,17 @@ def main():
                     help="time rkv_append + rkv_rebase + rkv_attend instead of rkv_step")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end loop (short runs under ncu)")
+    ap.add_argument("--per-layer", action="store_true",
+                    help="the fused step as one rkv_step_layers call per layer")
+    ap.add_argument("--graph", action="store_true",
+                    help="--per-layer, each step's calls replayed from a CUDA graph")
     ap.add_argument("--warm-l2", action="store_true",
                     help="no L2 flush between steps (reported alongside; the default is cold)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
-    wl, layout = _workload(args.workload)
+    wl, layout, _ = _workload(args.workload)
     peak, peak_kind = _peaks()
     tokens_per_step = wl.n_streams * wl.n_new
 
@@ -472,7 +517,13 @@ def main():
              "attend_us": att_ms * 1e3,
              "timing": "rkv_append + rkv_rebase and rkv_attend timed apart on extra steps "
                        "(an event between them)"}
-    if res["fused"]:
+    if res["fused"] and (args.per_layer or args.graph):
+        # One launch per layer: the step's bytes over the step's time; kernel_us
+        # is the average launch.
+        kernel_key = "attend_mma_step_layer"
+        kern_us = ms_local * 1e3 / wl.n_layers
+        achieved = bytes_local / (ms_local * 1e-3) / 1e9
+    elif res["fused"]:
         # The step is one launch of the fused kernel: its events bracket the kernel.
         kernel_key = "attend_mma_step"
         kern_us = ms_local * 1e3
@@ -496,7 +547,10 @@ def main():
                           "between steps, outside the timed events: 256 MiB written, then "
                           "another 256 MiB read (cold L2, no dirty lines)"),
                    "attend_impl": args.attend_impl, "parallelism": f"replicas x{world}",
-                   "step": ("rkv_step: append + rebase + attend (all layers), one launch"
+                   "step": (("rkv_step_layers x %d (one launch per layer%s)" %
+                             (wl.n_layers, ", replayed from a CUDA graph" if args.graph else ""))
+                            if res["fused"] and (args.per_layer or args.graph) else
+                            "rkv_step: append + rebase + attend (all layers), one launch"
                             if res["fused"] else "rkv_append + rkv_rebase + rkv_attend "
                             "(all layers)")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -65,7 +65,13 @@ typedef enum { RKV_BF16 = 0, RKV_F32 = 1 } rkv_dtype;
  * retained key by R(-e) after e evictions (rkv_rebase) -- the variant whose
  * repeated rounding "Audio8 ASR Infinite..." warns about in "Inside the
  * Rolling KV Cache and Exact RoPE Re-Basing" and "Failure Modes That Only
- * Appear on Day Three of a Session". */
+ * Appear on Day Three of a Session".  With rebase_epoch = E >= 2 the keys are
+ * instead kept rotated at (p - o_ref), where o_ref = origin - lag trails the
+ * origin by the evictions since the last re-rotation (lag < E + max_chunk);
+ * the queries take the lag into their own rotation, and rkv_rebase turns all
+ * retained keys by R(-lag) only once lag >= E: each key is rounded about
+ * W / E + 1 times in its life instead of once per eviction, and the
+ * re-rotation traffic drops by the factor E. */
 typedef enum { RKV_PRE_ROPE = 0, RKV_STORED_ROTATED = 1 } rkv_layout;
 
 /* Rotary pairing: split-half pairs element i with i + D/2 (rotate_half);
@@ -91,7 +97,9 @@ typedef struct {
   int32_t attend_impl;   /* rkv_attend_impl                                */
   double rope_theta;     /* > 1, e.g. 1e6                                  */
   float softmax_scale;   /* 0 => 1/sqrt(D)                                 */
-  int32_t reserved;      /* must be 0                                      */
+  int32_t rebase_epoch;  /* STORED_ROTATED only: 0 re-rotates at every      */
+                         /* eviction; E >= 2 re-rotates once every E        */
+                         /* evictions (see rkv_rebase); E + max_chunk <= W+1 */
 } rkv_config;
 
 typedef struct {
@@ -160,6 +168,23 @@ rkv_status rkv_rebase(rkv_handle* h, void* stream);
  * published by the last CTA of the launch to finish. */
 rkv_status rkv_step(rkv_handle* h, const void* k_new, const void* v_new, const void* q,
                     float* out, int64_t* step_log, void* stream);
+
+/* rkv_step for layers layer_begin .. layer_begin+n_layers-1 only, for a
+ * decoder that runs its layers one after another (the new K/V and the query
+ * of a layer exist only once the layer before it has run).  (The pages give
+ * no interface; this is the per-layer form of the same step.)
+ * k_new, v_new: [n_layers][S][1][H_kv][D]; q, out: [n_layers][S][1][H_q][D]
+ * (the step's tensors from layer layer_begin on).  Every call derives the
+ * step's geometry from the stream states as they were before the step, so the
+ * calls of one step may come in any order and each layer range must be passed
+ * exactly once; the call with last != 0 -- the step's final call, enqueued
+ * after all the others -- publishes the new states and fills step_log (NULL
+ * allowed).  Each call is one launch with no host synchronisation, so a
+ * step's calls can be captured in a CUDA graph.  Same support as rkv_step;
+ * a bad layer range returns RKV_ERR_INVALID_ARG. */
+rkv_status rkv_step_layers(rkv_handle* h, int32_t layer_begin, int32_t n_layers,
+                           const void* k_new, const void* v_new, const void* q, float* out,
+                           int64_t* step_log, int32_t last, void* stream);
 
 /* Size of the library-owned scratch array used by rkv_attend_static_scratch. */
 #define RKV_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)

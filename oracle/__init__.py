@@ -3,5 +3,5 @@ only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline legs use it."""
 from .rkv_oracle import *  # noqa: F401,F403
 from .rkv_oracle import (  # noqa: F401
     bf16_round, bookkeep, inv_freq, rope, softmax_attention, lse_merge,
-    softmax_partial, RollingCacheOracle, StoredRotatedOracle, rerotate,
+    softmax_partial, RollingCacheOracle, StoredRotatedOracle, EpochRotatedOracle, rerotate,
     brute_force_window, SPLIT_HALF, INTERLEAVED)

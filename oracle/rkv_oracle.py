@@ -397,6 +397,93 @@ class StoredRotatedOracle(RollingCacheOracle):
         return out
 
 
+class EpochRotatedOracle(RollingCacheOracle):
+    """Stored-rotated keys with lazy (epoch) re-basing.
+
+    Not a scheme the pages describe: a variant of their stored-rotated layout
+    that trades the every-eviction re-rotation (and its repeated rounding,
+    [LF] "Failure Modes That Only Appear on Day Three of a Session") for a
+    lag.  Keys are stored as bf16(R(p - o_ref) k), o_ref = origin' - lag, where
+    lag counts the evictions since the last re-rotation; the query at p_q is
+    turned by R(p_q - o_ref), so every query-key distance is unchanged.
+    ``rebase`` turns every retained key by R(-lag) and rounds it to bf16, once
+    lag >= epoch; an append with lag >= epoch is an error (a missed re-base).
+    """
+
+    def __init__(self, *a, epoch, **kw):
+        super().__init__(*a, **kw)
+        if epoch < 2:
+            raise ValueError("epoch >= 2")
+        self.epoch = int(epoch)
+        self.lag = [0] * self.S
+
+    def set_state(self, s, origin, fill, k=None, v=None):
+        """k holds *unrotated* keys; they are stored rotated to p - origin."""
+        super().set_state(s, origin, fill, k, v)
+        for p in list(self.window[s].keys()):
+            kk, vv = self.window[s][p]
+            self.window[s][p] = (bf16_round(rope(kk, p - origin, self.theta, self.style)), vv)
+        self.lag[s] = 0
+
+    def o_ref(self, s):
+        return self.origin[s] - self.lag[s]
+
+    def append(self, k_new, v_new):
+        k_new = np.asarray(k_new, np.float64)
+        v_new = np.asarray(v_new, np.float64)
+        c = k_new.shape[2]
+        logs = []
+        for s in range(self.S):
+            if self.lag[s] >= self.epoch:
+                raise RuntimeError("append before the due re-base")
+            bk = bookkeep(self.origin[s], self.fill[s], c, self.W)
+            for p in bk.evicted_positions:
+                del self.window[s][p]
+            lag2 = self.lag[s] + bk.evicted
+            ref = bk.origin - lag2
+            for j, p in enumerate(bk.new_positions):
+                kt = bf16_round(rope(k_new[:, s, j], p - ref, self.theta, self.style))
+                self.window[s][p] = (kt, v_new[:, s, j].copy())
+            self.origin[s], self.fill[s] = bk.origin, bk.fill
+            self.lag[s] = lag2
+            logs.append(bk.log())
+        return logs
+
+    def rebase(self):
+        """Streams whose lag reached the epoch: every retained key turns by
+        R(-lag) (float64) and is rounded to bf16; the lag returns to 0."""
+        for s in range(self.S):
+            lag = self.lag[s]
+            if lag >= self.epoch:
+                for p, (kt, vv) in list(self.window[s].items()):
+                    self.window[s][p] = (rerotate(kt, lag, self.theta, self.style), vv)
+                self.lag[s] = 0
+
+    def attend(self, q, layer_begin=0):
+        q = np.asarray(q, np.float64)
+        nl, S, c, Hq, D = q.shape
+        out = np.zeros_like(q)
+        for s in range(S):
+            pos = np.array(self.retained_positions(s), dtype=np.int64)
+            n = len(pos)
+            if n == 0:
+                continue
+            ref = self.o_ref(s)
+            for li in range(nl):
+                l = layer_begin + li
+                for g in range(self.Hkv):
+                    K = np.stack([self.window[s][p][0][l, g] for p in pos])
+                    V = np.stack([self.window[s][p][1][l, g] for p in pos])
+                    for j in range(c):
+                        pq = self.origin[s] + n - c + j
+                        vis = pos <= pq
+                        for hh in range(self.G):
+                            h = g * self.G + hh
+                            qr = rope(q[li, s, j, h], pq - ref, self.theta, self.style)
+                            out[li, s, j, h] = softmax_attention(qr, K[vis], V[vis], self.scale)
+        return out
+
+
 # ---------------------------------------------------------------------------
 # Brute force over the whole history (no ring, no re-basing)
 # ---------------------------------------------------------------------------

@@ -24,7 +24,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 rkv_status check_config(const rkv_config* c) {
   if (!c) return RKV_ERR_INVALID_ARG;
   if (c->n_streams < 1 || c->n_layers < 1 || c->n_kv_heads < 1 || c->n_q_heads < 1 ||
-      c->head_dim < 1 || c->capacity < 1 || c->max_chunk < 1 || c->reserved != 0)
+      c->head_dim < 1 || c->capacity < 1 || c->max_chunk < 1 || c->rebase_epoch < 0)
     return RKV_ERR_INVALID_ARG;
   if (c->n_q_heads % c->n_kv_heads) return RKV_ERR_INVALID_ARG;
   if (!(c->rope_theta > 1.0) || !std::isfinite(c->rope_theta)) return RKV_ERR_INVALID_ARG;
@@ -37,6 +37,10 @@ rkv_status check_config(const rkv_config* c) {
   if (c->attend_impl < RKV_ATTEND_AUTO || c->attend_impl > RKV_ATTEND_MMA)
     return RKV_ERR_INVALID_ARG;
   if (c->max_chunk > c->capacity) return RKV_ERR_CAPACITY;
+  // Lazy re-basing: positions p - o_ref stay below 2W (the RoPE table's rows).
+  if (c->rebase_epoch >= 2 &&
+      (c->layout != RKV_STORED_ROTATED || c->rebase_epoch + c->max_chunk > c->capacity + 1))
+    return RKV_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return RKV_ERR_UNSUPPORTED;
   if (c->capacity % rkv::TK || c->capacity > 65536) return RKV_ERR_UNSUPPORTED;
   if (c->n_streams > kMaxStreams) return RKV_ERR_UNSUPPORTED;
@@ -60,6 +64,7 @@ Shape make_shape(const rkv_config* c) {
   s.q_bf16 = c->q_dtype == RKV_BF16;
   s.style = c->rope_style;
   s.stored_rotated = c->layout == RKV_STORED_ROTATED;
+  s.epoch = (s.stored_rotated && c->rebase_epoch >= 2) ? c->rebase_epoch : 0;
   return s;
 }
 
@@ -294,9 +299,12 @@ rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_be
   return st;
 }
 
-rkv_status rkv_step(rkv_handle* h, const void* k_new, const void* v_new, const void* q,
-                    float* out, int64_t* step_log, void* stream) {
+rkv_status rkv_step_layers(rkv_handle* h, int32_t layer_begin, int32_t n_layers,
+                           const void* k_new, const void* v_new, const void* q, float* out,
+                           int64_t* step_log, int32_t last, void* stream) {
   if (!h || !k_new || !v_new || !q || !out) return RKV_ERR_INVALID_ARG;
+  if (layer_begin < 0 || n_layers < 1 || layer_begin + n_layers > h->sh.L)
+    return RKV_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(out) ||
       (step_log && !aligned16(step_log)))
     return RKV_ERR_INVALID_ARG;
@@ -311,8 +319,8 @@ rkv_status rkv_step(rkv_handle* h, const void* k_new, const void* v_new, const v
   p.table = reinterpret_cast<const float2*>(h->workspace + h->ws.table_off);
   p.partials = reinterpret_cast<float*>(h->workspace + h->ws.part_off);
   p.unit_tickets = reinterpret_cast<int*>(h->workspace + h->ws.unit_tk_off);
-  p.layer_begin = 0;
-  p.L_att = h->sh.L;
+  p.layer_begin = layer_begin;
+  p.L_att = n_layers;
   p.c = 1;
   p.R = h->sh.G;
   p.slot_floats = h->ws.slot_floats;
@@ -322,15 +330,22 @@ rkv_status rkv_step(rkv_handle* h, const void* k_new, const void* v_new, const v
   p.v_new = v_new;
   p.k_pool = h->k_pool;
   p.v_pool = h->v_pool;
-  p.log = reinterpret_cast<long long*>(step_log);
+  p.log = last ? reinterpret_cast<long long*>(step_log) : nullptr;
   p.step_ticket = reinterpret_cast<int*>(h->workspace + h->ws.append_tk_off);
-  const int grid = rkv::attend_grid(h, h->sh.L);
+  p.publish = last ? 1 : 0;
+  const int grid = rkv::attend_grid(h, n_layers);
   const cudaError_t e =
       rkv::launch_step_mma(p, h->tmK4, h->tmV4, grid, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return RKV_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return RKV_ERR_CUDA;
   h->last_launches = 1;
   return RKV_OK;
+}
+
+rkv_status rkv_step(rkv_handle* h, const void* k_new, const void* v_new, const void* q,
+                    float* out, int64_t* step_log, void* stream) {
+  if (!h) return RKV_ERR_INVALID_ARG;
+  return rkv_step_layers(h, 0, h->sh.L, k_new, v_new, q, out, step_log, 1, stream);
 }
 
 rkv_status rkv_rebase(rkv_handle* h, void* stream) {

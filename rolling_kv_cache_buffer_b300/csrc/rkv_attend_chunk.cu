@@ -269,8 +269,10 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             q1[kb][j] = v1.x; q1[kb][j + 1] = v1.y;
           }
         {
-          const float2* t0 = p.table + (size_t)max(rq0, 0) * HALF;
-          const float2* t1 = p.table + (size_t)max(rq1, 0) * HALF;
+          // Stored-rotated keys with a re-basing epoch sit at r + lag.
+          const int lag = p.sh.epoch ? p.st[u.s].pending : 0;
+          const float2* t0 = p.table + (size_t)(max(rq0, 0) + lag) * HALF;
+          const float2* t1 = p.table + (size_t)(max(rq1, 0) + lag) * HALF;
           if constexpr (STYLE == 0) {
 #pragma unroll
             for (int kb = 0; kb < NKB / 2; ++kb)

@@ -130,10 +130,12 @@ __global__ void __launch_bounds__(NWARP * 32, 1)
       for (int e = 0; e < DPL; ++e) o[r][e] = 0.f;
     }
     if (cb < ce) {
-      // Queries of this unit rotated to r_j = fill - c + j.
+      // Queries of this unit rotated to r_j = fill - c + j (+ the stream's lag
+      // when stored-rotated keys follow a re-basing epoch).
+      const int lag = p.sh.epoch ? p.st[u.s].pending : 0;
       for (int idx = lane; idx < R * HALF; idx += 32) {
         const int row = idx / HALF, i = idx % HALF;
-        const int rq = max(u.fill - p.c + row / G, 0);
+        const int rq = max(u.fill - p.c + row / G, 0) + lag;
         const size_t qo = row_offset(p, u, row);
         const int d1 = pair_d1(i, D, style), d2 = pair_d2(i, D, style);
         const float a = load_elem(p.q, qo + d1, p.sh.q_bf16), b = load_elem(p.q, qo + d2, p.sh.q_bf16);

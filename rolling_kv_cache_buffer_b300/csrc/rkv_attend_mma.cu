@@ -199,7 +199,8 @@ __device__ __forceinline__ void step_prepass(const AttendParams& p, const int* s
     if (new_slot >= p.sh.W) new_slot -= p.sh.W;
     const int l = (u % per_stream) / p.sh.Hkv, g = u % p.sh.Hkv;
     const size_t src = (((size_t)l * p.sh.S + s) * p.sh.Hkv + g) * D;
-    const size_t dst = ((((size_t)s * p.sh.L + l) * p.sh.Hkv + g) * p.sh.W + new_slot) * D;
+    const size_t dst =
+        ((((size_t)s * p.sh.L + p.layer_begin + l) * p.sh.Hkv + g) * p.sh.W + new_slot) * D;
     const int chunks = D * esz / 16;
     for (int i = t; i < 2 * chunks; i += nt) {
       const int kv = i >= chunks, q = i - kv * chunks;
@@ -426,8 +427,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
           qa[kb][j] = 0u;
         }
       if constexpr (!ROTK) {
-        // Stored-rotated keys sit at r already: one base, R(r_q) q.
-        const float2* t = p.table + (size_t)rq * HALF;
+        // Stored-rotated keys sit at r (+ the stream's lag, with a re-basing
+        // epoch) already: one base, R(r_q + lag) q.
+        const int lag = p.sh.epoch ? p.st[u.s].pending : 0;
+        const float2* t = p.table + (size_t)(rq + lag) * HALF;
         float qr[NKB][4];
         load_qf(qr);
         if constexpr (STYLE == 0) {
@@ -788,10 +791,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   }
   __syncthreads();
   if constexpr (FUSED) {
-    // Every CTA read the old states before it got here; the last CTA of the
-    // step to arrive publishes the new ones (the append's bookkeeping), one
-    // stream per lane of warp 0.
-    if (warp == 0) {
+    // Every CTA read the old states before it got here; on the step's last
+    // launch, the last CTA to arrive publishes the new ones (the append's
+    // bookkeeping), one stream per lane of warp 0.
+    if (warp == 0 && p.publish) {
       int last = 0;
       if (lane == 0) {
         __threadfence();

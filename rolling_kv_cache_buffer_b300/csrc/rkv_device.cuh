@@ -20,7 +20,7 @@ struct StreamState {
   long long origin;
   int fill;
   int status;     // 0, or an rkv_status code (sticky until rkv_set_stream_state)
-  int pending;    // stored-rotated: evictions of the last append not yet re-based
+  int pending;    // stored-rotated: evictions not yet re-based (the lag, with an epoch)
   int last_new;   // pairs inserted by the last append
   int ring;       // origin mod W (slot of the oldest pair), kept by every state writer
   int pad1;

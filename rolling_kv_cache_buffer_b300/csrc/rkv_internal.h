@@ -35,6 +35,7 @@ struct Shape {
   int q_bf16;                      // queries are bf16 (else f32)
   int style;                       // 0 split-half, 1 interleaved
   int stored_rotated;              // 1: keys kept rotated to (p - origin)
+  int epoch;                       // stored-rotated lazy re-basing period E (0: every eviction)
 };
 
 // Workspace carve-up (byte offsets from the workspace base).
@@ -94,6 +95,7 @@ struct AttendParams {
   void* v_pool;
   long long* log;             // nullable, [S][4]
   int* step_ticket;           // one int: CTAs done with the step
+  int publish;                // the step's last launch: publish the new states
 };
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);

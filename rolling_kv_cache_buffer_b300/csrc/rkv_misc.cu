@@ -100,9 +100,14 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
   const int part = blockIdx.x, parts = gridDim.x;
   const StreamState st = p.st[s];
   const int c = p.c, W = sh.W, D = sh.D, Hkv = sh.Hkv;
-  const bool ok = state_ok(st, W) && c >= 1 && c <= W &&
-                  !(sh.stored_rotated && st.pending != 0);
+  // Stored-rotated: re-based before this append (every eviction), or, with an
+  // epoch E, lagging by fewer than E evictions.
+  const bool rebased = !sh.stored_rotated || (sh.epoch ? st.pending < sh.epoch : st.pending == 0);
+  const bool ok = state_ok(st, W) && c >= 1 && c <= W && rebased;
   const int e = max(0, st.fill + c - W);
+  // Keys are stored rotated to p - o_ref: o_ref = o2 (every eviction) or
+  // o2 - lag2 (epoch), lag2 = the evictions since the last re-rotation.
+  const int lag2 = sh.epoch ? st.pending + e : 0;
   const long long o2 = st.origin + e;
   const int n2 = st.fill + c - e;
   const long long first = st.origin + st.fill;
@@ -158,7 +163,7 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
       }
     }
   } else if (ok) {
-    // Stored-rotated: keys are stored as R(p - origin') k, four pairs per step.
+    // Stored-rotated: keys are stored as R(p - o_ref) k, four pairs per step.
     const int quads = D / 8;
     const int lo = static_cast<int>((long long)rows * quads * part / parts);
     const int hi = static_cast<int>((long long)rows * quads * (part + 1) / parts);
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
       load_pairs(p.k_new, src, i, D, sh.style, bf, ka, kb);
       load_pairs(p.v_new, src, i, D, sh.style, bf, va, vb);
       float2 cs[4];
-      load_cs4(p.table, (size_t)(pos - o2) * (D / 2), i, cs);
+      load_cs4(p.table, (size_t)(pos - o2 + lag2) * (D / 2), i, cs);
       rotate4(ka, kb, cs, 1.f);
       store_pairs(p.k_pool, dst, i, D, sh.style, bf, ka, kb);
       store_pairs(p.v_pool, dst, i, D, sh.style, bf, va, vb);
@@ -197,7 +202,7 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
       ns.origin = o2;
       ns.fill = n2;
       ns.ring = st.ring + e < W ? st.ring + e : st.ring + e - W;
-      ns.pending = sh.stored_rotated ? e : 0;
+      ns.pending = sh.stored_rotated ? (sh.epoch ? lag2 : e) : 0;
       ns.last_new = c;
     } else if (ns.status == 0) {
       ns.status = STATUS_DEVICE_STATE;
@@ -216,16 +221,20 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
 // ----------------------------------------------------------------------------
 // K4: stored-rotated re-base.  Every retained key older than the last append is
 // turned by R(-e), e = pairs that append evicted, in f32 and rounded back to
-// the storage type.  grid = (blocks_per_stream, S).
+// the storage type.  With an epoch E, a stream is re-based only once its lag
+// (evictions since the last re-rotation) reaches E, and then every retained
+// key, new ones included, turns by R(-lag).  grid = (blocks_per_stream, S).
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) rerotate_kernel(const RerotParams p) {
   const Shape& sh = p.sh;
   const int s = blockIdx.y;
   const StreamState st = p.st[s];
   const int W = sh.W, D = sh.D, Hkv = sh.Hkv;
-  const bool work = sh.stored_rotated && state_ok(st, W) && st.pending > 0;
+  const bool work = sh.stored_rotated && state_ok(st, W) &&
+                    (sh.epoch ? st.pending >= sh.epoch : st.pending > 0);
   if (work) {
-    const int nr = st.fill - st.last_new;               // keys that predate the append
+    // Keys that predate the append (every eviction), or all of them (epoch).
+    const int nr = sh.epoch ? st.fill : st.fill - st.last_new;
     const int total = sh.L * Hkv * max(nr, 0);
     const int r0 = blockIdx.x * p.rows_per_block;
     const int r1 = min(total, r0 + p.rows_per_block);

@@ -30,7 +30,7 @@ class rkv_config(ctypes.Structure):
         ("n_kv_heads", c_int32), ("head_dim", c_int32), ("capacity", c_int32),
         ("max_chunk", c_int32), ("kv_dtype", c_int32), ("q_dtype", c_int32),
         ("layout", c_int32), ("rope_style", c_int32), ("attend_impl", c_int32),
-        ("rope_theta", c_double), ("softmax_scale", c_float), ("reserved", c_int32),
+        ("rope_theta", c_double), ("softmax_scale", c_float), ("rebase_epoch", c_int32),
     ]
 
 
@@ -67,6 +67,7 @@ def load_library():
         "rkv_attend_static_scratch": (c_int32, [P, P, P, c_int32, c_int32, c_int32, P]),
         "rkv_rebase": (c_int32, [P, P]),
         "rkv_step": (c_int32, [P, P, P, P, P, P, P]),
+        "rkv_step_layers": (c_int32, [P, c_int32, c_int32, P, P, P, P, P, c_int32, P]),
         "rkv_destroy": (c_int32, [P]),
         "rkv_set_stream_state": (c_int32, [P, c_int32, c_int64, c_int32, P]),
         "rkv_get_stream_state": (c_int32, [P, P, P, P, P]),
@@ -131,6 +132,11 @@ def rkv_rebase(h, stream):
     _check(load_library().rkv_rebase(h, stream), "rkv_rebase")
 
 
+def rkv_step_layers(h, layer_begin, n_layers, k_new, v_new, q, out, step_log, last, stream):
+    _check(load_library().rkv_step_layers(h, layer_begin, n_layers, k_new, v_new, q, out,
+                                          step_log, last, stream), "rkv_step_layers")
+
+
 def rkv_step(h, k_new, v_new, q, out, step_log, stream):
     """Fused decode step: append one pair per stream, re-base, attend all layers."""
     _check(load_library().rkv_step(h, k_new, v_new, q, out, step_log, stream), "rkv_step")
@@ -164,11 +170,12 @@ _IMPL = {"auto": RKV_ATTEND_AUTO, "fma": RKV_ATTEND_FMA, "mma": RKV_ATTEND_MMA}
 
 def make_config(n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, capacity, max_chunk=1,
                 kv_dtype="bf16", q_dtype=None, layout="pre_rope", rope_style="split_half",
-                rope_theta=1e6, softmax_scale=0.0, attend_impl="auto") -> rkv_config:
+                rope_theta=1e6, softmax_scale=0.0, attend_impl="auto",
+                rebase_epoch=0) -> rkv_config:
     return rkv_config(n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, capacity, max_chunk,
                       _DT[kv_dtype], _DT[q_dtype or kv_dtype], _LAYOUT[layout],
                       _STYLE[rope_style], _IMPL[attend_impl], float(rope_theta),
-                      float(softmax_scale), 0)
+                      float(softmax_scale), int(rebase_epoch))
 
 
 class RollingKV:
@@ -177,12 +184,12 @@ class RollingKV:
     def __init__(self, n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, capacity,
                  max_chunk=1, kv_dtype="bf16", q_dtype=None, layout="pre_rope",
                  rope_style="split_half", rope_theta=1e6, softmax_scale=0.0,
-                 attend_impl="auto", device="cuda"):
+                 attend_impl="auto", device="cuda", rebase_epoch=0):
         import torch
         self.torch = torch
         self.cfg = make_config(n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, capacity,
                                max_chunk, kv_dtype, q_dtype, layout, rope_style, rope_theta,
-                               softmax_scale, attend_impl)
+                               softmax_scale, attend_impl, rebase_epoch)
         pool_b, state_b, ws_b = rkv_required_bytes(self.cfg)
         self.kv_dtype = torch.bfloat16 if kv_dtype == "bf16" else torch.float32
         self.q_dtype = torch.bfloat16 if (q_dtype or kv_dtype) == "bf16" else torch.float32
@@ -248,6 +255,24 @@ class RollingKV:
             lp = step_log.data_ptr()
         rkv_step(self.handle, k_new.data_ptr(), v_new.data_ptr(), q.data_ptr(), out.data_ptr(),
                  lp, self._stream())
+        return out
+
+    def step_layers(self, layer_begin, k_new, v_new, q, out, last, step_log=None):
+        """The step for layers layer_begin .. layer_begin + n - 1 (n = k_new's
+        first dimension): each layer range of a step once, `last` on the final
+        call (it publishes the new stream states)."""
+        n = k_new.shape[0]
+        shp = (n, self.S, 1, self.Hkv, self.D)
+        self._need(k_new, shp, self.kv_dtype, "k_new")
+        self._need(v_new, shp, self.kv_dtype, "v_new")
+        self._need(q, (n, self.S, 1, self.Hq, self.D), self.q_dtype, "q")
+        self._need(out, tuple(q.shape), self.torch.float32, "out")
+        lp = 0
+        if step_log is not None:
+            self._need(step_log, (self.S, 4), self.torch.int64, "step_log")
+            lp = step_log.data_ptr()
+        rkv_step_layers(self.handle, layer_begin, n, k_new.data_ptr(), v_new.data_ptr(),
+                        q.data_ptr(), out.data_ptr(), lp, 1 if last else 0, self._stream())
         return out
 
     def set_stream_state(self, s, origin, fill):

@@ -64,11 +64,22 @@ def test_required_bytes_closed_form(name):
     (dict(n_streams=0), R.rkv.RKV_ERR_INVALID_ARG),
     (dict(rope_theta=1.0), R.rkv.RKV_ERR_INVALID_ARG),
     (dict(n_streams=2000), R.rkv.RKV_ERR_UNSUPPORTED),
+    (dict(rebase_epoch=-1), R.rkv.RKV_ERR_INVALID_ARG),
+    (dict(rebase_epoch=64), R.rkv.RKV_ERR_INVALID_ARG),                       # pre-RoPE
+    (dict(layout="stored_rotated", rebase_epoch=4096, max_chunk=2), R.rkv.RKV_ERR_INVALID_ARG),
 ])
 def test_config_rejected(kw, status):
     with pytest.raises(R.RkvError) as e:
         R.rkv_required_bytes(_cfg(**kw))
     assert e.value.status == status
+
+
+def test_rebase_epoch_bounds_accepted():
+    # an epoch E needs E + max_chunk <= W + 1 (positions p - o_ref stay below 2W)
+    R.rkv_required_bytes(_cfg(layout="stored_rotated", rebase_epoch=4096))
+    R.rkv_required_bytes(_cfg(layout="stored_rotated", rebase_epoch=4090, max_chunk=7))
+    R.rkv_required_bytes(_cfg(layout="stored_rotated", rebase_epoch=0))
+    R.rkv_required_bytes(_cfg(layout="stored_rotated", rebase_epoch=1))   # 1 = every eviction
 
 
 def test_create_rejects_null_and_misaligned_buffers_without_gpu():

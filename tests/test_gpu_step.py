@@ -96,3 +96,91 @@ def test_step_unsupported_layouts_are_refused():
     with pytest.raises(RkvError) as e:
         cache.step(dev(k, torch.bfloat16), dev(v, torch.bfloat16), dev(q, torch.bfloat16))
     assert e.value.status == RKV_ERR_UNSUPPORTED
+
+
+# ----------------------------------------------------------------------------
+# Per-layer form of the step (rkv_step_layers), also under a CUDA graph
+# ----------------------------------------------------------------------------
+
+def _layer_calls(cache, kd, vd, qd, out, order, log=None):
+    """One step as one rkv_step_layers call per layer, in `order`; the last
+    call publishes."""
+    for i, l in enumerate(order):
+        cache.step_layers(l, kd[l:l + 1], vd[l:l + 1], qd[l:l + 1], out[l:l + 1],
+                          last=(i == len(order) - 1), step_log=log)
+
+
+@pytest.mark.parametrize("order", ["forward", "reverse"])
+def test_step_layers_equals_step(order):
+    """Per-layer calls (any order, the last one publishing) leave the same
+    pools, states and logs as rkv_step, and outputs within float rounding of
+    it (the two launch shapes split the windows differently)."""
+    wl = WORKLOADS["qwen3b"].replace(n_layers=4, capacity=128)
+    whole = make_cache(wl)
+    per = make_cache(wl)
+    orc = make_oracle(wl)
+    L = wl.n_layers
+    seq = list(range(L)) if order == "forward" else list(reversed(range(L)))
+    log_a = torch.zeros((1, 4), dtype=torch.int64, device="cuda")
+    log_b = torch.zeros((1, 4), dtype=torch.int64, device="cuda")
+    for t in range(1, 2 * wl.capacity + 10):
+        q, k, v = step_inputs(wl, t)
+        qd, kd, vd = dev(q, torch.bfloat16), dev(k, torch.bfloat16), dev(v, torch.bfloat16)
+        a = whole.step(kd, vd, qd, step_log=log_a)
+        b = torch.empty_like(a)
+        # intermediate calls must leave the state alone
+        st0 = per.state.clone()
+        per.step_layers(seq[0], kd[seq[0]:seq[0] + 1], vd[seq[0]:seq[0] + 1],
+                        qd[seq[0]:seq[0] + 1], b[seq[0]:seq[0] + 1], last=False)
+        assert torch.equal(per.state, st0)
+        _layer_calls(per, kd, vd, qd, b, seq[1:], log=log_b)
+        orc.append(k.double().numpy(), v.double().numpy())
+        assert torch.equal(log_a, log_b), f"step {t}"
+        if t % 11 == 0 or t in (1, 2, 127, 128, 129):
+            assert torch.allclose(a, b, atol=1e-5, rtol=0), f"step {t}"
+            compare(b, orc.attend(q.double().numpy()))
+    assert torch.equal(whole.k_pool, per.k_pool) and torch.equal(whole.v_pool, per.v_pool)
+    assert torch.equal(whole.state, per.state)
+
+
+def test_step_layers_in_a_cuda_graph():
+    """A step's per-layer calls captured once in a CUDA graph and replayed
+    every step (inputs copied into the graph's static buffers) give the same
+    results as the same calls made eagerly."""
+    wl = WORKLOADS["qwen3b"].replace(n_layers=3, capacity=64)
+    eager = make_cache(wl)
+    graphed = make_cache(wl)
+    L = wl.n_layers
+    q0, k0, v0 = step_inputs(wl, 1)
+    qs, ks, vs = dev(q0, torch.bfloat16), dev(k0, torch.bfloat16), dev(v0, torch.bfloat16)
+    outs = torch.zeros(q0.shape, dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        _layer_calls(graphed, ks, vs, qs, outs, list(range(L)))   # warm-up (step 1)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _layer_calls(graphed, ks, vs, qs, outs, list(range(L)))
+    e1 = torch.empty_like(outs)
+    _layer_calls(eager, ks, vs, qs, e1, list(range(L)))           # eager step 1
+    for t in range(2, 150):
+        q, k, v = step_inputs(wl, t)
+        qd, kd, vd = dev(q, torch.bfloat16), dev(k, torch.bfloat16), dev(v, torch.bfloat16)
+        ref = torch.empty_like(outs)
+        _layer_calls(eager, kd, vd, qd, ref, list(range(L)))
+        qs.copy_(qd), ks.copy_(kd), vs.copy_(vd)
+        g.replay()
+        assert torch.equal(outs, ref), f"step {t}"
+    assert torch.equal(eager.k_pool, graphed.k_pool) and torch.equal(eager.state, graphed.state)
+
+
+def test_step_layers_bad_range():
+    wl = WORKLOADS["qwen3b"].replace(n_layers=2, capacity=64)
+    cache = make_cache(wl)
+    q, k, v = step_inputs(wl, 1)
+    qd, kd, vd = dev(q, torch.bfloat16), dev(k, torch.bfloat16), dev(v, torch.bfloat16)
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    from rolling_kv_cache_buffer_b300 import RkvError
+    with pytest.raises(RkvError):
+        cache.step_layers(1, kd, vd, qd, out, last=True)      # layers 1..2 of 2
