@@ -124,7 +124,7 @@ __device__ __forceinline__ void rotate_unit(uint8_t* kt, int d, int m, const flo
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int i = 8 * m + 2 * t;          // pairs i, i+1
-      const float4 ds = *reinterpret_cast<const float4*>(frow + fine_chunk<D>(d, i >> 1));
+      const float4 ds = *reinterpret_cast<const float4*>(frow + fine_chunk_keys<D>(d, i >> 1));
       const float4 bs = *reinterpret_cast<const float4*>(tb + i);
       rot_pair2_composed(xw[t], yw[t], bs, sg, ds);
     }
@@ -137,7 +137,7 @@ __device__ __forceinline__ void rotate_unit(uint8_t* kt, int d, int m, const flo
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int i = 4 * m + t;              // the pair in word t
-      const float2 cd = *reinterpret_cast<const float2*>(frow + fine_chunk<D>(d, i >> 1) +
+      const float2 cd = *reinterpret_cast<const float2*>(frow + fine_chunk_keys<D>(d, i >> 1) +
                                                         ((i & 1) << 3));
       const float2 cb = tb[i];
       const float cbs = sg * cb.y;
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     flag[2] = 0;
   }
   if constexpr (ROTK) {
-    if (warp > 0) load_fine<D, STYLE>(p, fine, tid - 32, CCONS);
+    if (warp > 0) load_fine<D, STYLE, true>(p, fine, tid - 32, CCONS);
   }
   prefetch_queries(p, D);
   prefetch_states(p);
@@ -347,7 +347,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             const float2* trA = reinterpret_cast<const float2*>(ktw + 2 * TILE);
             constexpr int UPK = STYLE == 0 ? D / 16 : D / 8;   // units per key
             for (int un = rg * 32 + lane; un < TK * UPK; un += RG * 32) {
-              const int d = un / UPK, m = un % UPK;
+              // Keys fastest: eight lanes take keys d..d+7 of the same chunk m,
+              // which the tile swizzle and the table layout spread over all banks.
+              const int d = un % TK, m = un / TK;
               const bool useB = d >= wrap_at;                  // past the ring's end
               rotate_unit<D, STYLE>(ktw, d, m, useB ? trA + HALF : trA, useB ? -1.f : 1.f,
                                     fine + d * HALF * 8);
@@ -534,11 +536,13 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
           for (int idx = ct; idx < R * D; idx += CCONS) {
             const int row = idx / D, d = idx % D;
             float M = NEG_BIG;
+#pragma unroll 8
             for (int bb = b0; bb <= b1; ++bb) {
               const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
               M = fmaxf(M, __ldcg(p.partials + (size_t)(2 * bb + k) * p.slot_floats + row));
             }
             float num = 0.f, den = 0.f;
+#pragma unroll 8
             for (int bb = b0; bb <= b1; ++bb) {
               const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
               const float* pp = p.partials + (size_t)(2 * bb + k) * p.slot_floats;

@@ -761,11 +761,15 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
           for (int idx = ct; idx < R * D; idx += CONS_THREADS) {
             const int h = idx / D, d = idx % D;
             float M = NEG_BIG;
+            // Unrolled so that the partials' loads overlap instead of paying
+            // one L2 round trip each.
+#pragma unroll 8
             for (int bb = b0; bb <= b1; ++bb) {
               const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
               M = fmaxf(M, __ldcg(p.partials + (size_t)(2 * bb + k) * p.slot_floats + h));
             }
             float num = 0.f, den = 0.f;
+#pragma unroll 8
             for (int bb = b0; bb <= b1; ++bb) {
               const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
               const float* pp = p.partials + (size_t)(2 * bb + k) * p.slot_floats;

@@ -54,9 +54,17 @@ __device__ __forceinline__ uint32_t fine_chunk(int d, int k) {
   return static_cast<uint32_t>((k ^ ((d & (NCH / 4 - 1)) << 2)) << 4);
 }
 
+// The chunk kernel's layout of the same table: chunk k of row d at position
+// k ^ (d mod 8), so that eight keys d..d+7 reading the same chunk k (one phase
+// of a 128-bit load) hit eight different 16-byte bank groups.
+template <int D>
+__device__ __forceinline__ uint32_t fine_chunk_keys(int d, int k) {
+  return static_cast<uint32_t>((k ^ (d & 7)) << 4);
+}
+
 // Threads t0, t0+nt, ... fill the fine table from rows 0..TK-1 of the global
-// (cos, sin) table.
-template <int D, int STYLE>
+// (cos, sin) table (KEYS: in the chunk kernel's layout).
+template <int D, int STYLE, bool KEYS = false>
 __device__ __forceinline__ void load_fine(const AttendParams& p, uint8_t* fine, int t0, int nt) {
   constexpr int HALF = D / 2;
   for (int idx = t0; idx < TK * HALF / 2; idx += nt) {
@@ -65,7 +73,8 @@ __device__ __forceinline__ void load_fine(const AttendParams& p, uint8_t* fine, 
     const float2 c = __ldg(p.table + (size_t)d * HALF + 2 * k + 1);
     const float4 v = STYLE == 0 ? make_float4(a.x, c.x, a.y, c.y)
                                 : make_float4(a.x, a.y, c.x, c.y);
-    *reinterpret_cast<float4*>(fine + d * HALF * 8 + fine_chunk<D>(d, k)) = v;
+    *reinterpret_cast<float4*>(fine + d * HALF * 8 +
+                               (KEYS ? fine_chunk_keys<D>(d, k) : fine_chunk<D>(d, k))) = v;
   }
 }
 

@@ -27,6 +27,8 @@ struct rkv_handle {
 namespace rkv {
 // Largest persistent grid of the attention kernels.
 constexpr int kMaxCtas = 1024;
+// Fewest blocks of a full window per CTA when a unit is split across CTAs.
+constexpr int kMinBlocksPerCta = 8;
 
 // Persistent grid of an attention call over n_layers layers.  The block list
 // is cut into equal shares, CTA b taking [b*T/P, (b+1)*T/P).  With one stream
@@ -37,7 +39,15 @@ constexpr int kMaxCtas = 1024;
 inline int attend_grid(const rkv_handle* h, int n_layers) {
   const int sms = h->num_sms < kMaxCtas ? h->num_sms : kMaxCtas;
   const int units = n_layers * h->sh.Hkv;
-  if (h->sh.S == 1 && units <= sms) return units * (sms / units);
+  if (h->sh.S == 1 && units <= sms) {
+    // Every unit cut into the same number of CTAs, each with at least
+    // kMinBlocksPerCta of a full window's blocks: a launch over few units (one
+    // layer) streams its few MB from a few dozen SMs and merges few partials.
+    int per = sms / units;
+    const int cap = h->sh.NB / kMinBlocksPerCta;
+    if (per > cap) per = cap > 1 ? cap : 1;
+    return units * per;
+  }
   return sms;
 }
 
