@@ -425,14 +425,17 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             m_run[rw] = mnew;
           }
           // o columns of this thread: rows nt*8 + 2cq (+1); their alphas sit in
-          // quads 2cq and 2cq+1.
+          // quads 2cq and 2cq+1.  Once the running maxima settle, most blocks
+          // raise none of them: every alpha is 1 and the rescale is skipped.
+          if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const float ae = __shfl_sync(0xffffffffu, alpha[nt], 8 * cq);
-            const float ao = __shfl_sync(0xffffffffu, alpha[nt], 8 * cq + 4);
+            for (int nt = 0; nt < 2; ++nt) {
+              const float ae = __shfl_sync(0xffffffffu, alpha[nt], 8 * cq);
+              const float ao = __shfl_sync(0xffffffffu, alpha[nt], 8 * cq + 4);
 #pragma unroll
-            for (int mt = 0; mt < NKB; ++mt) {
-              o[mt][nt][0] *= ae; o[mt][nt][1] *= ao; o[mt][nt][2] *= ae; o[mt][nt][3] *= ao;
+              for (int mt = 0; mt < NKB; ++mt) {
+                o[mt][nt][0] *= ae; o[mt][nt][1] *= ao; o[mt][nt][2] *= ae; o[mt][nt][3] *= ao;
+              }
             }
           }
           // ---- O^T += V^T P^T ----
@@ -453,13 +456,23 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
               mhi = (ok(d0 + 8) ? 0x0000ffffu : 0u) | (ok(d0 + 9) ? 0xffff0000u : 0u);
             }
             const int vrow = 16 * kk + ((lane >> 4) << 3) + (lane & 7);
+            if (allvalid) {
 #pragma unroll
-            for (int mt = 0; mt < NKB; ++mt) {
-              uint32_t v0, v1, v2, v3;
-              ldsm_x4_t(vt_s + tile_swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
-              v0 &= mlo; v1 &= mlo; v2 &= mhi; v3 &= mhi;
-              mma_bf16(o[mt][0], v0, v1, v2, v3, bb[0][0], bb[0][1]);
-              mma_bf16(o[mt][1], v0, v1, v2, v3, bb[1][0], bb[1][1]);
+              for (int mt = 0; mt < NKB; ++mt) {
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_t(vt_s + tile_swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
+                mma_bf16(o[mt][0], v0, v1, v2, v3, bb[0][0], bb[0][1]);
+                mma_bf16(o[mt][1], v0, v1, v2, v3, bb[1][0], bb[1][1]);
+              }
+            } else {
+#pragma unroll
+              for (int mt = 0; mt < NKB; ++mt) {
+                uint32_t v0, v1, v2, v3;
+                ldsm_x4_t(vt_s + tile_swz(vrow, 2 * mt + ((lane >> 3) & 1)), v0, v1, v2, v3);
+                v0 &= mlo; v1 &= mlo; v2 &= mhi; v3 &= mhi;
+                mma_bf16(o[mt][0], v0, v1, v2, v3, bb[0][0], bb[0][1]);
+                mma_bf16(o[mt][1], v0, v1, v2, v3, bb[1][0], bb[1][1]);
+              }
             }
           }
           __syncwarp();

@@ -59,7 +59,7 @@ constexpr int BAR_PREFIX = 2;                 // the producer warp's block prefi
 
 constexpr int TKH = TK / 2;     // keys of a block each warp of a pair takes
 constexpr int NPAIR = NCW / 2;  // consumer warp pairs
-static_assert(NCW % 2 == 0 && NCW <= 8, "consumer warps come in pairs; the merge covers 8 heads");
+static_assert(NCW % 2 == 0, "consumer warps come in pairs");
 
 template <int D, bool ROTK>
 struct MmaCfg : PipeCfg<D, ROTK> {
@@ -603,11 +603,15 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             }
           l_run = l_run * alpha + psum;
           m_run = mnew;
-          const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * cq);      // head 2cq
-          const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * cq + 4);  // head 2cq+1
+          // Most blocks raise no running maximum once it settles: then every
+          // alpha is 1 and the rescale is skipped.
+          if (!__all_sync(0xffffffffu, alpha == 1.f)) {
+            const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * cq);      // head 2cq
+            const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * cq + 4);  // head 2cq+1
 #pragma unroll
-          for (int mt = 0; mt < NKB; ++mt) {
-            o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
+            for (int mt = 0; mt < NKB; ++mt) {
+              o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
+            }
           }
           // ---- O^T += V^T P^T over the 16 keys of this half ----
           {
