@@ -8,6 +8,7 @@ import math
 import numpy as np
 import pytest
 import torch
+from hypothesis import given, settings, strategies as st
 
 import oracle as O
 
@@ -120,3 +121,27 @@ def test_epoch_bounds_the_drift_of_stored_keys():
     e_lazy = err(lazy, lazy.o_ref(0))
     assert e_lazy <= 3 * 2.0 ** -8
     assert e_eager > 4 * e_lazy
+
+
+
+@settings(max_examples=40, deadline=None)
+@given(W=st.sampled_from([8, 16, 32]), c=st.integers(1, 3), data=st.data())
+def test_epoch_lag_and_positions_stay_bounded(W, c, data):
+    """For any epoch E with E + c <= W + 1: after an append the lag is below
+    E + c, every stored position p - o_ref lies in [0, 2W) (the RoPE table's
+    rows), and a re-base leaves the lag below E; bookkeeping is the plain one."""
+    E = data.draw(st.integers(2, W + 1 - c))
+    steps = data.draw(st.integers(1, 5 * W // c))
+    o = O.EpochRotatedOracle(1, 1, 2, 1, 4, W, epoch=E)
+    origin, fill = 0, 0
+    for _ in range(steps):
+        kv = np.zeros((1, 1, c, 1, 4))
+        o.append(kv, kv)
+        bk = O.bookkeep(origin, fill, c, W)
+        origin, fill = bk.origin, bk.fill
+        assert (o.origin[0], o.fill[0]) == (origin, fill)
+        assert 0 <= o.lag[0] < E + c
+        ref = o.o_ref(0)
+        assert all(0 <= p - ref < 2 * W for p in o.retained_positions(0))
+        o.rebase()
+        assert o.lag[0] < E
