@@ -21,7 +21,8 @@
 //    b - a);
 //  * the S accumulator fragment is exactly the B fragment P^T of the second
 //    product, so probabilities never leave registers.
-// Stored-rotated keys skip the key rotation and use R(r_q) q alone.
+// Stored-rotated keys skip the key rotation and use R(r_q + lag) q alone (lag
+// = 0 unless the keys follow a re-basing epoch).
 //
 // Pipeline (one persistent CTA per SM).  Warp 0 is the producer: one lane
 // walks the CTA's share of the block list and streams every block's K and V
@@ -35,8 +36,13 @@
 // producer waits for that merge before it reuses the stages.  A unit split
 // across CTAs is finished either by the CTA that arrives last on the unit's
 // ticket (global partials), or, when the grid is exactly two CTAs per unit,
-// by rank 0 of a 2-CTA cluster, into whose shared memory rank 1 writes its
-// partial.  No CTA ever waits on a CTA that may not be resident.
+// by rank 0 of a 2-CTA cluster, into whose shared memory the warps of rank 1
+// write their slots.  No CTA ever waits on a CTA that may not be resident.
+//
+// Fused step (FUSED): the same kernel also appends one pair per stream -- the
+// geometry after the append comes from the old state, a prepass writes the
+// new rows, the CTA that finishes a unit adds the new pair from the inputs,
+// and the step's last launch publishes the new states.
 #include <climits>
 #include <type_traits>
 

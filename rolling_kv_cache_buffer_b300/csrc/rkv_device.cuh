@@ -97,9 +97,9 @@ __device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 // Thread-block clusters: rank of this CTA, the shared::cluster address of a
-// shared-memory word in CTA `rank`, an arrival on such a remote mbarrier
-// (release at cluster scope), a local wait that acquires at cluster scope, and
-// the cluster-wide barrier.
+// shared-memory word in CTA `rank`, asynchronous stores into a partner CTA's
+// shared memory, a local wait that acquires at cluster scope, and the
+// cluster-wide barrier.
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -110,18 +110,11 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
-}
 // Asynchronous 4-byte store into another CTA's shared memory that counts its
 // bytes on that CTA's mbarrier (complete_tx).
 __device__ __forceinline__ void st_async_f32(uint32_t cluster_addr, float v, uint32_t cluster_bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
                ::"r"(cluster_addr), "r"(__float_as_uint(v)), "r"(cluster_bar)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -161,10 +154,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // Hint: bring the 128-byte line holding p into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-// Shared-memory float atomic add (no return value).
-__device__ __forceinline__ void red_add_shared(float* addr, float v) {
-  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_u32(addr)), "f"(v) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

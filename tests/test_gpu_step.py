@@ -184,3 +184,36 @@ def test_step_layers_bad_range():
     from rolling_kv_cache_buffer_b300 import RkvError
     with pytest.raises(RkvError):
         cache.step_layers(1, kd, vd, qd, out, last=True)      # layers 1..2 of 2
+
+
+def test_step_layers_many_streams():
+    """Per-layer calls over eight streams with fills 0 .. W and scattered
+    origins (several units per CTA, split units merged through global
+    partials): every stream's outputs against the oracle, states published by
+    the last call only."""
+    wl = WORKLOADS["qwen3b"].replace(n_streams=8, n_layers=3, capacity=256)
+    fills = [0, 1, 5, 31, 32, 33, 200, 256]
+    origins = [0, 7, 250, 1000, 77, 12345, 999_999, 256 * 9 + 3]
+    cache = make_cache(wl)
+    orcs = []
+    for s in range(8):
+        k = random_rows((3, 2, fills[s], 128), 700 + s, torch.bfloat16)
+        v = random_rows((3, 2, fills[s], 128), 800 + s, torch.bfloat16)
+        write_window(cache, s, origins[s], fills[s], k, v)
+        orc = make_oracle(wl, n_streams=1)
+        orc.set_state(0, origins[s], fills[s], k.double().numpy(), v.double().numpy())
+        orcs.append(orc)
+    for t in range(1, 4):
+        q, k, v = step_inputs(wl, t)
+        qd, kd, vd = dev(q, torch.bfloat16), dev(k, torch.bfloat16), dev(v, torch.bfloat16)
+        out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+        st0 = cache.state.clone()
+        cache.step_layers(0, kd[0:2], vd[0:2], qd[0:2], out[0:2], last=False)
+        assert torch.equal(cache.state, st0)
+        cache.step_layers(2, kd[2:3], vd[2:3], qd[2:3], out[2:3], last=True)
+        for s in range(8):
+            orcs[s].append(k[:, s:s + 1].double().numpy(), v[:, s:s + 1].double().numpy())
+            compare(out[:, s:s + 1], orcs[s].attend(q[:, s:s + 1].double().numpy()))
+        o, f, _ = cache.get_stream_state()
+        assert [int(x) for x in f] == [orcs[s].fill[0] for s in range(8)]
+        assert [int(x) for x in o] == [orcs[s].origin[0] for s in range(8)]
