@@ -392,6 +392,46 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     }
     named_bar_sync(BAR_CONS, CONS_THREADS);
     if constexpr (CL) cluster_wait();   // long after both CTAs arrived
+    if constexpr (FUSED) {
+      // Every CTA reads the old states in its prologue and keeps what it needs
+      // in shared memory; once all have, the last CTA past this point
+      // publishes the new ones (the append's bookkeeping), one stream per
+      // lane of the last consumer warp, on the step's last launch only.
+      if (cw == NCW - 1 && p.publish) {
+        int last = 0;
+        if (lane == 0) {
+          __threadfence();
+          last = atomicAdd(p.step_ticket, 1) == static_cast<int>(gridDim.x) - 1;
+          if (last) __threadfence();
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          for (int s2 = lane; s2 < p.sh.S; s2 += 32) {
+            const StreamState st = p.st[s2];
+            const StepState ss = step_state(st, W);
+            StreamState ns = st;
+            if (ss.ok) {
+              ns.origin = st.origin + ss.e;
+              ns.fill = ss.n2;
+              ns.ring = ss.ring2;
+              ns.pending = 0;
+              ns.last_new = 1;
+            } else if (ns.status == 0) {
+              ns.status = STATUS_DEVICE_STATE;
+            }
+            p.st[s2] = ns;
+            if (p.log) {
+              long long* lg = p.log + 4 * (size_t)s2;
+              lg[0] = ss.ok ? ns.origin : st.origin;
+              lg[1] = ss.ok ? ns.fill : st.fill;
+              lg[2] = ss.ok ? ss.e : -1;
+              lg[3] = ss.ok ? ss.new_slot : -1;
+            }
+          }
+          if (lane == 0) *p.step_ticket = 0;
+        }
+      }
+    }
 
     // Dims of the thread's A-fragment elements: k-block kb, j in {0,1,2,3}:
     //   dim 16kb + (j>>1)*8 + 2cq + (j&1)
@@ -804,45 +844,6 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     }
   }
   __syncthreads();
-  if constexpr (FUSED) {
-    // Every CTA read the old states before it got here; on the step's last
-    // launch, the last CTA to arrive publishes the new ones (the append's
-    // bookkeeping), one stream per lane of warp 0.
-    if (warp == 0 && p.publish) {
-      int last = 0;
-      if (lane == 0) {
-        __threadfence();
-        last = atomicAdd(p.step_ticket, 1) == static_cast<int>(gridDim.x) - 1;
-        if (last) __threadfence();
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        for (int s2 = lane; s2 < p.sh.S; s2 += 32) {
-          const StreamState st = p.st[s2];
-          const StepState ss = step_state(st, W);
-          StreamState ns = st;
-          if (ss.ok) {
-            ns.origin = st.origin + ss.e;
-            ns.fill = ss.n2;
-            ns.ring = ss.ring2;
-            ns.pending = 0;
-            ns.last_new = 1;
-          } else if (ns.status == 0) {
-            ns.status = STATUS_DEVICE_STATE;
-          }
-          p.st[s2] = ns;
-          if (p.log) {
-            long long* lg = p.log + 4 * (size_t)s2;
-            lg[0] = ss.ok ? ns.origin : st.origin;
-            lg[1] = ss.ok ? ns.fill : st.fill;
-            lg[2] = ss.ok ? ss.e : -1;
-            lg[3] = ss.ok ? ss.new_slot : -1;
-          }
-        }
-        if (lane == 0) *p.step_ticket = 0;
-      }
-    }
-  }
   if constexpr (CL) cluster_sync_all();   // neither CTA leaves while the other may reach it
   if (tid == 0 && *abort_flag) {
     // Normally every issued stage was waited on by its consumers.  After an
