@@ -81,7 +81,11 @@ struct MmaCfg : PipeCfg<D, ROTK> {
   // Bytes after the stages (the warp slots of a segment merge alias the
   // stages), without the per-stream prefix: R(d) table, query rows, flags and
   // the merge-done barrier.
-  static constexpr int FIXED = FINE + 8 * QSTR * 4 + 10 * D * 4 + 16 + 16 + 32 + 2 * D * 4;
+  // Query-base rows (cos, sin) of every consumer warp's current block and of
+  // its wrap base, and the two constant steps R(-NPAIR*TK) and R(W).
+  static constexpr int QROWS = ROTK ? (2 * NCW + 2) * (D / 2) * 8 : 0;
+  static constexpr int FIXED =
+      FINE + QROWS + 8 * QSTR * 4 + 10 * D * 4 + 16 + 16 + 32 + 2 * D * 4;
 };
 
 // `rx`: bytes of the cluster receive area (0 without cluster merge).
@@ -243,7 +247,11 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   uint8_t* stages = smem;                                          // [NS][STAGE]
   float* slots = reinterpret_cast<float*>(smem);                   // [NCW][SLOT], between segments
   uint8_t* fine = stages + (size_t)NS * C::STAGE;                  // [TK][D/2] (cos, sin)
-  float* qs = reinterpret_cast<float*>(fine + C::FINE);            // [8][QSTR] raw query
+  float2* qrow = reinterpret_cast<float2*>(fine + C::FINE);        // [NCW][D/2] R(r_q - r0)
+  float2* wrow = qrow + NCW * (D / 2);                             // [NCW][D/2] R(r_q - r0 + W)
+  float2* srow = wrow + NCW * (D / 2);                             // [D/2] R(-NPAIR*TK)
+  float2* Wrow = srow + D / 2;                                     // [D/2] R(W)
+  float* qs = reinterpret_cast<float*>(fine + C::FINE + C::QROWS);  // [8][QSTR] raw query
   uint8_t* qraw = reinterpret_cast<uint8_t*>(qs + 8 * QSTR);       // [8][D] query, as stored
   uint8_t* nraw = qraw + 8 * D * 4;                                // [2][D] new pair, as stored
   int* flag = reinterpret_cast<int*>(nraw + 2 * D * 4);            // ticket, abort, issued
@@ -282,7 +290,20 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     flag[2] = 0;
   }
   if constexpr (ROTK) {
-    if (warp > 0) load_fine<D, STYLE>(p, fine, tid - 32, CONS_THREADS);
+    if (warp > 0) {
+      load_fine<D, STYLE>(p, fine, tid - 32, CONS_THREADS);
+      // The constant steps of the query bases: R(-NPAIR*TK) (table row NPAIR*TK,
+      // sine negated) and R(W) (row W).
+      for (int i = tid - 32; i < 2 * HALF; i += CONS_THREADS) {
+        const int k = i % HALF;
+        if (i < HALF) {
+          const float2 cs = __ldg(p.table + (size_t)(NPAIR * TK) * HALF + k);
+          srow[k] = make_float2(cs.x, -cs.y);
+        } else {
+          Wrow[k] = __ldg(p.table + (size_t)W * HALF + k);
+        }
+      }
+    }
   }
   prefetch_queries(p, D);
   // Cluster merge: the partner's barrier must exist before this CTA touches
@@ -320,8 +341,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0)
-      flag[2] = produce<D, ROTK, QUERY_BASES>(p, &tmK, &tmV, stages, full, empty, mdone, pre, sa,
-                                              sfill, rb, re, abort_flag, FUSED ? 1 : 0);
+      flag[2] = produce<D, ROTK, NO_ROWS>(p, &tmK, &tmV, stages, full, empty, mdone, pre, sa,
+                                          sfill, rb, re, abort_flag, FUSED ? 1 : 0);
     __syncwarp();
     if constexpr (CL) cluster_wait();
   } else {
@@ -504,13 +525,50 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       }
 
       int r0 = -1;                     // re-based position of the block's first slot
+      // The warp's query base R(r_q - r0) as a row of (cos, sin) per pair
+      // (lane t holds pairs 2t and 2t+1 of `qrow`): seeded from the table for
+      // the warp's first block of the segment, then stepped from block to
+      // block by R(-NPAIR*TK), and by R(W) where the ring wraps.
+      float4 seed = make_float4(0.f, 0.f, 0.f, 0.f);
+      bool seeded = true;
+      float2* my_row = qrow + cw * HALF;
+      if constexpr (ROTK) {
+        if (rb + jb < x1) {
+          const int m0 = rq - block_geo(rb + jb, u, W, NB).r0;
+          const int am = m0 < 0 ? -m0 : m0;
+          if (2 * lane < HALF) {
+            seed = __ldg(reinterpret_cast<const float4*>(p.table + (size_t)am * HALF) + lane);
+            if (m0 < 0) { seed.y = -seed.y; seed.w = -seed.w; }
+          }
+          seeded = false;
+        }
+      }
+      auto cmul_row = [&](float2* row, const float2* f) {   // row *= f, per pair
+        if (2 * lane < HALF) {
+          const float4 a = reinterpret_cast<const float4*>(row)[lane];
+          const float4 b = reinterpret_cast<const float4*>(f)[lane];
+          reinterpret_cast<float4*>(row)[lane] =
+              make_float4(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x,
+                          a.z * b.z - a.w * b.w, a.z * b.w + a.w * b.z);
+        }
+      };
       for (; rb + jb < x1; jb += NPAIR) {
         const int y = rb + jb;
         if (r0 < 0) {
           r0 = block_geo(y, u, W, NB).r0;
         } else {
           r0 += NPAIR * TK;              // NPAIR blocks further on along the ring
-          while (r0 >= W) r0 -= W;
+          if constexpr (ROTK) {
+            __syncwarp();
+            cmul_row(my_row, srow);
+          }
+          while (r0 >= W) {
+            r0 -= W;
+            if constexpr (ROTK) {
+              __syncwarp();
+              cmul_row(my_row, Wrow);
+            }
+          }
         }
         const int wrap_at = W - r0;      // keys d >= wrap_at sit at r0 + d - W
         const bool wraps = wrap_at < TK;
@@ -538,8 +596,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
           // ---- query fragments for this block's base(s) ----
           if constexpr (ROTK) {
             {
-              const float2* ta = reinterpret_cast<const float2*>(kt + 2 * TILE);
-              const float sa = (rq - r0) < 0 ? -1.f : 1.f;
+              if (!seeded) {
+                if (2 * lane < HALF) reinterpret_cast<float4*>(my_row)[lane] = seed;
+                seeded = true;
+              }
+              __syncwarp();
+              const float2* ta = my_row;
+              const float sa = 1.f;
               // Rows 0..7 (hi = 0) or 8..15 (hi = 1) of the A operand.
               auto rotate_q = [&](const float2* tr, float sg, auto hi_c) {
                 constexpr int hi = decltype(hi_c)::value;
@@ -570,7 +633,15 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                 }
               };
               rotate_q(ta, sa, std::integral_constant<int, 0>{});
-              if (wraps) rotate_q(ta + HALF, 1.f, std::integral_constant<int, 1>{});
+              if (wraps) {
+                // The keys past the ring's end take R(r_q - r0 + W).
+                float2* wr = wrow + cw * HALF;
+                if (2 * lane < HALF) reinterpret_cast<float4*>(wr)[lane] =
+                    reinterpret_cast<const float4*>(my_row)[lane];
+                cmul_row(wr, Wrow);
+                __syncwarp();
+                rotate_q(wr, 1.f, std::integral_constant<int, 1>{});
+              }
             }
           }
           // ---- S = Q K^T per 8-key group; select each key's base ----

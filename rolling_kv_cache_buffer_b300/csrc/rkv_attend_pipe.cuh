@@ -31,8 +31,9 @@ struct PipeCfg {
 //     consumer flips the sine when negative) and, when the block holds the
 //     ring's end, row fill-1-r0+W;
 //   KEY_BASES: row r0 and, when the block holds the ring's end, row W-r0 (the
-//     consumer flips its sine to get R(r0-W)).
-enum TableRows { QUERY_BASES = 0, KEY_BASES = 1 };
+//     consumer flips its sine to get R(r0-W));
+//   NO_ROWS: none (the consumers derive the rows themselves).
+enum TableRows { QUERY_BASES = 0, KEY_BASES = 1, NO_ROWS = 2 };
 
 // 16-byte chunk `grp` of key row `row` (0..TK-1) of a block tile: the tile is
 // D/64 boxes of TK rows x 128 bytes, 128-byte swizzled.
@@ -139,12 +140,12 @@ __device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap*
       const uint32_t dst = smem_u32(stages + (size_t)stage * C::STAGE);
       const bool wraps = W - r0 < TK;
       uint32_t bytes = 2 * C::TILE;
-      if constexpr (ROTK) bytes += wraps ? 2 * C::TROW : C::TROW;
+      if constexpr (ROTK && ROWS != NO_ROWS) bytes += wraps ? 2 * C::TROW : C::TROW;
       mbar_arrive_expect_tx(bar, bytes);
       // One box per tile: {64 elements, TK rows, the D/64 row halves, one unit}.
       tma_load_4d(dst, tmK, 0, blk * TK, 0, ug, bar);
       tma_load_4d(dst + C::TILE, tmV, 0, blk * TK, 0, ug, bar);
-      if constexpr (ROTK) {
+      if constexpr (ROTK && ROWS != NO_ROWS) {
         int rowA, rowB;
         if constexpr (ROWS == QUERY_BASES) {
           const int mA = u.fill - 1 + rq_off - r0;
