@@ -292,13 +292,17 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   if constexpr (ROTK) {
     if (warp > 0) {
       load_fine<D, STYLE>(p, fine, tid - 32, CONS_THREADS);
-      // The constant steps of the query bases: R(-NPAIR*TK) (table row NPAIR*TK,
-      // sine negated) and R(W) (row W).
+      // The constant steps of the query bases: R(-NPAIR*TK), the NPAIR-th
+      // power of table row TK with its sine negated (rows stop below 2W, and
+      // TK < 2W always), and R(W) (row W).
       for (int i = tid - 32; i < 2 * HALF; i += CONS_THREADS) {
         const int k = i % HALF;
         if (i < HALF) {
-          const float2 cs = __ldg(p.table + (size_t)(NPAIR * TK) * HALF + k);
-          srow[k] = make_float2(cs.x, -cs.y);
+          const float2 c = __ldg(p.table + (size_t)TK * HALF + k);
+          float2 a = c;
+          for (int r = 1; r < NPAIR; ++r)
+            a = make_float2(a.x * c.x - a.y * c.y, a.x * c.y + a.y * c.x);
+          srow[k] = make_float2(a.x, -a.y);
         } else {
           Wrow[k] = __ldg(p.table + (size_t)W * HALF + k);
         }
