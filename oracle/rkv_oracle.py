@@ -23,7 +23,7 @@ Sources, cited by page title and section:
 * [TT]  "audio8-asr-infinite-p150", section "At a glance": the decoder
         keeps a fixed rolling context.
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
 
 * origin = absolute position of the oldest retained token; re-based
   position r = p - origin, so 0 <= r < capacity;

@@ -7,7 +7,7 @@ and seeded random draws.  Every value is drawn as float32 N(0, 1) from a CPU
 nearest even, torch's conversion), so both the CUDA path and the oracle see the
 same bf16-exact numbers.
 
-Recipe (stated here and in the design doc):
+Recipe:
 * seed(config) = 20261202 + config index;
 * inputs of step t come from Generator.manual_seed(seed * 1_000_003 + t),
   drawn in the order q, k, v;
