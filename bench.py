@@ -204,7 +204,9 @@ def run_gpu(args, rank, world):
 
     # The fused decode step (rkv_step: one launch) wherever it applies; the
     # three calls otherwise and for the append/attend split below.
-    fused = layout == "pre_rope" and wl.kv_dtype == "bf16" and c == 1 and \
+    # (pre-RoPE keys, or stored-rotated keys with a re-basing epoch, whose
+    # step is rkv_step + rkv_rebase: the re-base launch acts once per epoch)
+    fused = (layout == "pre_rope" or epoch > 0) and wl.kv_dtype == "bf16" and c == 1 and \
         args.attend_impl != "fma" and not args.no_fused
 
     per_layer = fused and (args.per_layer or args.graph)
@@ -238,6 +240,8 @@ def run_gpu(args, rank, world):
                 layer_calls(q, k, v)
         elif fused and not split:
             cache.step(k, v, q, out)
+            if layout == "stored_rotated":
+                cache.rebase()
         else:
             cache.append(k, v)
             cache.rebase()
@@ -256,7 +260,8 @@ def run_gpu(args, rank, world):
         step(n_done)
         n_done += 1
     torch.cuda.synchronize(dev)
-    launches_per_step = (wl.n_layers if per_layer else 1) if fused else \
+    launches_per_step = ((wl.n_layers if per_layer else 1) +
+                         (1 if layout == "stored_rotated" else 0)) if fused else \
         2 + (1 if layout == "stored_rotated" else 0)
 
     # Timed region: exactly `steps` whole steps, one event pair around each.
@@ -334,6 +339,8 @@ def run_e2e(args, cache, ring, dev, wl, stream, fused):
         dv.copy_(v, non_blocking=True)
         if fused:
             cache.step(dk, dv, dq, out)
+            if cache.stored:
+                cache.rebase()
         else:
             cache.append(dk, dv)
             cache.rebase()

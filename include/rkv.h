@@ -162,8 +162,11 @@ rkv_status rkv_rebase(rkv_handle* h, void* stream);
  * rkv_rebase and rkv_attend(q, out, 0, L, 1) in sequence: the new pair is
  * written to its slot, and the attention takes it from k_new/v_new (its score
  * is <q, k_new>, the query and the key sharing a position) together with the
- * other retained pairs from the pools.  PRE_ROPE bf16 caches served by the
- * tensor-core kernel only; anything else returns RKV_ERR_UNSUPPORTED before
+ * other retained pairs from the pools.  Served by the tensor-core kernel for
+ * bf16 caches with PRE_ROPE keys, or STORED_ROTATED keys with a re-basing
+ * epoch (rebase_epoch >= 2: the new key is stored rotated to its position
+ * from o_ref and the lag grows by the evictions; call rkv_rebase after the
+ * step as after rkv_append); anything else returns RKV_ERR_UNSUPPORTED before
  * touching the GPU (use the three calls instead).  The new states are
  * published by the last CTA of the launch to finish. */
 rkv_status rkv_step(rkv_handle* h, const void* k_new, const void* v_new, const void* q,

@@ -308,7 +308,7 @@ rkv_status rkv_step_layers(rkv_handle* h, int32_t layer_begin, int32_t n_layers,
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(out) ||
       (step_log && !aligned16(step_log)))
     return RKV_ERR_INVALID_ARG;
-  if (h->sh.stored_rotated || !h->sh.bf16 || !h->has_map4 ||
+  if ((h->sh.stored_rotated && !h->sh.epoch) || !h->sh.bf16 || !h->has_map4 ||
       h->cfg.attend_impl == RKV_ATTEND_FMA || !rkv::attend_mma_supported(h->sh, 1))
     return RKV_ERR_UNSUPPORTED;
   rkv::AttendParams p = {};

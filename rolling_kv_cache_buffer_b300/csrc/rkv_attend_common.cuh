@@ -56,9 +56,10 @@ __device__ __forceinline__ void build_prefix(const AttendParams& p, int* pre) {
 
 // As build_prefix_warp, and also caches every stream's ring start a = origin
 // mod W (-1 for a stream whose state is not valid) and fill in shared memory,
-// so later unit lookups need no global load.
+// so later unit lookups need no global load; with `slag`, also the lag of
+// stored-rotated keys that follow a re-basing epoch (0 otherwise).
 __device__ __forceinline__ void build_prefix_cached(const AttendParams& p, int* pre, int* sa,
-                                                    int* sfill, int lane) {
+                                                    int* sfill, int lane, int* slag = nullptr) {
   const int per_unit = p.L_att * p.sh.Hkv;
   int carry = 0;
   if (lane == 0) pre[0] = 0;
@@ -71,6 +72,7 @@ __device__ __forceinline__ void build_prefix_cached(const AttendParams& p, int* 
       const int a = ok ? st.ring : -1;
       sa[s] = a;
       sfill[s] = ok ? st.fill : 0;
+      if (slag) slag[s] = (ok && p.sh.epoch) ? st.pending : 0;
       v = ok ? touched_blocks(a, st.fill, p.sh.NB) * per_unit : 0;
     }
 #pragma unroll

@@ -47,6 +47,7 @@
 #include <type_traits>
 
 #include "rkv_attend_pipe.cuh"
+#include "rkv_rows.cuh"
 
 #ifndef RKV_MMA_NCW
 #define RKV_MMA_NCW 8
@@ -91,7 +92,7 @@ struct MmaCfg : PipeCfg<D, ROTK> {
 // `rx`: bytes of the cluster receive area (0 without cluster merge).
 __host__ __device__ constexpr size_t mma_smem_bytes(int stage, int fixed, int ns, int S,
                                                     int rx = 0) {
-  return 1024 + (size_t)ns * stage + (size_t)fixed + (size_t)ns * 16 + (size_t)(3 * S + 1) * 4 +
+  return 1024 + (size_t)ns * stage + (size_t)fixed + (size_t)ns * 16 + (size_t)(4 * S + 1) * 4 +
          (rx ? 16 + 16 + (size_t)rx : 0);
 }
 // Cluster merge: rank 0 receives rank 1's NCW warp partials.
@@ -144,19 +145,24 @@ __device__ __forceinline__ void rot_pair2(uint32_t& x, uint32_t& y, float4 cs) {
 
 // Fused decode step: what rkv_append of one pair would leave in a stream's
 // state, from the state the step starts from (the bookkeeping of the append
-// kernel: e = max(0, n + 1 - W), o' = o + e, n' = n + 1 - e).
+// kernel: e = max(0, n + 1 - W), o' = o + e, n' = n + 1 - e; stored-rotated
+// keys with a re-basing epoch E also carry their lag, which must be below E
+// before the append and grows by e).
 struct StepState {
   bool ok;
   int e, n2, ring2;   // evictions, fill and origin mod W after the append
   int new_slot;       // slot of the new pair
+  int lag2;           // lag after the append (epoch), else 0
 };
-__device__ __forceinline__ StepState step_state(const StreamState& st, int W) {
+__device__ __forceinline__ StepState step_state(const StreamState& st, const Shape& sh) {
+  const int W = sh.W;
   StepState r;
-  r.ok = state_ok(st, W);
+  r.ok = state_ok(st, W) && (!sh.stored_rotated || (sh.epoch && st.pending < sh.epoch));
   r.e = max(0, st.fill + 1 - W);
   r.n2 = st.fill + 1 - r.e;
   r.ring2 = st.ring + r.e < W ? st.ring + r.e : st.ring + r.e - W;
   r.new_slot = st.ring + st.fill < W ? st.ring + st.fill : st.ring + st.fill - W;
+  r.lag2 = sh.epoch ? st.pending + r.e : 0;
   return r;
 }
 
@@ -164,7 +170,7 @@ __device__ __forceinline__ StepState step_state(const StreamState& st, int W) {
 // its new pair (the kernels read the new pair from the step's inputs, not from
 // the pool), i.e. ring start ring', n' - 1 pairs; the query sits at n' - 1.
 __device__ __forceinline__ void build_prefix_step(const AttendParams& p, int* pre, int* sa,
-                                                  int* sfill, int lane) {
+                                                  int* sfill, int* slag, int lane) {
   const int per_unit = p.L_att * p.sh.Hkv;
   int carry = 0;
   if (lane == 0) pre[0] = 0;
@@ -172,9 +178,10 @@ __device__ __forceinline__ void build_prefix_step(const AttendParams& p, int* pr
     const int s = base + lane;
     int v = 0;
     if (s < p.sh.S) {
-      const StepState ss = step_state(p.st[s], p.sh.W);
+      const StepState ss = step_state(p.st[s], p.sh);
       sa[s] = ss.ok ? ss.ring2 : -1;
       sfill[s] = ss.ok ? ss.n2 - 1 : 0;
+      slag[s] = ss.ok ? ss.lag2 : 0;
       v = ss.ok ? touched_blocks(ss.ring2, ss.n2 - 1, p.sh.NB) * per_unit : 0;
     }
 #pragma unroll
@@ -193,10 +200,12 @@ __device__ __forceinline__ void build_prefix_step(const AttendParams& p, int* pr
 // holds only the new pair gets v_new as its output.  Reads the post-append
 // geometry from the CTA's cache (sa = ring start after the append, or -1 for
 // a bad state; sfill = fill after the append minus the new pair), so the new
-// pair's slot is (sa + sfill) mod W.
-template <int D>
+// pair's slot is (sa + sfill) mod W.  STORED: stored-rotated keys (with a
+// re-basing epoch), whose new key goes in rotated.
+template <int D, bool STORED>
 __device__ __forceinline__ void step_prepass(const AttendParams& p, const int* sa,
-                                             const int* sfill, int w, int nw, int lane) {
+                                             const int* sfill, const int* slag, int w, int nw,
+                                             int lane) {
   const int per_stream = p.L_att * p.sh.Hkv;
   const int units = p.sh.S * per_stream;
   const int esz = p.sh.bf16 ? 2 : 4;
@@ -212,8 +221,22 @@ __device__ __forceinline__ void step_prepass(const AttendParams& p, const int* s
     const size_t dst =
         ((((size_t)s * p.sh.L + p.layer_begin + l) * p.sh.Hkv + g) * p.sh.W + new_slot) * D;
     const int chunks = D * esz / 16;
+    if constexpr (STORED) {
+      // Stored-rotated keys (with an epoch): the new key goes in rotated to
+      // its position from o_ref, n' - 1 + lag', four pairs per lane.
+      const size_t trow = (size_t)(sfill[s] + slag[s]) * (D / 2);
+      for (int i = t; i < D / 8; i += nt) {
+        float ka[4], kb[4];
+        float2 cs[4];
+        load_pairs(p.k_new, src, 4 * i, D, p.sh.style, p.sh.bf16 != 0, ka, kb);
+        load_cs4(p.table, trow, 4 * i, cs);
+        rotate4(ka, kb, cs, 1.f);
+        store_pairs(p.k_pool, dst, 4 * i, D, p.sh.style, p.sh.bf16 != 0, ka, kb);
+      }
+    }
     for (int i = t; i < 2 * chunks; i += nt) {
       const int kv = i >= chunks, q = i - kv * chunks;
+      if (STORED && !kv) continue;   // rotated above
       const uint4* from = reinterpret_cast<const uint4*>(
           static_cast<const uint8_t*>(kv ? p.v_new : p.k_new) + src * esz) + q;
       uint4* to = reinterpret_cast<uint4*>(
@@ -263,9 +286,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   int* pre = reinterpret_cast<int*>(empty + NS);                   // [S+1] block prefix
   int* sa = pre + p.sh.S + 1;                                      // [S] origin mod W
   int* sfill = sa + p.sh.S;                                        // [S] fill
+  int* slag = sfill + p.sh.S;                                      // [S] lag (epoch)
   // Cluster merge (CL): the pair of CTAs that shares a unit meets here.
   uint64_t* rx_bar = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(sfill + p.sh.S) + 15) & ~uintptr_t(15));
+      (reinterpret_cast<uintptr_t>(slag + p.sh.S) + 15) & ~uintptr_t(15));
   float* rslots = reinterpret_cast<float*>(rx_bar + 2);            // [NCW][SLOT] rank 1's slots
   volatile int* abort_flag = flag + 1;
 
@@ -329,9 +353,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   // consumers pick the prefix up from the named barrier.
   if (warp == 0) {
     if constexpr (FUSED)
-      build_prefix_step(p, pre, sa, sfill, lane);
+      build_prefix_step(p, pre, sa, sfill, slag, lane);
     else
-      build_prefix_cached(p, pre, sa, sfill, lane);
+      build_prefix_cached(p, pre, sa, sfill, lane, slag);
     __syncwarp();
     named_bar_arrive(BAR_PREFIX, MMA_THREADS);
   } else {
@@ -408,7 +432,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       qs[(G + i / D) * QSTR + i % D] = 0.f;
     if (rb < re) stage_unit(unit_of_cached(rb, p, pre, sa, sfill));
     if constexpr (FUSED)
-      step_prepass<D>(p, sa, sfill, cw, NCW, lane);
+      step_prepass<D, !ROTK>(p, sa, sfill, slag, cw, NCW, lane);
     else
       zero_empty_units_cached(p, sa, sfill, ct, CONS_THREADS);
     if (rb < re) {
@@ -433,13 +457,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
         if (last) {
           for (int s2 = lane; s2 < p.sh.S; s2 += 32) {
             const StreamState st = p.st[s2];
-            const StepState ss = step_state(st, W);
+            const StepState ss = step_state(st, p.sh);
             StreamState ns = st;
             if (ss.ok) {
               ns.origin = st.origin + ss.e;
               ns.fill = ss.n2;
               ns.ring = ss.ring2;
-              ns.pending = 0;
+              ns.pending = ss.lag2;
               ns.last_new = 1;
             } else if (ns.status == 0) {
               ns.status = STATUS_DEVICE_STATE;
@@ -500,7 +524,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       if constexpr (!ROTK) {
         // Stored-rotated keys sit at r (+ the stream's lag, with a re-basing
         // epoch) already: one base, R(r_q + lag) q.
-        const int lag = p.sh.epoch ? p.st[u.s].pending : 0;
+        const int lag = slag[u.s];
         const float2* t = p.table + (size_t)(rq + lag) * HALF;
         float qr[NKB][4];
         load_qf(qr);
@@ -1025,8 +1049,16 @@ cudaError_t launch_attend_mma(const AttendParams& p, const CUtensorMap& tk, cons
 
 cudaError_t launch_step_mma(const AttendParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                             int grid, cudaStream_t s) {
-  if (!attend_mma_supported(p.sh, 1) || p.sh.stored_rotated || p.c != 1)
+  // Pre-RoPE keys, or stored-rotated keys that follow a re-basing epoch.
+  if (!attend_mma_supported(p.sh, 1) || (p.sh.stored_rotated && !p.sh.epoch) || p.c != 1)
     return cudaErrorNotSupported;
+  if (p.sh.stored_rotated) {
+    if (p.sh.D == 128)
+      return p.sh.style == 0 ? launch_mma_t<128, false, 0, true>(p, tk, tv, grid, s)
+                             : launch_mma_t<128, false, 1, true>(p, tk, tv, grid, s);
+    return p.sh.style == 0 ? launch_mma_t<64, false, 0, true>(p, tk, tv, grid, s)
+                           : launch_mma_t<64, false, 1, true>(p, tk, tv, grid, s);
+  }
   if (p.sh.D == 128)
     return p.sh.style == 0 ? launch_mma_t<128, true, 0, true>(p, tk, tv, grid, s)
                            : launch_mma_t<128, true, 1, true>(p, tk, tv, grid, s);

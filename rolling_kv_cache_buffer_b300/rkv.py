@@ -195,6 +195,7 @@ class RollingKV:
         self.q_dtype = torch.bfloat16 if (q_dtype or kv_dtype) == "bf16" else torch.float32
         self.S, self.L, self.Hq, self.Hkv = n_streams, n_layers, n_q_heads, n_kv_heads
         self.D, self.W, self.max_chunk = head_dim, capacity, max_chunk
+        self.stored = layout == "stored_rotated"
         self.device = torch.device(device)
         shape = (n_streams, n_layers, n_kv_heads, capacity, head_dim)
         self.k_pool = torch.zeros(shape, dtype=self.kv_dtype, device=self.device)

@@ -153,3 +153,39 @@ def test_drift_of_stored_keys_across_layouts():
     assert kerr["epoch"] <= 3 * 2.0 ** -8
     assert kerr["eager"] > 2 * kerr["epoch"]
     assert oerr["epoch"] <= 2e-2 and oerr["pre_rope"] <= 2e-2
+
+
+@pytest.mark.parametrize("style", ["split_half", "interleaved"])
+def test_epoch_fused_step_matches_three_calls(style):
+    """rkv_step on stored-rotated keys with an epoch (then rkv_rebase) against
+    rkv_append + rkv_rebase + rkv_attend and the oracle's epoch model, across
+    several due re-bases: states and lag equal, V pools equal, K pools within
+    one bf16 ulp, outputs within tolerance."""
+    wl = WORKLOADS["qwen3b"].replace(n_layers=2, capacity=64)
+    E = wl.capacity
+    kw = dict(layout="stored_rotated", rope_theta=wl.rope_theta, rebase_epoch=E,
+              rope_style=style)
+    fused = RollingKV(1, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.capacity, **kw)
+    split = RollingKV(1, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.capacity, **kw)
+    orc = O.EpochRotatedOracle(1, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                               wl.capacity, theta=wl.rope_theta, epoch=E, style=style)
+    for t in range(1, 3 * wl.capacity + 5):
+        q, k, v = step_inputs(wl, t)
+        qd, kd, vd = dev(q, torch.bfloat16), dev(k, torch.bfloat16), dev(v, torch.bfloat16)
+        a = fused.step(kd, vd, qd)
+        fused.rebase()
+        split.append(kd, vd)
+        split.rebase()
+        b = split.attend(qd)
+        orc.append(k.double().numpy(), v.double().numpy())
+        orc.rebase()
+        assert torch.equal(fused.state, split.state), f"step {t}"
+        assert int(_lag(fused)[0]) == orc.lag[0]
+        if t % 7 == 0 or orc.lag[0] in (0, E - 1) or t < 4:
+            ref = orc.attend(q.double().numpy())
+            compare(a, ref)
+            compare(b, ref)
+    assert torch.equal(fused.v_pool, split.v_pool)
+    kf = fused.k_pool.double().cpu().numpy()
+    ks = split.k_pool.double().cpu().numpy()
+    assert np.all(np.abs(kf - ks) <= _ulp(ks) + 1e-30)
