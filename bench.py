@@ -1,11 +1,14 @@
 """Benchmark of the rolling-KV hot path on B300.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-rkv_append (bookkeeping + scatter, one kernel), rkv_rebase (no launch for the
-pre-RoPE layout; the re-rotation kernel for the stored-rotated one) and
-rkv_attend over every layer (one kernel).  Default workload: the 36-layer GQA
-16/2 x 128 decoder shape, one stream, window 4096, full (steady state: one
-pair evicted per step), as BASELINE's metric is quoted on.
+append one K/V pair per stream and layer (evicting the oldest), re-base the
+origin, and attend every layer's queries over the window.  Where it applies
+(pre-RoPE keys, or stored-rotated keys with a re-basing epoch; one new pair,
+bf16) that is rkv_step, one kernel, followed for stored-rotated keys by
+rkv_rebase (the re-rotation of the key pool, which acts once per epoch);
+otherwise rkv_append + rkv_rebase + rkv_attend.  Default workload: the
+36-layer GQA 16/2 x 128 decoder, one stream, window 4096, full (steady state:
+one pair evicted per step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...      # the float64 CPU oracle
@@ -260,6 +263,18 @@ def run_gpu(args, rank, world):
         step(n_done)
         n_done += 1
     torch.cuda.synchronize(dev)
+    # Stored-rotated keys with a re-basing epoch E: the re-rotation of the whole
+    # key pool runs once every E evictions.  With fewer than E timed steps, lead
+    # the streams (untimed steps) so that one re-rotation falls in the middle
+    # of the timed region, which then carries more than its share of that work.
+    if layout == "stored_rotated" and epoch:
+        lead = max(0, epoch - args.steps // 2 - int(_lags(cache).max())) \
+            if args.steps < epoch else 0
+        for _ in range(lead):
+            step(n_done)
+            n_done += 1
+        torch.cuda.synchronize(dev)
+        lags = [int(x) for x in _lags(cache)]
     launches_per_step = ((wl.n_layers if per_layer else 1) +
                          (1 if layout == "stored_rotated" else 0)) if fused else \
         2 + (1 if layout == "stored_rotated" else 0)
@@ -274,12 +289,18 @@ def run_gpu(args, rank, world):
     for _ in range(n_done):
         fl = [min(wl.capacity, f + c) for f in fl]
     bytes_per_step = []
+    rerotations = 0
     with ClockSampler(dev.index) as clk:
         t0 = time.perf_counter()
         for i in range(args.steps):
             cold()
             step(n_done, evs[i])
             n_done += 1
+            if layout == "stored_rotated" and epoch:
+                lags = [g + max(0, f + c - wl.capacity) for g, f in zip(lags, fl)]
+                if max(lags) >= epoch:
+                    rerotations += 1
+                    lags = [0 if g >= epoch else g for g in lags]
             fl = [min(wl.capacity, f + c) for f in fl]   # each step attends over fill'
             bytes_per_step.append(_kv_bytes_per_step(wl, fl))
         torch.cuda.synchronize(dev)
@@ -315,8 +336,16 @@ def run_gpu(args, rank, world):
                step_ms=step_ms, attend_ms=attend_ms, append_ms=append_ms, wall_s=wall,
                split_bytes=split_bytes,
                clocks=clk.summary(), launches=launches_per_step * args.steps,
-               bytes_per_step=bytes_per_step, e2e=e2e, fills=res_fills)
+               bytes_per_step=bytes_per_step, e2e=e2e, fills=res_fills,
+               rerotations=rerotations if layout == "stored_rotated" and epoch else None)
     return res
+
+
+def _lags(cache):
+    """Per-stream lag of stored-rotated keys behind the origin (int32 field 4
+    of each 32-byte stream state record)."""
+    import torch
+    return cache.state.view(torch.int32)[: 8 * cache.S].view(cache.S, 8)[:, 4].cpu().numpy()
 
 
 def run_e2e(args, cache, ring, dev, wl, stream, fused):
@@ -559,7 +588,9 @@ def main():
                    "step": (("rkv_step_layers x %d (one launch per layer%s)" %
                              (wl.n_layers, ", replayed from a CUDA graph" if args.graph else ""))
                             if res["fused"] and (args.per_layer or args.graph) else
-                            "rkv_step: append + rebase + attend (all layers), one launch"
+                            ("rkv_step (append + attend, all layers, one launch) + rkv_rebase "
+                             "(the re-rotation when due)" if args.workload.endswith("epoch") else
+                             "rkv_step: append + attend (all layers), one launch")
                             if res["fused"] else "rkv_append + rkv_rebase + rkv_attend "
                             "(all layers)")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -570,6 +601,8 @@ def main():
                 "us_per_step": e2e_ms * 1e3, "h2d_bytes_per_step": res["e2e"]["h2d"],
                 "d2h_bytes_per_step": res["e2e"]["d2h"]},
         "gpu_launches": res["launches"],
+        **({"rerotations_in_timed_region": res["rerotations"]}
+           if res["rerotations"] is not None else {}),
         "clocks": res["clocks"],
         "wall_s_timed_region": res["wall_s"],
     }

@@ -84,7 +84,7 @@ typedef enum { RKV_ATTEND_AUTO = 0, RKV_ATTEND_FMA = 1, RKV_ATTEND_MMA = 2 } rkv
 
 typedef struct {
   int32_t n_streams;     /* S, 1..1024                                    */
-  int32_t n_layers;      /* L, >= 1                                       */
+  int32_t n_layers;      /* L, >= 1; L * H_kv * W * D / 8 < 2^31          */
   int32_t n_q_heads;     /* H_q, multiple of n_kv_heads                   */
   int32_t n_kv_heads;    /* H_kv, >= 1                                    */
   int32_t head_dim;      /* D: 64 or 128                                  */

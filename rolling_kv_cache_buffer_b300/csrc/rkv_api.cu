@@ -3,6 +3,7 @@
 // allocates device memory; only rkv_get_stream_state waits for the device.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -47,6 +48,9 @@ rkv_status check_config(const rkv_config* c) {
   if (c->kv_dtype == RKV_F32 && c->head_dim == 128) return RKV_ERR_UNSUPPORTED;
   const long long units = (long long)c->n_streams * c->n_layers * c->n_kv_heads;
   if (units * (c->capacity / rkv::TK) >= (1LL << 31)) return RKV_ERR_UNSUPPORTED;
+  // The re-rotation kernel indexes a stream's (key, four-pair) items in int32.
+  if ((long long)c->n_layers * c->n_kv_heads * c->capacity * (c->head_dim / 8) >= (1LL << 31))
+    return RKV_ERR_UNSUPPORTED;
   return RKV_OK;
 }
 
@@ -358,9 +362,12 @@ rkv_status rkv_rebase(rkv_handle* h, void* stream) {
   p.k_pool = h->k_pool;
   p.tickets = reinterpret_cast<int*>(h->workspace + h->ws.rerot_tk_off);
   p.table = reinterpret_cast<const float2*>(h->workspace + h->ws.table_off);
-  p.rows_per_block = 4 * (256 / (h->sh.D / 8));
-  const long long rows = (long long)h->sh.L * h->sh.Hkv * h->sh.W;
-  const int bps = (int)((rows + p.rows_per_block - 1) / p.rows_per_block);
+  // One resident wave (4 CTAs of 256 threads per SM), split over the streams,
+  // and no more CTAs than a stream's (key, four-pair) items need.
+  const long long items = (long long)h->sh.L * h->sh.Hkv * h->sh.W * (h->sh.D / 8);
+  const long long need = (items + 255) / 256;
+  const long long wave = std::max(1LL, (4LL * h->num_sms) / h->sh.S);
+  const int bps = (int)std::max(1LL, std::min(need, wave));
   h->last_launches = 1;
   return cuda_status(rkv::launch_rerotate(p, bps, static_cast<cudaStream_t>(stream)));
 }

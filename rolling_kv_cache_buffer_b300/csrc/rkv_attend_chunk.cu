@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   prefetch_queries(p, D);
   prefetch_states(p);
   pdl_wait();   // from here on: stream state, pools, queries, outputs
+  pdl_trigger();   // a kernel launched next may start its own prologue
   if (warp == 0) {
     build_prefix_cached(p, pre, sa, sfill, lane);
     __syncwarp();

@@ -349,6 +349,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   }
   prefetch_states(p);
   pdl_wait();   // from here on: stream state, pools, queries, outputs
+  pdl_trigger();   // a kernel launched next may start its own prologue
   // Warp 0 builds the block prefix and starts streaming at once; the
   // consumers pick the prefix up from the named barrier.
   if (warp == 0) {

@@ -71,7 +71,6 @@ struct RerotParams {
   void* k_pool;
   int* tickets;
   const float2* table;
-  int rows_per_block;
 };
 
 struct AttendParams {

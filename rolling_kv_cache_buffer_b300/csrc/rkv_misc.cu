@@ -154,37 +154,54 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
 // turned by R(-e), e = pairs that append evicted, in f32 and rounded back to
 // the storage type.  With an epoch E, a stream is re-based only once its lag
 // (evictions since the last re-rotation) reaches E, and then every retained
-// key, new ones included, turns by R(-lag).  grid = (blocks_per_stream, S).
+// key, new ones included, turns by R(-lag).  grid = (CTAs per stream, S), at
+// most one resident wave; the CTAs stride over the stream's (key, four-pair)
+// items.  A stream with nothing due costs one state read per CTA.
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) rerotate_kernel(const RerotParams p) {
+__global__ void __launch_bounds__(256, 4) rerotate_kernel(const RerotParams p) {
+  pdl_wait();      // the state and the pool come from the kernel launched before
+  pdl_trigger();   // the attention launched next may start its prologue now
   const Shape& sh = p.sh;
   const int s = blockIdx.y;
   const StreamState st = p.st[s];
   const int W = sh.W, D = sh.D, Hkv = sh.Hkv;
   const bool work = sh.stored_rotated && state_ok(st, W) &&
                     (sh.epoch ? st.pending >= sh.epoch : st.pending > 0);
-  if (work) {
-    // Keys that predate the append (every eviction), or all of them (epoch).
-    const int nr = sh.epoch ? st.fill : st.fill - st.last_new;
-    const int total = sh.L * Hkv * max(nr, 0);
-    const int r0 = blockIdx.x * p.rows_per_block;
-    const int r1 = min(total, r0 + p.rows_per_block);
-    const int quads = D / 8;
-    const bool bf = sh.bf16 != 0;
-    const size_t trow = (size_t)st.pending * (D / 2);
-    for (int idx = threadIdx.x; idx < (r1 - r0) * quads; idx += blockDim.x) {
-      const int row = r0 + idx / quads;
-      const int i = (idx % quads) * 4;
-      const int r = row % nr;
-      const int lg = row / nr;                          // l * Hkv + g
-      const int slot = st.ring + r < W ? st.ring + r : st.ring + r - W;
-      const size_t base = (((size_t)s * sh.L * Hkv + lg) * W + slot) * D;
-      float a[4], b[4];
-      float2 cs[4];
-      load_pairs(p.k_pool, base, i, D, sh.style, bf, a, b);
-      load_cs4(p.table, trow, i, cs);
-      rotate4(a, b, cs, -1.f);
-      store_pairs(p.k_pool, base, i, D, sh.style, bf, a, b);
+  // Every CTA of the stream reads the same state (it changes only after the
+  // last CTA's ticket below), so either all take a ticket or none does.
+  if (!work) return;
+  // Keys that predate the append (every eviction), or all of them (epoch).
+  const int nr = sh.epoch ? st.fill : st.fill - st.last_new;
+  const int qsh = D == 128 ? 4 : 3;                  // log2 of D / 8 four-pair items per key
+  const int items = (sh.L * Hkv * max(nr, 0)) << qsh;   // < 2^31 (create checks)
+  const bool bf = sh.bf16 != 0;
+  const size_t trow = (size_t)st.pending * (D / 2);
+  const int stride = gridDim.x * blockDim.x;
+  constexpr int NB = 4;   // items per thread in flight: all loads, then all stores
+  for (int i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < items; i0 += NB * stride) {
+    float a[NB][4], b[NB][4];
+    size_t base[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int idx = i0 + j * stride;
+      if (idx < items) {
+        const int row = idx >> qsh;
+        const int r = row % nr, lg = row / nr;        // lg = l * Hkv + g
+        const int slot = st.ring + r < W ? st.ring + r : st.ring + r - W;
+        base[j] = (((size_t)s * sh.L * Hkv + lg) * W + slot) * D;
+        load_pairs(p.k_pool, base[j], (idx & ((1 << qsh) - 1)) * 4, D, sh.style, bf, a[j], b[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int idx = i0 + j * stride;
+      if (idx < items) {
+        const int i = (idx & ((1 << qsh) - 1)) * 4;
+        float2 cs[4];
+        load_cs4(p.table, trow, i, cs);
+        rotate4(a[j], b[j], cs, -1.f);
+        store_pairs(p.k_pool, base[j], i, D, sh.style, bf, a[j], b[j]);
+      }
     }
   }
   __syncthreads();
@@ -192,7 +209,7 @@ __global__ void __launch_bounds__(256) rerotate_kernel(const RerotParams p) {
     __threadfence();
     const int old = atomicAdd(&p.tickets[s], 1);
     if (old == static_cast<int>(gridDim.x) - 1) {
-      if (work) p.st[s].pending = 0;
+      p.st[s].pending = 0;
       p.tickets[s] = 0;
     }
   }
@@ -216,8 +233,18 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 cudaError_t launch_rerotate(const RerotParams& p, int blocks_per_stream, cudaStream_t s) {
-  rerotate_kernel<<<dim3(blocks_per_stream, p.sh.S), 256, 0, s>>>(p);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the launch overlaps the previous kernel's
+  // tail; the kernel waits for it before reading anything.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks_per_stream, p.sh.S);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rerotate_kernel, p);
 }
 cudaError_t launch_set_state(StreamState* st, int s_idx, long long origin, int fill, int ring,
                              cudaStream_t s) {
