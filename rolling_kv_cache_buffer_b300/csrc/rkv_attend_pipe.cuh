@@ -113,6 +113,7 @@ __device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap*
   const int W = p.sh.W, NB = p.sh.NB, NS = p.ns;
   int stage = 0, round = 0, issued = 0, seg = 0;
   bool stop = false;
+  const uint64_t pol = l2_evict_first_policy();   // every K/V row is read once
   for (int x = rb; x < re && !stop; ++seg) {
     // Per unit segment: the unit, then the block geometry advanced per block.
     const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
@@ -143,8 +144,8 @@ __device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap*
       if constexpr (ROTK && ROWS != NO_ROWS) bytes += wraps ? 2 * C::TROW : C::TROW;
       mbar_arrive_expect_tx(bar, bytes);
       // One box per tile: {64 elements, TK rows, the D/64 row halves, one unit}.
-      tma_load_4d(dst, tmK, 0, blk * TK, 0, ug, bar);
-      tma_load_4d(dst + C::TILE, tmV, 0, blk * TK, 0, ug, bar);
+      tma_load_4d_hint(dst, tmK, 0, blk * TK, 0, ug, bar, pol);
+      tma_load_4d_hint(dst + C::TILE, tmV, 0, blk * TK, 0, ug, bar, pol);
       if constexpr (ROTK && ROWS != NO_ROWS) {
         int rowA, rowB;
         if constexpr (ROWS == QUERY_BASES) {

@@ -171,13 +171,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
-// 4-D tiled TMA load (global -> shared), completion counted on `bar`.
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
-                                            int c2, int c3, uint32_t bar) {
+// L2 policy for data read once: its lines are the first to go, so a stream of
+// them does not push out what the kernel reads again (states, code, partials).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// 4-D tiled TMA load (global -> shared) under L2 cache policy `pol`,
+// completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* tm, int c0,
+                                                 int c1, int c2, int c3, uint32_t bar,
+                                                 uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(pol)
       : "memory");
 }
 // 1-D bulk copy (global -> shared); both addresses 16-byte aligned, bytes % 16 == 0.
