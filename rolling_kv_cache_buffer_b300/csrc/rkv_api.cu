@@ -282,11 +282,13 @@ rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_be
     return RKV_ERR_INVALID_ARG;
   if (n_q > h->sh.W) return RKV_ERR_CAPACITY;
   if (n_q < 1 || n_q > h->cfg.max_chunk) return RKV_ERR_INVALID_ARG;
-  rkv::AttendParams p;
+  rkv::AttendParams p = {};
   p.sh = h->sh;
   p.st = h->state;
   p.q = q;
   p.out = out;
+  p.k_pool = h->k_pool;   // read only through the tensor maps (and L2 prefetches)
+  p.v_pool = h->v_pool;
   p.table = reinterpret_cast<const float2*>(h->workspace + h->ws.table_off);
   p.partials = reinterpret_cast<float*>(h->workspace + h->ws.part_off);
   p.unit_tickets = reinterpret_cast<int*>(h->workspace + h->ws.unit_tk_off);

@@ -71,11 +71,13 @@ extern "C" rkv_status rkv_attend_static_scratch(rkv_handle* h, const void* q, fl
   // The array keeps the previous call's contents; the tickets must start at 0.
   if (cudaMemsetAsync(base, 0, tickets, s) != cudaSuccess) return RKV_ERR_CUDA;
 
-  rkv::AttendParams p;
+  rkv::AttendParams p = {};
   p.sh = h->sh;
   p.st = h->state;
   p.q = q;
   p.out = out;
+  p.k_pool = h->k_pool;   // read only through the tensor maps (and L2 prefetches)
+  p.v_pool = h->v_pool;
   p.table = reinterpret_cast<const float2*>(h->workspace + h->ws.table_off);
   p.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kTicketBytes);
   p.unit_tickets = static_cast<int*>(base);

@@ -90,8 +90,8 @@ struct AttendParams {
   int fused;                  // 0: attention only
   const void* k_new;          // [L][S][1][H_kv][D] of the cache type
   const void* v_new;
-  void* k_pool;               // the pools the new pair goes into
-  void* v_pool;
+  void* k_pool;               // the pools (the fused step writes the new pair
+  void* v_pool;               // into them; the attention reads them via TMA)
   long long* log;             // nullable, [S][4]
   int* step_ticket;           // one int: CTAs done with the step
   int publish;                // the step's last launch: publish the new states
