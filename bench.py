@@ -562,8 +562,11 @@ def main():
         kern_us = ms_local * 1e3 / wl.n_layers
         achieved = bytes_local / (ms_local * 1e-3) / 1e9
     elif res["fused"]:
-        # The step is one launch of the fused kernel: its events bracket the kernel.
-        kernel_key = "attend_mma_step"
+        # The step is one launch of the fused kernel (for stored-rotated keys
+        # followed by the re-base launch, which acts once per epoch): the
+        # events bracket the kernel.
+        stored = _workload(args.workload)[1] == "stored_rotated"
+        kernel_key = "attend_mma_step_stored" if stored else "attend_mma_step"
         kern_us = ms_local * 1e3
         achieved = bytes_local / (ms_local * 1e-3) / 1e9
     else:
