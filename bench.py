@@ -28,6 +28,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -81,23 +82,51 @@ def _kv_bytes_per_step(wl, fills):
     return sum(fills) * wl.n_layers * wl.n_kv_heads * wl.head_dim * wl.elem_bytes * 2
 
 
-def _kernel_hash():
+# The source file each timed kernel is compiled from.
+KERNEL_SOURCE = {
+    "attend_mma": "rkv_attend_mma.cu", "attend_mma_step": "rkv_attend_mma.cu",
+    "attend_mma_step_stored": "rkv_attend_mma.cu", "attend_mma_step_layer": "rkv_attend_mma.cu",
+    "attend_mma_chunk": "rkv_attend_chunk.cu", "attend_fma": "rkv_attend_fma.cu",
+    "rerotate": "rkv_misc.cu",
+}
+
+
+def _sources(main):
+    """`main` and the C-ABI entry points (which set the launch parameters and
+    grid), with every header they include, transitively."""
+    dirs = [os.path.join(ROOT, "rolling_kv_cache_buffer_b300", "csrc"), os.path.join(ROOT, "include")]
+    seen, todo = {}, [main, "rkv_api.cu"]
+    while todo:
+        name = todo.pop()
+        if name in seen:
+            continue
+        path = next((os.path.join(d, name) for d in dirs if os.path.exists(os.path.join(d, name))),
+                    None)
+        if path is None:
+            continue
+        with open(path, "rb") as fh:
+            seen[name] = fh.read()
+        todo += re.findall(r'#include "([^"]+)"', seen[name].decode())
+    return seen
+
+
+def kernel_hash(kernel_key):
+    """Hash of the sources a timed kernel is built from (file names and contents)."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "rolling_kv_cache_buffer_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+    for name, text in sorted(_sources(KERNEL_SOURCE[kernel_key]).items()):
+        h.update(name.encode())
+        h.update(text)
     return h.hexdigest()[:16]
 
 
 def _traffic(kernel_key):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel sources changed since the counters were taken."""
+    kernel's sources changed since the counters were taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
             d = json.load(f)
         ent = d.get(kernel_key)
-        if ent and ent.get("source_hash") == _kernel_hash():
+        if ent and ent.get("source_hash") == kernel_hash(kernel_key):
             return ent["bytes_per_launch"]
     except Exception:
         pass

@@ -48,7 +48,7 @@ rkv_status check_config(const rkv_config* c) {
   if (c->kv_dtype == RKV_F32 && c->head_dim == 128) return RKV_ERR_UNSUPPORTED;
   const long long units = (long long)c->n_streams * c->n_layers * c->n_kv_heads;
   if (units * (c->capacity / rkv::TK) >= (1LL << 31)) return RKV_ERR_UNSUPPORTED;
-  // The re-rotation kernel indexes a stream's (key, four-pair) items in int32.
+  // The re-rotation kernel indexes a stream's work items in int32.
   if ((long long)c->n_layers * c->n_kv_heads * c->capacity * (c->head_dim / 8) >= (1LL << 31))
     return RKV_ERR_UNSUPPORTED;
   return RKV_OK;
@@ -364,11 +364,11 @@ rkv_status rkv_rebase(rkv_handle* h, void* stream) {
   p.k_pool = h->k_pool;
   p.tickets = reinterpret_cast<int*>(h->workspace + h->ws.rerot_tk_off);
   p.table = reinterpret_cast<const float2*>(h->workspace + h->ws.table_off);
-  // One resident wave (4 CTAs of 256 threads per SM), split over the streams,
-  // and no more CTAs than a stream's (key, four-pair) items need.
-  const long long items = (long long)h->sh.L * h->sh.Hkv * h->sh.W * (h->sh.D / 8);
+  // One resident wave (3 CTAs of 256 threads per SM), split over the streams,
+  // and no more CTAs than a stream's (key, eight-pair) items need.
+  const long long items = (long long)h->sh.L * h->sh.Hkv * h->sh.W * (h->sh.D / 16);
   const long long need = (items + 255) / 256;
-  const long long wave = std::max(1LL, (4LL * h->num_sms) / h->sh.S);
+  const long long wave = std::max(1LL, (3LL * h->num_sms) / h->sh.S);
   const int bps = (int)std::max(1LL, std::min(need, wave));
   h->last_launches = 1;
   return cuda_status(rkv::launch_rerotate(p, bps, static_cast<cudaStream_t>(stream)));

@@ -4,6 +4,8 @@
 // Bookkeeping follows the flowchart of "Audio8 ASR Infinite: What It Actually
 // Takes to Listen Forever": a pair that does not fit makes the cache evict the
 // oldest pair and shift the sliding origin forward.
+#include <type_traits>
+
 #include "rkv_internal.h"
 #include "rkv_rows.cuh"
 
@@ -155,52 +157,132 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
 // the storage type.  With an epoch E, a stream is re-based only once its lag
 // (evictions since the last re-rotation) reaches E, and then every retained
 // key, new ones included, turns by R(-lag).  grid = (CTAs per stream, S), at
-// most one resident wave; the CTAs stride over the stream's (key, four-pair)
-// items.  A stream with nothing due costs one state read per CTA.
+// most one resident wave (3 CTAs per SM).  Work item = eight rotary pairs of
+// one key (two 16-byte loads of bf16); the CTAs stride over the stream's
+// items.  The stride is a multiple of a key's D/16 items, so a thread always
+// turns the same eight pairs and loads their (cos, sin) once.  A stream with
+// nothing due costs one state read per CTA.
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(256, 4) rerotate_kernel(const RerotParams p) {
+// Eight consecutive pool elements as f32, from / to their raw 16-byte words
+// (one for bf16, two for f32).
+template <bool BF>
+__device__ __forceinline__ void widen8(const uint4* w, float (&x)[8]) {
+  if constexpr (BF) {
+    x[0] = bf_lo(w[0].x); x[1] = bf_hi(w[0].x); x[2] = bf_lo(w[0].y); x[3] = bf_hi(w[0].y);
+    x[4] = bf_lo(w[0].z); x[5] = bf_hi(w[0].z); x[6] = bf_lo(w[0].w); x[7] = bf_hi(w[0].w);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      x[4 * k] = __uint_as_float(w[k].x); x[4 * k + 1] = __uint_as_float(w[k].y);
+      x[4 * k + 2] = __uint_as_float(w[k].z); x[4 * k + 3] = __uint_as_float(w[k].w);
+    }
+  }
+}
+template <bool BF>
+__device__ __forceinline__ void narrow8(const float (&x)[8], uint4* w) {
+  if constexpr (BF) {
+    w[0] = make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]), pack_bf2(x[4], x[5]),
+                      pack_bf2(x[6], x[7]));
+  } else {
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      w[k] = make_uint4(__float_as_uint(x[4 * k]), __float_as_uint(x[4 * k + 1]),
+                        __float_as_uint(x[4 * k + 2]), __float_as_uint(x[4 * k + 3]));
+  }
+}
+// (x, y) -> (x cos + y sin, y cos - x sin): the rotation by minus the angle.
+__device__ __forceinline__ void unrotate(float& x, float& y, float2 cs) {
+  const float c = cs.x, s = -cs.y;
+  const float x0 = x, y0 = y;
+  x = x0 * c - y0 * s;
+  y = y0 * c + x0 * s;
+}
+
+template <bool BF>
+__global__ void __launch_bounds__(256, 3) rerotate_kernel(const RerotParams p) {
   pdl_wait();      // the state and the pool come from the kernel launched before
   pdl_trigger();   // the attention launched next may start its prologue now
   const Shape& sh = p.sh;
   const int s = blockIdx.y;
   const StreamState st = p.st[s];
-  const int W = sh.W, D = sh.D, Hkv = sh.Hkv;
+  const int W = sh.W, D = sh.D;
   const bool work = sh.stored_rotated && state_ok(st, W) &&
                     (sh.epoch ? st.pending >= sh.epoch : st.pending > 0);
   // Every CTA of the stream reads the same state (it changes only after the
   // last CTA's ticket below), so either all take a ticket or none does.
   if (!work) return;
   // Keys that predate the append (every eviction), or all of them (epoch).
-  const int nr = sh.epoch ? st.fill : st.fill - st.last_new;
-  const int qsh = D == 128 ? 4 : 3;                  // log2 of D / 8 four-pair items per key
-  const int items = (sh.L * Hkv * max(nr, 0)) << qsh;   // < 2^31 (create checks)
-  const bool bf = sh.bf16 != 0;
-  const size_t trow = (size_t)st.pending * (D / 2);
-  const int stride = gridDim.x * blockDim.x;
-  constexpr int NB = 4;   // items per thread in flight: all loads, then all stores
-  for (int i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < items; i0 += NB * stride) {
-    float a[NB][4], b[NB][4];
-    size_t base[NB];
+  const int nr = max(sh.epoch ? st.fill : st.fill - st.last_new, 0);
+  const int cshift = D == 128 ? 3 : 2;             // log2 of D / 16 items per key
+  const int per_lg = nr << cshift;                 // items per (layer, KV head)
+  const int LH = sh.L * sh.Hkv;
+  const int stride = gridDim.x * blockDim.x;       // a multiple of D / 16
+  const int t0 = blockIdx.x * blockDim.x + threadIdx.x;
+  const int i = (t0 & ((1 << cshift) - 1)) * 8;    // the thread's first pair
+  float2 cs[8];
+  {
+    const float4* t = reinterpret_cast<const float4*>(p.table + (size_t)st.pending * (D / 2) + i);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 v = __ldg(t + k);
+      cs[2 * k] = make_float2(v.x, v.y);
+      cs[2 * k + 1] = make_float2(v.z, v.w);
+    }
+  }
+  // Element offsets (within a key) of the item's two groups of eight: the
+  // pairs' first and second halves (split-half) or 16 consecutive elements.
+  const int e0 = sh.style == 0 ? i : 2 * i, e1 = sh.style == 0 ? D / 2 + i : 2 * i + 8;
+  constexpr int NW = BF ? 1 : 2;                   // 16-byte words per group
+  using Elem = typename std::conditional<BF, uint16_t, float>::type;
+  Elem* pool = static_cast<Elem*>(p.k_pool);
+  // (layer * H_kv + head, item within it) of the thread's next item, advanced
+  // by the stride without a division per item.
+  int lg = per_lg ? t0 / per_lg : LH, rem = per_lg ? t0 - lg * per_lg : 0;
+  const int dq = per_lg ? stride / per_lg : 0, dr = per_lg ? stride - dq * per_lg : 0;
+  const size_t sbase = (size_t)s * LH * W;
+  constexpr int NB = BF ? 4 : 2;   // items per thread in flight: all loads, then all stores
+  while (lg < LH) {
+    uint4 w[NB][2][NW];
+    Elem* row[NB];
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
-      const int idx = i0 + j * stride;
-      if (idx < items) {
-        const int row = idx >> qsh;
-        const int r = row % nr, lg = row / nr;        // lg = l * Hkv + g
+      row[j] = nullptr;
+      if (lg < LH) {
+        const int r = rem >> cshift;
         const int slot = st.ring + r < W ? st.ring + r : st.ring + r - W;
-        base[j] = (((size_t)s * sh.L * Hkv + lg) * W + slot) * D;
-        load_pairs(p.k_pool, base[j], (idx & ((1 << qsh) - 1)) * 4, D, sh.style, bf, a[j], b[j]);
+        row[j] = pool + (sbase + (size_t)lg * W + slot) * D;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+          w[j][0][k] = reinterpret_cast<const uint4*>(row[j] + e0)[k];
+          w[j][1][k] = reinterpret_cast<const uint4*>(row[j] + e1)[k];
+        }
       }
+      lg += dq;
+      rem += dr;
+      if (rem >= per_lg) { rem -= per_lg; ++lg; }
     }
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
-      const int idx = i0 + j * stride;
-      if (idx < items) {
-        const int i = (idx & ((1 << qsh) - 1)) * 4;
-        float2 cs[4];
-        load_cs4(p.table, trow, i, cs);
-        rotate4(a[j], b[j], cs, -1.f);
-        store_pairs(p.k_pool, base[j], i, D, sh.style, bf, a[j], b[j]);
+      if (!row[j]) continue;
+      float u[8], v[8];
+      widen8<BF>(w[j][0], u);
+      widen8<BF>(w[j][1], v);
+      if (sh.style == 0) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) unrotate(u[k], v[k], cs[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          unrotate(u[2 * k], u[2 * k + 1], cs[k]);
+          unrotate(v[2 * k], v[2 * k + 1], cs[4 + k]);
+        }
+      }
+      narrow8<BF>(u, w[j][0]);
+      narrow8<BF>(v, w[j][1]);
+#pragma unroll
+      for (int k = 0; k < NW; ++k) {
+        reinterpret_cast<uint4*>(row[j] + e0)[k] = w[j][0][k];
+        reinterpret_cast<uint4*>(row[j] + e1)[k] = w[j][1][k];
       }
     }
   }
@@ -244,7 +326,8 @@ cudaError_t launch_rerotate(const RerotParams& p, int blocks_per_stream, cudaStr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, rerotate_kernel, p);
+  return p.sh.bf16 ? cudaLaunchKernelEx(&cfg, rerotate_kernel<true>, p)
+                   : cudaLaunchKernelEx(&cfg, rerotate_kernel<false>, p);
 }
 cudaError_t launch_set_state(StreamState* st, int s_idx, long long origin, int fill, int ring,
                              cudaStream_t s) {
