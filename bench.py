@@ -2,11 +2,12 @@
 
 One step = one pass of the whole hot path over one batch of synthetic input:
 append one K/V pair per stream and layer (evicting the oldest), re-base the
-origin, and attend every layer's queries over the window.  Where it applies
-(pre-RoPE keys, or stored-rotated keys with a re-basing epoch; one new pair,
-bf16) that is rkv_step, one kernel, followed for stored-rotated keys by
-rkv_rebase (the re-rotation of the key pool, which acts once per epoch);
-otherwise rkv_append + rkv_rebase + rkv_attend.  Default workload: the
+origin, and attend every layer's queries over the window.  By default the
+step is the faster of two call sequences measured on B300 for its layout:
+rkv_append + rkv_rebase + rkv_attend (pre-RoPE keys: two launches, the
+re-base being the origin update itself), or the fused rkv_step (one kernel)
+followed by rkv_rebase for stored-rotated keys with a re-basing epoch (the
+re-rotation acts once per epoch); --path picks one.  Default workload: the
 36-layer GQA 16/2 x 128 decoder, one stream, window 4096, full (steady state:
 one pair evicted per step).
 
@@ -234,12 +235,19 @@ def run_gpu(args, rank, world):
             flush.zero_()
             torch.amax(drain)
 
-    # The fused decode step (rkv_step: one launch) wherever it applies; the
-    # three calls otherwise and for the append/attend split below.
-    # (pre-RoPE keys, or stored-rotated keys with a re-basing epoch, whose
-    # step is rkv_step + rkv_rebase: the re-base launch acts once per epoch)
-    fused = (layout == "pre_rope" or epoch > 0) and wl.kv_dtype == "bf16" and c == 1 and \
-        args.attend_impl != "fma" and not args.no_fused
+    # Which calls make the step.  The fused decode step (rkv_step, one launch)
+    # applies to pre-RoPE keys and to stored-rotated keys with a re-basing
+    # epoch (then rkv_step + rkv_rebase, whose launch acts once per epoch),
+    # one new pair, bf16.  "auto" takes the faster path measured on B300: the
+    # separate calls for pre-RoPE keys (the attention's prologue overlaps the
+    # append kernel through programmatic dependent launch, 41.4 against
+    # 43.1 us per step on qwen3b), the fused step for the epoch layout.
+    fusable = (layout == "pre_rope" or epoch > 0) and wl.kv_dtype == "bf16" and c == 1 and \
+        args.attend_impl != "fma"
+    path = "split" if args.no_fused else args.path
+    if path == "auto":
+        path = "fused" if epoch > 0 or args.per_layer or args.graph else "split"
+    fused = fusable and path == "fused"
 
     per_layer = fused and (args.per_layer or args.graph)
     graphs = {}
@@ -517,8 +525,10 @@ def main():
     ap.add_argument("--ring", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-fused", action="store_true",
-                    help="time rkv_append + rkv_rebase + rkv_attend instead of rkv_step")
+    ap.add_argument("--path", default="auto", choices=["auto", "fused", "split"],
+                    help="fused: rkv_step where it applies; split: rkv_append + rkv_rebase + "
+                         "rkv_attend; auto: the faster of the two for the layout")
+    ap.add_argument("--no-fused", action="store_true", help="same as --path split")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer end-to-end loop (short runs under ncu)")
     ap.add_argument("--per-layer", action="store_true",
@@ -623,8 +633,10 @@ def main():
                             ("rkv_step (append + attend, all layers, one launch) + rkv_rebase "
                              "(the re-rotation when due)" if args.workload.endswith("epoch") else
                              "rkv_step: append + attend (all layers), one launch")
-                            if res["fused"] else "rkv_append + rkv_rebase + rkv_attend "
-                            "(all layers)")},
+                            if res["fused"] else
+                            "rkv_append + rkv_attend (all layers; rkv_rebase launches nothing "
+                            "for pre-RoPE keys)" if _workload(args.workload)[1] == "pre_rope" else
+                            "rkv_append + rkv_rebase + rkv_attend (all layers)")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "kernel": kernel_key, "traffic": _traffic(kernel_key),
