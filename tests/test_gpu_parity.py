@@ -335,6 +335,60 @@ def test_stored_rotated_stream_matches_oracle():
             compare(out, orc.attend(q.double().numpy()))
 
 
+@pytest.mark.parametrize("style", ["split_half", "interleaved"])
+def test_stored_rotated_float32_head_dim_64(style):
+    """Stored-rotated keys in float32 pools (tiny workload, D = 64), re-rotated
+    at every eviction for 100 steps (three trips round the ring): each call's
+    re-rotation equals the float64 rotation R(-e) of the stored keys within
+    float32 rounding, and the attention equals the exact (pre-RoPE) oracle
+    within the float32 path's 1e-4 / 1e-5."""
+    wl = WORKLOADS["tiny"]
+    cache = make_cache(wl, layout="stored_rotated", style=style)
+    orc = make_oracle(wl, style=style)
+    W = wl.capacity
+    for t in range(1, 101):
+        q, k, v = step_inputs(wl, t)
+        cache.append(dev(k, torch.float32), dev(v, torch.float32))
+        o, f, _ = cache.get_stream_state()
+        old = [(int(o[0]) + r) % W for r in range(int(f[0]) - 1)]
+        src = cache.k_pool[0][:, :, old].double().cpu().numpy()
+        cache.rebase()
+        if t > W:   # one eviction per step from here on
+            got = cache.k_pool[0][:, :, old].double().cpu().numpy()
+            want = O.rope(src, -1.0, wl.rope_theta, style)
+            assert np.abs(got - want).max() <= 1e-5
+        orc.append(k.double().numpy(), v.double().numpy())
+        compare(cache.attend(dev(q, torch.float32)), orc.attend(q.double().numpy()), 1e-4, 1e-5)
+
+
+def test_stored_rotated_bf16_head_dim_64():
+    """Stored-rotated bf16 keys with D = 64 and the interleaved pairing (audio8
+    shape, 2 layers, W = 64), every eviction re-rotated: each call within one
+    bf16 ulp of the float64 rotation, outputs against the oracle that stores
+    bf16 keys the same way."""
+    wl = WORKLOADS["audio8"].replace(n_layers=2, capacity=64)
+    style = "interleaved"
+    cache = make_cache(wl, layout="stored_rotated", style=style)
+    orc = make_oracle(wl, cls=O.StoredRotatedOracle, style=style)
+    W = wl.capacity
+    for t in range(1, 151):
+        q, k, v = step_inputs(wl, t)
+        cache.append(dev(k, torch.bfloat16), dev(v, torch.bfloat16))
+        o, f, _ = cache.get_stream_state()
+        old = [(int(o[0]) + r) % W for r in range(int(f[0]) - 1)]
+        src = cache.k_pool[0][:, :, old].double().cpu().numpy()
+        cache.rebase()
+        if t > W and t % 5 == 0:
+            got = cache.k_pool[0][:, :, old].double().cpu().numpy()
+            want = O.rerotate(src, 1, wl.rope_theta, style)
+            ulp = np.ldexp(1.0, np.frexp(np.abs(want))[1] - 8)
+            assert np.all(np.abs(got - want) <= ulp + 1e-30)
+        orc.append(k.double().numpy(), v.double().numpy())
+        orc.rebase()
+        if t % 7 == 0 or t > 145:
+            compare(cache.attend(dev(q, torch.bfloat16)), orc.attend(q.double().numpy()))
+
+
 # ----------------------------------------------------------------------------
 # Device-side error paths (no fault: a status word)
 # ----------------------------------------------------------------------------
