@@ -111,12 +111,19 @@ def _sources(main):
     return seen
 
 
+def _code_only(text):
+    """C/C++/CUDA source without its comments, whitespace runs collapsed."""
+    text = re.sub(r"/\*.*?\*/", " ", text.decode(), flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split()).encode()
+
+
 def kernel_hash(kernel_key):
-    """Hash of the sources a timed kernel is built from (file names and contents)."""
+    """Hash of the code (comments aside) a timed kernel is built from."""
     h = hashlib.sha256()
     for name, text in sorted(_sources(KERNEL_SOURCE[kernel_key]).items()):
         h.update(name.encode())
-        h.update(text)
+        h.update(_code_only(text))
     return h.hexdigest()[:16]
 
 

@@ -150,7 +150,12 @@ rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_be
 /* Re-base.  PRE_ROPE: nothing moves (the origin update of rkv_append is the
  * whole re-base) and nothing is launched.  STORED_ROTATED: one launch that
  * re-rotates every retained key older than the last append by R(-e), e = the
- * pairs that append evicted, in float32, rounded to nearest even. */
+ * pairs that append evicted, in float32, rounded to nearest even.  With
+ * rebase_epoch = E >= 2 the launch leaves a stream alone until its lag has
+ * reached E and then turns all of its retained keys, the newest included, by
+ * R(-lag) and sets the lag to 0; a stream with nothing due costs one state
+ * read.  The launch is stream-ordered after the previous work on `stream`
+ * (programmatic dependent launch lets it start its prologue early). */
 rkv_status rkv_rebase(rkv_handle* h, void* stream);
 
 /* One decode step in one kernel launch: rkv_append of one new pair per stream,
