@@ -56,10 +56,12 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
   // New pair j goes to slot first_slot + j (mod W); the state keeps origin mod W.
   const int first_slot = st.ring + st.fill < W ? st.ring + st.fill : st.ring + st.fill - W;
 
-  if (ok && !sh.stored_rotated) {
+  if (!sh.stored_rotated) {
     // Pre-RoPE: a plain copy of each row in 16-byte chunks.  Each thread loads
     // up to APPEND_BATCH chunks before storing any, so the loads of a pass
-    // overlap instead of paying one memory round trip each.
+    // overlap instead of paying one memory round trip each.  The loads do not
+    // depend on the state and go out while it is still on its way; only the
+    // stores wait for it (and are skipped for a bad state).
     const int esz = bf ? 2 : 4;
     const int lch = __ffs(D * esz / 16) - 1;          // log2(16-byte chunks per row)
     const int all = (2 * rows) << lch;                // K rows, then V rows
@@ -84,7 +86,7 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
       }
 #pragma unroll
       for (int t = 0; t < APPEND_BATCH; ++t) {
-        if (rr[t] < 0) continue;
+        if (!ok || rr[t] < 0) continue;
         const int kvrow = rr[t] >> lch, q = rr[t] & ((1 << lch) - 1);
         const int kv = kvrow >= rows;
         int l, j, g;
