@@ -249,12 +249,7 @@ def run_gpu(args, rank, world):
     # separate calls for pre-RoPE keys (the attention's prologue overlaps the
     # append kernel through programmatic dependent launch, 41.4 against
     # 43.1 us per step on qwen3b), the fused step for the epoch layout.
-    fusable = (layout == "pre_rope" or epoch > 0) and wl.kv_dtype == "bf16" and c == 1 and \
-        args.attend_impl != "fma"
-    path = "split" if args.no_fused else args.path
-    if path == "auto":
-        path = "fused" if epoch > 0 or args.per_layer or args.graph else "split"
-    fused = fusable and path == "fused"
+    fused = step_is_fused(wl, layout, epoch, args)
 
     per_layer = fused and (args.per_layer or args.graph)
     graphs = {}
@@ -383,6 +378,20 @@ def run_gpu(args, rank, world):
                bytes_per_step=bytes_per_step, e2e=e2e, fills=res_fills,
                rerotations=rerotations if layout == "stored_rotated" and epoch else None)
     return res
+
+
+def step_is_fused(wl, layout, epoch, args):
+    """Whether the timed step is the fused rkv_step (else the separate calls).
+    The fused step applies to pre-RoPE keys and to stored-rotated keys with a
+    re-basing epoch, one new pair, bf16, tensor-core kernels; "auto" takes the
+    faster path measured on B300 (the separate calls for pre-RoPE keys, the
+    fused step for the epoch layout; --per-layer and --graph are fused forms)."""
+    fusable = (layout == "pre_rope" or epoch > 0) and wl.kv_dtype == "bf16" and \
+        wl.n_new == 1 and args.attend_impl != "fma"
+    path = "split" if args.no_fused else args.path
+    if path == "auto":
+        path = "fused" if epoch > 0 or args.per_layer or args.graph else "split"
+    return fusable and path == "fused"
 
 
 def _lags(cache):

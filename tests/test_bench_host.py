@@ -1,0 +1,54 @@
+"""Host logic of bench.py on CPU: the step's call sequence per layout, the
+algorithmic bytes, and the source hash that keys the committed DRAM counters."""
+import argparse
+
+import bench
+from rkv_inputs import WORKLOADS
+
+
+def _args(**kw):
+    a = dict(path="auto", no_fused=False, per_layer=False, graph=False, attend_impl="auto")
+    a.update(kw)
+    return argparse.Namespace(**a)
+
+
+def test_auto_path_per_layout():
+    q = WORKLOADS["qwen3b"]
+    # Pre-RoPE keys: the separate calls (faster on B300); the fused forms on request.
+    assert not bench.step_is_fused(q, "pre_rope", 0, _args())
+    assert bench.step_is_fused(q, "pre_rope", 0, _args(path="fused"))
+    assert bench.step_is_fused(q, "pre_rope", 0, _args(per_layer=True))
+    assert bench.step_is_fused(q, "pre_rope", 0, _args(graph=True))
+    assert not bench.step_is_fused(q, "pre_rope", 0, _args(path="fused", no_fused=True))
+    # Stored-rotated keys: fused only with a re-basing epoch.
+    assert bench.step_is_fused(q, "stored_rotated", 4096, _args())
+    assert not bench.step_is_fused(q, "stored_rotated", 4096, _args(path="split"))
+    assert not bench.step_is_fused(q, "stored_rotated", 0, _args(path="fused"))
+
+
+def test_fused_step_needs_one_bf16_pair_and_tensor_cores():
+    assert not bench.step_is_fused(WORKLOADS["qwen3b_chunk6"], "pre_rope", 0, _args(path="fused"))
+    assert not bench.step_is_fused(WORKLOADS["tiny"], "pre_rope", 0, _args(path="fused"))
+    assert not bench.step_is_fused(WORKLOADS["qwen3b"], "pre_rope", 0,
+                                   _args(path="fused", attend_impl="fma"))
+
+
+def test_kv_bytes_per_step_closed_form():
+    q = WORKLOADS["qwen3b"]
+    # 36 layers x 2 KV heads x 4096 pairs x 128 dims x 2 bytes x (K and V)
+    assert bench._kv_bytes_per_step(q, [4096]) == 36 * 2 * 4096 * 128 * 2 * 2 == 150_994_944
+    assert bench._kv_bytes_per_step(q, [10, 20]) == 30 * 36 * 2 * 128 * 2 * 2
+
+
+def test_code_hash_ignores_comments_and_layout_only():
+    a = bench._code_only(b"int a = 1;  // note\n/* block\n comment */\nint b;\n")
+    assert a == bench._code_only(b"int a = 1;\nint b;")
+    assert a != bench._code_only(b"int a = 2;\nint b;")
+
+
+def test_kernel_sources_include_their_headers():
+    src = bench._sources(bench.KERNEL_SOURCE["attend_mma_step"])
+    assert {"rkv_attend_mma.cu", "rkv_attend_pipe.cuh", "rkv_attend_common.cuh",
+            "rkv_device.cuh", "rkv_api.cu", "rkv.h"} <= set(src)
+    assert "rkv_misc.cu" not in src
+    assert "rkv_misc.cu" in bench._sources(bench.KERNEL_SOURCE["rerotate"])
