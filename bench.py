@@ -94,8 +94,10 @@ KERNEL_SOURCE = {
 
 def _sources(main):
     """`main` and the C-ABI entry points (which set the launch parameters and
-    grid), with every header they include, transitively."""
-    dirs = [os.path.join(ROOT, "rolling_kv_cache_buffer_b300", "csrc"), os.path.join(ROOT, "include")]
+    grid), with every library header they include, transitively.  The public
+    header include/rkv.h (declarations and their documentation; no kernel
+    includes it) is not part of a kernel's sources."""
+    dirs = [os.path.join(ROOT, "rolling_kv_cache_buffer_b300", "csrc")]
     seen, todo = {}, [main, "rkv_api.cu"]
     while todo:
         name = todo.pop()

@@ -223,6 +223,23 @@ rkv_status rkv_attend_static_scratch(rkv_handle* h, const void* q, float* out,
 /* Frees the handle (host memory only). */
 rkv_status rkv_destroy(rkv_handle* h);
 
+/* Utterance reset of stream s, with an optional prefix: the stream restarts at
+ * `origin` holding the n_prefix pairs (k, v) -- e.g. a constant prompt
+ * prepared once -- at positions origin .. origin + n_prefix - 1 (re-based
+ * positions 0 .. n_prefix - 1), and its status is cleared; other streams are
+ * untouched.  "Audio8 ASR Infinite..." resets the utterance state when a turn
+ * completes and re-checks a prepared, audio-independent prefix on every
+ * silence reset; the pages do not pin the prefix inside the rolling window, so
+ * later appends evict it like any other pair.
+ * k, v: device, [L][n_prefix][H_kv][D] of kv_dtype, keys before rotation (the
+ * call stores them rotated to 0 .. n_prefix - 1 for STORED_ROTATED), 16-byte
+ * aligned; NULL allowed when n_prefix = 0 (an empty window, as
+ * rkv_set_stream_state(s, origin, 0)).  0 <= s < S, origin >= 0,
+ * 0 <= n_prefix <= W, else RKV_ERR_INVALID_ARG before touching the GPU.
+ * One launch on `stream`, no host synchronisation. */
+rkv_status rkv_reset_stream(rkv_handle* h, int32_t s, int64_t origin, const void* k,
+                            const void* v, int32_t n_prefix, void* stream);
+
 /* Sets stream s to (origin, fill) and clears its status, enqueued on `stream`.
  * The caller must already hold that window's pairs in slots (origin+i) mod W
  * (keys rotated to i for STORED_ROTATED).  Used to seed workloads and to jump

@@ -70,6 +70,7 @@ def load_library():
         "rkv_step_layers": (c_int32, [P, c_int32, c_int32, P, P, P, P, P, c_int32, P]),
         "rkv_destroy": (c_int32, [P]),
         "rkv_set_stream_state": (c_int32, [P, c_int32, c_int64, c_int32, P]),
+        "rkv_reset_stream": (c_int32, [P, c_int32, c_int64, P, P, c_int32, P]),
         "rkv_get_stream_state": (c_int32, [P, P, P, P, P]),
         "rkv_last_launch_count": (c_int32, [P]),
         "rkv_status_string": (c_char_p, [c_int32]),
@@ -149,6 +150,13 @@ def rkv_destroy(h):
 def rkv_set_stream_state(h, s, origin, fill, stream):
     _check(load_library().rkv_set_stream_state(h, s, origin, fill, stream),
            "rkv_set_stream_state")
+
+
+def rkv_reset_stream(h, s, origin, k, v, n_prefix, stream):
+    """Utterance reset of stream s, with n_prefix prefix pairs (k, v) at its
+    start (0: an empty window)."""
+    _check(load_library().rkv_reset_stream(h, s, origin, k, v, n_prefix, stream),
+           "rkv_reset_stream")
 
 
 def rkv_get_stream_state(h, origins, fills, status, stream):
@@ -278,6 +286,19 @@ class RollingKV:
 
     def set_stream_state(self, s, origin, fill):
         rkv_set_stream_state(self.handle, s, origin, fill, self._stream())
+
+    def reset_stream(self, s, origin, k=None, v=None):
+        """Utterance reset of stream s at `origin`, with the prefix k, v
+        ([L][n][H_kv][D] of the cache type, keys before rotation) as the first
+        pairs of its new window, or an empty window."""
+        n, kp, vp = 0, 0, 0
+        if k is not None:
+            n = int(k.shape[1])
+            shape = (self.L, n, self.Hkv, self.D)
+            self._need(k, shape, self.kv_dtype, "k")
+            self._need(v, shape, self.kv_dtype, "v")
+            kp, vp = k.data_ptr(), v.data_ptr()
+        rkv_reset_stream(self.handle, s, origin, kp, vp, n, self._stream())
 
     def get_stream_state(self):
         import numpy as np

@@ -106,3 +106,9 @@ def test_null_handle_calls():
     assert lib.rkv_last_launch_count(None) == 0
     for s in range(6):
         assert R.status_string(s)
+
+
+def test_reset_stream_rejects_bad_arguments_without_gpu():
+    """rkv_reset_stream checks its arguments before touching the GPU."""
+    lib = R.load_library()
+    assert lib.rkv_reset_stream(None, 0, 0, None, None, 0, None) == R.rkv.RKV_ERR_INVALID_ARG

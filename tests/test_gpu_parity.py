@@ -390,6 +390,61 @@ def test_stored_rotated_bf16_head_dim_64():
 
 
 # ----------------------------------------------------------------------------
+# Utterance reset with a prefix
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("layout", ["pre_rope", "stored_rotated"])
+def test_reset_stream_with_prefix(layout):
+    """Stream 1 restarts at a new origin holding a 20-pair prefix while stream 0
+    keeps its window (its pools untouched): outputs match the oracle whose
+    window is set to the same prefix, through the appends that later evict
+    the prefix; states and logs follow the closed form; a sticky status is
+    cleared by the reset; a reset without prefix leaves an empty window."""
+    stored = layout == "stored_rotated"
+    wl = WORKLOADS["qwen3b"].replace(n_streams=2, n_layers=2, capacity=64)
+    cache = make_cache(wl, layout=layout)
+    orc = make_oracle(wl, cls=O.StoredRotatedOracle if stored else O.RollingCacheOracle)
+
+    def step(t):
+        q, k, v = step_inputs(wl, t)
+        cache.append(dev(k, torch.bfloat16), dev(v, torch.bfloat16))
+        orc.append(k.double().numpy(), v.double().numpy())
+        if stored:
+            cache.rebase()
+            orc.rebase()
+        return cache.attend(dev(q, torch.bfloat16)), orc.attend(q.double().numpy())
+
+    for t in range(1, 11):
+        step(t)
+    st32 = cache.state.view(torch.int32)
+    st32[8 * 1 + 2] = 65     # stream 1: fill 65 > W (corrupt) ...
+    st32[8 * 1 + 3] = 5      # ... and flagged
+    n, origin = 20, 777_777
+    kp = random_rows((2, n, 2, 128), 11, torch.bfloat16)   # [L][n][H_kv][D]
+    vp = random_rows((2, n, 2, 128), 12, torch.bfloat16)
+    pool0 = cache.k_pool[0].clone(), cache.v_pool[0].clone()
+    cache.reset_stream(1, origin, dev(kp, torch.bfloat16), dev(vp, torch.bfloat16))
+    orc.set_state(1, origin, n, kp.permute(0, 2, 1, 3).double().numpy(),
+                  vp.permute(0, 2, 1, 3).double().numpy())
+    assert torch.equal(cache.k_pool[0], pool0[0]) and torch.equal(cache.v_pool[0], pool0[1])
+    o, f, st = cache.get_stream_state()
+    assert (int(o[1]), int(f[1]), int(st[1])) == (origin, n, 0)
+    assert (int(o[0]), int(f[0]), int(st[0])) == (0, 10, 0)
+    for t in range(11, 11 + 60):   # stream 1 fills at 64 and then evicts the prefix
+        out, ref = step(t)
+        if t % 6 == 0 or t > 65:
+            compare(out, ref)
+    o, f, st = cache.get_stream_state()
+    assert (int(o[1]), int(f[1]), int(st[1])) == (origin + 20 + 60 - 64, 64, 0)
+    cache.reset_stream(1, 5)
+    orc.set_state(1, 5, 0)
+    o, f, st = cache.get_stream_state()
+    assert (int(o[1]), int(f[1]), int(st[1])) == (5, 0, 0)
+    out, ref = step(71)
+    compare(out, ref)
+
+
+# ----------------------------------------------------------------------------
 # Device-side error paths (no fault: a status word)
 # ----------------------------------------------------------------------------
 
