@@ -265,6 +265,34 @@ def test_cache_matches_brute_force_with_eviction(W, cs, style):
         assert all(0 <= p - cache.origin[0] < W for p in cache.retained_positions(0))
 
 
+@pytest.mark.parametrize("n_prefix,cs", [(5, [1] * 12), (8, [2, 3, 1, 4]), (0, [1, 2, 1])])
+def test_reset_with_prefix_is_a_new_history(n_prefix, cs):
+    """Utterance reset with a prefix (the window set to n prefix pairs at a new
+    origin): every later step equals brute force over the history "prefix,
+    then the appended tokens" from that origin, so the prefix is the oldest
+    part of the window and the first to be evicted."""
+    S, L, Hq, Hkv, D, W = 1, 2, 4, 2, 8, 8
+    origin = 4_321
+    cache = O.RollingCacheOracle(S, L, Hq, Hkv, D, W, theta=1e6)
+    cache.append(RNG.standard_normal((L, S, 3, Hkv, D)), RNG.standard_normal((L, S, 3, Hkv, D)))
+    kp = RNG.standard_normal((L, Hkv, n_prefix, D))
+    vp = RNG.standard_normal((L, Hkv, n_prefix, D))
+    cache.set_state(0, origin, n_prefix, kp, vp)
+    hk = [kp[:, :, i] for i in range(n_prefix)]
+    hv = [vp[:, :, i] for i in range(n_prefix)]
+    for c in cs:
+        k = RNG.standard_normal((L, S, c, Hkv, D))
+        v = RNG.standard_normal((L, S, c, Hkv, D))
+        q = RNG.standard_normal((L, S, c, Hq, D))
+        cache.append(k, v)
+        hk += [k[:, 0, j] for j in range(c)]
+        hv += [v[:, 0, j] for j in range(c)]
+        want = O.brute_force_window(np.array(hk), np.array(hv), q[:, 0], W, c, Hkv,
+                                    theta=1e6, p0=origin)
+        np.testing.assert_allclose(cache.attend(q)[:, 0], want, rtol=1e-9, atol=1e-11)
+    assert cache.origin[0] == origin + max(0, len(hk) - W)
+
+
 def test_brute_force_window_is_last_w_tokens():
     """Brute force itself: with one key per step and q = 0 the output is the
     mean of the values of the last W tokens (closed form)."""
