@@ -52,3 +52,19 @@ def test_kernel_sources_include_their_headers():
             "rkv_device.cuh", "rkv_api.cu"} <= set(src)
     assert "rkv_misc.cu" not in src and "rkv.h" not in src
     assert "rkv_misc.cu" in bench._sources(bench.KERNEL_SOURCE["rerotate"])
+
+
+def test_pack_lays_out_aligned_views():
+    """The e2e loop's packed buffer: each tensor's view starts on a 16-byte
+    boundary, round-trips its contents, and the buffer holds nothing else
+    beyond the alignment padding."""
+    import torch
+    q = torch.randn(36, 1, 1, 16, 128).bfloat16()
+    k = torch.randn(36, 1, 1, 2, 128).bfloat16()
+    x = torch.randn(3).bfloat16()
+    flat, views = bench._pack([q, x, k], lambda n, dt: torch.empty(n, dtype=dt))
+    for view, t in zip(views, (q, x, k)):
+        view.copy_(t)
+        assert torch.equal(view, t) and view.is_contiguous()
+        assert (view.data_ptr() - flat.data_ptr()) % 16 == 0
+    assert flat.numel() == q.numel() + 8 + k.numel()
