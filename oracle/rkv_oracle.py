@@ -45,7 +45,10 @@ something other than itself -- closed forms, torch's bf16 conversion and
 scaled_dot_product_attention, complex-number rotation, brute force over the
 full history, and invariants the pages state.  ``rerotate`` carries the pin
 "identity at delta 0, inverse of rotation before rounding"; its rounding
-step is pinned separately through ``bf16_round``.
+step is pinned separately through ``bf16_round``.  The stored-rotated models'
+``set_state`` (tests/test_oracle_set_state.py) is pinned to complex-number
+rotation rounded by torch's bf16 conversion (key i of a seeded window stored
+as bf16(R(i) k_i)) and to brute force over the history after a reset.
 """
 
 from __future__ import annotations

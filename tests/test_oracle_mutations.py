@@ -117,3 +117,40 @@ def test_query_offset_mutation_is_caught(monkeypatch):
     monkeypatch.setattr(O, "RollingCacheOracle", _ShiftedQuery)
     with pytest.raises(AssertionError):
         T.test_cache_matches_brute_force_with_eviction(8, [1] * 30, O.SPLIT_HALF)
+
+
+# ---- set_state of the stored-rotated models --------------------------------
+
+def _set_state_absolute(self, s, origin, fill, k=None, v=None):
+    """Keys rotated to their absolute position p instead of p - origin."""
+    O.RollingCacheOracle.set_state(self, s, origin, fill, k, v)
+    for p in list(self.window[s].keys()):
+        kk, vv = self.window[s][p]
+        self.window[s][p] = (O.bf16_round(O.rope(kk, p, self.theta, self.style)), vv)
+    if hasattr(self, "lag"):
+        self.lag[s] = 0
+    else:
+        self.pending[s] = 0
+
+
+def _set_state_unrounded(self, s, origin, fill, k=None, v=None):
+    """Rotated keys kept in float64 (the bf16 round forgotten)."""
+    O.RollingCacheOracle.set_state(self, s, origin, fill, k, v)
+    for p in list(self.window[s].keys()):
+        kk, vv = self.window[s][p]
+        self.window[s][p] = (O.rope(kk, p - origin, self.theta, self.style), vv)
+    if hasattr(self, "lag"):
+        self.lag[s] = 0
+    else:
+        self.pending[s] = 0
+
+
+@pytest.mark.parametrize("cls", ["StoredRotatedOracle", "EpochRotatedOracle"])
+@pytest.mark.parametrize("mutant", [_set_state_absolute, _set_state_unrounded],
+                         ids=["absolute_position", "no_bf16_round"])
+def test_set_state_mutation_is_caught(monkeypatch, cls, mutant):
+    from tests import test_oracle_set_state as T2
+    monkeypatch.setattr(getattr(O, cls), "set_state", mutant)
+    kind = "stored" if cls == "StoredRotatedOracle" else "epoch"
+    with pytest.raises(AssertionError):
+        T2.test_set_state_stores_keys_rotated_from_the_new_origin(kind, O.SPLIT_HALF, 987_654, 11)
