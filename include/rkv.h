@@ -252,8 +252,10 @@ rkv_status rkv_set_stream_state(rkv_handle* h, int32_t s, int64_t origin, int32_
 rkv_status rkv_get_stream_state(rkv_handle* h, int64_t* origins, int32_t* fills,
                                 int32_t* status, void* stream);
 
-/* Number of kernel launches the last rkv_append / rkv_attend / rkv_rebase call
- * on this handle enqueued. */
+/* Number of kernels the last enqueuing call on this handle launched: rkv_append,
+ * rkv_attend, rkv_attend_static_scratch (its ticket clear is a memset, not a
+ * kernel), rkv_rebase (0 for PRE_ROPE), rkv_step, rkv_step_layers,
+ * rkv_reset_stream and rkv_set_stream_state. */
 int32_t rkv_last_launch_count(const rkv_handle* h);
 
 /* Static description of a status code. */

@@ -378,6 +378,7 @@ rkv_status rkv_set_stream_state(rkv_handle* h, int32_t s, int64_t origin, int32_
                                 void* stream) {
   if (!h || s < 0 || s >= h->sh.S || origin < 0 || fill < 0 || fill > h->sh.W)
     return RKV_ERR_INVALID_ARG;
+  h->last_launches = 1;
   return cuda_status(
       rkv::launch_set_state(h->state, s, origin, fill, static_cast<int>(origin % h->sh.W),
                             static_cast<cudaStream_t>(stream)));

@@ -68,7 +68,10 @@ extern "C" rkv_status rkv_attend_static_scratch(rkv_handle* h, const void* q, fl
   rkv_status st = scratch_address(&base);
   if (st != RKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's contents; the tickets must start at 0.
+  // Every merge returns its unit's ticket to 0, so after a completed call the
+  // tickets are already 0.  The clear guards against tickets left behind by a
+  // call that aborted (a device-detected error stops a CTA before its merge)
+  // or that used the array for another handle's shape.
   if (cudaMemsetAsync(base, 0, tickets, s) != cudaSuccess) return RKV_ERR_CUDA;
 
   rkv::AttendParams p = {};
@@ -88,6 +91,6 @@ extern "C" rkv_status rkv_attend_static_scratch(rkv_handle* h, const void* q, fl
   p.slot_floats = h->ws.slot_floats;
   p.scale_log2 = h->scale * 1.4426950408889634f;
   const rkv_status ls = rkv::launch_attend_any(h, p, grid, s);
-  if (ls == RKV_OK) h->last_launches = 2;   // the ticket clear and the attention kernel
+  if (ls == RKV_OK) h->last_launches = 1;   // the attention kernel (the clear is a memset)
   return ls;
 }
