@@ -110,17 +110,22 @@ class Bookkeeping:
         return (self.origin, self.fill, self.evicted, self.first_slot)
 
 
-def bookkeep(origin: int, fill: int, n_new: int, capacity: int) -> Bookkeeping:
-    """One append of ``n_new`` pairs to a window of ``capacity`` slots.
+def bookkeep(origin: int, fill: int, n_new: int, capacity: int,
+             slots: int | None = None) -> Bookkeeping:
+    """One append of ``n_new`` pairs to a window that retains ``capacity`` pairs.
 
     [LF] flowchart: a token that does not fit makes the cache "evict oldest
     pair" and "shift sliding origin forward".  Retained absolute positions
     before the step are origin .. origin+fill-1; the new tokens take the next
     positions origin+fill .. origin+fill+n_new-1.  Just enough of the oldest
-    pairs are evicted that the fill never exceeds the capacity.
+    pairs are evicted that the fill never exceeds the capacity.  Position p
+    lives in slot p mod ``slots`` (default: the capacity); a ring with more
+    slots than retained pairs (the 750-frame encoder window of [TT] "At a
+    glance" in 768 slots) keeps the same FIFO.
     """
-    if capacity <= 0:
-        raise ValueError("capacity must be positive")
+    slots = capacity if slots is None else slots
+    if capacity <= 0 or slots < capacity:
+        raise ValueError("capacity must be positive and at most the slot count")
     if n_new < 0 or n_new > capacity:
         raise ValueError("n_new must be in [0, capacity]")
     if origin < 0 or not (0 <= fill <= capacity):
@@ -132,9 +137,9 @@ def bookkeep(origin: int, fill: int, n_new: int, capacity: int) -> Bookkeeping:
         origin=origin + evicted,
         fill=fill + n_new - evicted,
         evicted=evicted,
-        first_slot=first_pos % capacity,
+        first_slot=first_pos % slots,
         new_positions=new_positions,
-        new_slots=[p % capacity for p in new_positions],
+        new_slots=[p % slots for p in new_positions],
         evicted_positions=list(range(origin, origin + evicted)),
     )
 
@@ -229,17 +234,23 @@ class RollingCacheOracle:
     position (p - origin), which leaves query-key distances unchanged.
 
     Per stream the window is an ordered map from absolute position p to the
-    pair (k[L][H_kv][D], v[L][H_kv][D]) in float64.
+    pair (k[L][H_kv][D], v[L][H_kv][D]) in float64.  ``capacity`` is the
+    number of ring slots; ``window`` (default: the capacity) the number of
+    pairs retained, which may be smaller (an encoder's 750-frame window kept
+    in 768 slots, [TT] "At a glance").
     """
 
     def __init__(self, n_streams, n_layers, n_q_heads, n_kv_heads, head_dim,
-                 capacity, theta=1e6, style=SPLIT_HALF, scale=None):
+                 capacity, theta=1e6, style=SPLIT_HALF, scale=None, window=None):
         if n_q_heads % n_kv_heads:
             raise ValueError("n_q_heads must be a multiple of n_kv_heads")
         self.S, self.L = n_streams, n_layers
         self.Hq, self.Hkv, self.D = n_q_heads, n_kv_heads, head_dim
         self.G = n_q_heads // n_kv_heads
         self.W = capacity
+        self.Wr = capacity if window is None else int(window)
+        if not 0 < self.Wr <= capacity:
+            raise ValueError("window must be in [1, capacity]")
         self.theta, self.style = theta, style
         self.scale = (1.0 / math.sqrt(head_dim)) if not scale else float(scale)
         self.origin = [0] * n_streams
@@ -250,7 +261,7 @@ class RollingCacheOracle:
     def set_state(self, s, origin, fill, k=None, v=None):
         """Jump stream ``s`` to (origin, fill) holding the given contents.
         k, v: [L][H_kv][fill][D] in position order (position origin + i)."""
-        if origin < 0 or not (0 <= fill <= self.W):
+        if origin < 0 or not (0 <= fill <= self.Wr):
             raise ValueError("corrupt state")
         self.origin[s], self.fill[s] = int(origin), int(fill)
         self.window[s] = OrderedDict()
@@ -270,7 +281,7 @@ class RollingCacheOracle:
         c = k_new.shape[2]
         logs = []
         for s in range(self.S):
-            bk = bookkeep(self.origin[s], self.fill[s], c, self.W)
+            bk = bookkeep(self.origin[s], self.fill[s], c, self.Wr, self.W)
             for p in bk.evicted_positions:
                 del self.window[s][p]
             for j, p in enumerate(bk.new_positions):
@@ -352,7 +363,7 @@ class StoredRotatedOracle(RollingCacheOracle):
         c = k_new.shape[2]
         logs = []
         for s in range(self.S):
-            bk = bookkeep(self.origin[s], self.fill[s], c, self.W)
+            bk = bookkeep(self.origin[s], self.fill[s], c, self.Wr, self.W)
             for p in bk.evicted_positions:
                 del self.window[s][p]
             for j, p in enumerate(bk.new_positions):
@@ -439,7 +450,7 @@ class EpochRotatedOracle(RollingCacheOracle):
         for s in range(self.S):
             if self.lag[s] >= self.epoch:
                 raise RuntimeError("append before the due re-base")
-            bk = bookkeep(self.origin[s], self.fill[s], c, self.W)
+            bk = bookkeep(self.origin[s], self.fill[s], c, self.Wr, self.W)
             for p in bk.evicted_positions:
                 del self.window[s][p]
             lag2 = self.lag[s] + bk.evicted
