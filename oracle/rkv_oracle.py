@@ -235,27 +235,42 @@ class RollingCacheOracle:
 
     Per stream the window is an ordered map from absolute position p to the
     pair (k[L][H_kv][D], v[L][H_kv][D]) in float64.  ``capacity`` is the
-    number of ring slots; ``window`` (default: the capacity) the number of
-    pairs retained, which may be smaller (an encoder's 750-frame window kept
-    in 768 slots, [TT] "At a glance").
+    number of slots; ``window`` (default: the ring's slot count) the number
+    of pairs retained, which may be smaller (an encoder's 750-frame window
+    kept in 768 slots, [TT] "At a glance").
+
+    Pinned prefix (``n_pinned`` = P > 0 slots, the rest a ring of capacity - P
+    slots): ``reset`` places a constant prefix -- the audio-independent prompt
+    prepared once and checked again on every silence reset ([CPU] "Linux
+    CPU") -- in the pinned slots, where no append evicts it.  The window is
+    read as a re-prefill of "prefix, then the retained tokens" ([TT]
+    "Limitations": the decoder's rolling context is rebuilt by re-prefilling
+    the window): prefix pair i sits at position i, a retained token p at
+    npin + (p - origin), the query of token p_q at npin + (p_q - origin).
     """
 
     def __init__(self, n_streams, n_layers, n_q_heads, n_kv_heads, head_dim,
-                 capacity, theta=1e6, style=SPLIT_HALF, scale=None, window=None):
+                 capacity, theta=1e6, style=SPLIT_HALF, scale=None, window=None,
+                 n_pinned=0):
         if n_q_heads % n_kv_heads:
             raise ValueError("n_q_heads must be a multiple of n_kv_heads")
         self.S, self.L = n_streams, n_layers
         self.Hq, self.Hkv, self.D = n_q_heads, n_kv_heads, head_dim
         self.G = n_q_heads // n_kv_heads
         self.W = capacity
-        self.Wr = capacity if window is None else int(window)
-        if not 0 < self.Wr <= capacity:
-            raise ValueError("window must be in [1, capacity]")
+        self.P = int(n_pinned)
+        if not 0 <= self.P < capacity:
+            raise ValueError("n_pinned must be in [0, capacity)")
+        self.ring = capacity - self.P            # slots of the rolling part
+        self.Wr = self.ring if window is None else int(window)
+        if not 0 < self.Wr <= self.ring:
+            raise ValueError("window must be in [1, capacity - n_pinned]")
         self.theta, self.style = theta, style
         self.scale = (1.0 / math.sqrt(head_dim)) if not scale else float(scale)
         self.origin = [0] * n_streams
         self.fill = [0] * n_streams
         self.window = [OrderedDict() for _ in range(n_streams)]
+        self.prefix = [[] for _ in range(n_streams)]   # pinned (k, v) pairs
 
     # -- state --------------------------------------------------------------
     def set_state(self, s, origin, fill, k=None, v=None):
@@ -265,13 +280,31 @@ class RollingCacheOracle:
             raise ValueError("corrupt state")
         self.origin[s], self.fill[s] = int(origin), int(fill)
         self.window[s] = OrderedDict()
+        self.prefix[s] = []
         for i in range(fill):
             self.window[s][origin + i] = (
                 np.asarray(k[:, :, i, :], np.float64).copy(),
                 np.asarray(v[:, :, i, :], np.float64).copy())
 
+    def reset(self, s, origin, k=None, v=None, n=0):
+        """Utterance reset of stream ``s`` at ``origin`` with an ``n``-pair
+        prefix (k, v: [L][H_kv][n][D]).  With pinned slots the prefix is
+        pinned (n <= n_pinned) and the rolling window starts empty; without,
+        the prefix is the rolling window's first n pairs (``set_state``)."""
+        if not self.P:
+            self.set_state(s, origin, n, k, v)
+            return
+        if not 0 <= n <= self.P:
+            raise ValueError("prefix longer than the pinned slots")
+        self.set_state(s, origin, 0)
+        self.prefix[s] = [(np.asarray(k[:, :, i, :], np.float64).copy(),
+                           np.asarray(v[:, :, i, :], np.float64).copy()) for i in range(n)]
+
     def retained_positions(self, s):
         return list(self.window[s].keys())
+
+    def n_prefix(self, s):
+        return len(self.prefix[s])
 
     # -- append ---------------------------------------------------------------
     def append(self, k_new, v_new):
@@ -281,7 +314,7 @@ class RollingCacheOracle:
         c = k_new.shape[2]
         logs = []
         for s in range(self.S):
-            bk = bookkeep(self.origin[s], self.fill[s], c, self.Wr, self.W)
+            bk = self._bookkeep(s, c)
             for p in bk.evicted_positions:
                 del self.window[s][p]
             for j, p in enumerate(bk.new_positions):
@@ -289,6 +322,14 @@ class RollingCacheOracle:
             self.origin[s], self.fill[s] = bk.origin, bk.fill
             logs.append(bk.log())
         return logs
+
+    def _bookkeep(self, s, c):
+        """The append's bookkeeping in the rolling part: the ring is the slots
+        after the pinned ones, so the logged first slot is P + p mod (W - P)."""
+        bk = bookkeep(self.origin[s], self.fill[s], c, self.Wr, self.ring)
+        bk.first_slot += self.P
+        bk.new_slots = [self.P + x for x in bk.new_slots]
+        return bk
 
     # -- attend ---------------------------------------------------------------
     def _attend(self, q, layer_begin, absolute):
@@ -298,22 +339,28 @@ class RollingCacheOracle:
         for s in range(S):
             pos = np.array(self.retained_positions(s), dtype=np.int64)
             n = len(pos)
+            npin = self.n_prefix(s)
+            if absolute and npin:
+                raise ValueError("a pinned prefix has re-based positions only")
             base = 0 if absolute else self.origin[s]
-            r = pos - base                      # re-based (or absolute) positions
+            # prefix pair i at i, retained token p at npin + (p - base)
+            r = np.concatenate([np.arange(npin), npin + pos - base]).astype(np.int64)
             for li in range(nl):
                 l = layer_begin + li
                 for g in range(self.Hkv):
-                    if n:
-                        K = np.stack([self.window[s][p][0][l, g] for p in pos])
-                        V = np.stack([self.window[s][p][1][l, g] for p in pos])
+                    pairs = [self.prefix[s][i] for i in range(npin)] + \
+                        [self.window[s][p] for p in pos]
+                    if pairs:
+                        K = np.stack([kv[0][l, g] for kv in pairs])
+                        V = np.stack([kv[1][l, g] for kv in pairs])
                         Kr = rope(K, r, self.theta, self.style)
                     for j in range(c):
                         pq = self.origin[s] + n - c + j   # absolute query position
-                        rq = pq - base
-                        vis = pos <= pq
+                        rq = npin + pq - base
+                        vis = np.concatenate([np.ones(npin, bool), pos <= pq])
                         for hh in range(self.G):
                             h = g * self.G + hh
-                            if n == 0:
+                            if not pairs:
                                 continue
                             qr = rope(q[li, s, j, h], rq, self.theta, self.style)
                             out[li, s, j, h] = softmax_attention(
@@ -343,7 +390,10 @@ def rerotate(k_stored, delta, theta, style=SPLIT_HALF):
 
 class StoredRotatedOracle(RollingCacheOracle):
     """Keys are stored as bf16(R(p - origin') k) and re-rotated by R(-e)
-    (then rounded to bf16 again) whenever e pairs are evicted."""
+    (then rounded to bf16 again) whenever e pairs are evicted.  With a pinned
+    prefix, prefix pair i is stored as bf16(R(i) k) once and never turned
+    again (its position does not move); retained keys sit at
+    npin + (p - origin')."""
 
     def __init__(self, *a, **kw):
         super().__init__(*a, **kw)
@@ -357,17 +407,26 @@ class StoredRotatedOracle(RollingCacheOracle):
             self.window[s][p] = (bf16_round(rope(kk, p - origin, self.theta, self.style)), vv)
         self.pending[s] = 0
 
+    def reset(self, s, origin, k=None, v=None, n=0):
+        """As the base class; pinned prefix keys are stored rotated to i."""
+        super().reset(s, origin, k, v, n)
+        self.prefix[s] = [(bf16_round(rope(kk, i, self.theta, self.style)), vv)
+                          for i, (kk, vv) in enumerate(self.prefix[s])]
+        self.pending[s] = 0
+
     def append(self, k_new, v_new):
         k_new = np.asarray(k_new, np.float64)
         v_new = np.asarray(v_new, np.float64)
         c = k_new.shape[2]
         logs = []
         for s in range(self.S):
-            bk = bookkeep(self.origin[s], self.fill[s], c, self.Wr, self.W)
+            bk = self._bookkeep(s, c)
+            npin = self.n_prefix(s)
             for p in bk.evicted_positions:
                 del self.window[s][p]
             for j, p in enumerate(bk.new_positions):
-                kt = bf16_round(rope(k_new[:, s, j], p - bk.origin, self.theta, self.style))
+                kt = bf16_round(rope(k_new[:, s, j], npin + p - bk.origin, self.theta,
+                                     self.style))
                 self.window[s][p] = (kt, v_new[:, s, j].copy())
             self.origin[s], self.fill[s] = bk.origin, bk.fill
             self.pending[s] = bk.evicted
@@ -394,19 +453,22 @@ class StoredRotatedOracle(RollingCacheOracle):
         for s in range(S):
             pos = np.array(self.retained_positions(s), dtype=np.int64)
             n = len(pos)
-            if n == 0:
+            npin = self.n_prefix(s)
+            if n + npin == 0:
                 continue
             for li in range(nl):
                 l = layer_begin + li
                 for g in range(self.Hkv):
-                    K = np.stack([self.window[s][p][0][l, g] for p in pos])
-                    V = np.stack([self.window[s][p][1][l, g] for p in pos])
+                    pairs = list(self.prefix[s]) + [self.window[s][p] for p in pos]
+                    K = np.stack([kv[0][l, g] for kv in pairs])
+                    V = np.stack([kv[1][l, g] for kv in pairs])
                     for j in range(c):
                         pq = self.origin[s] + n - c + j
-                        vis = pos <= pq
+                        vis = np.concatenate([np.ones(npin, bool), pos <= pq])
                         for hh in range(self.G):
                             h = g * self.G + hh
-                            qr = rope(q[li, s, j, h], pq - self.origin[s], self.theta, self.style)
+                            qr = rope(q[li, s, j, h], npin + pq - self.origin[s], self.theta,
+                                      self.style)
                             out[li, s, j, h] = softmax_attention(qr, K[vis], V[vis], self.scale)
         return out
 
@@ -428,6 +490,9 @@ class EpochRotatedOracle(RollingCacheOracle):
         super().__init__(*a, **kw)
         if epoch < 2:
             raise ValueError("epoch >= 2")
+        if self.P:
+            # A pinned key would need the lag in its position as well: not modelled.
+            raise ValueError("no pinned prefix with a re-basing epoch")
         self.epoch = int(epoch)
         self.lag = [0] * self.S
 
@@ -450,7 +515,7 @@ class EpochRotatedOracle(RollingCacheOracle):
         for s in range(self.S):
             if self.lag[s] >= self.epoch:
                 raise RuntimeError("append before the due re-base")
-            bk = bookkeep(self.origin[s], self.fill[s], c, self.Wr, self.W)
+            bk = self._bookkeep(s, c)
             for p in bk.evicted_positions:
                 del self.window[s][p]
             lag2 = self.lag[s] + bk.evicted
@@ -501,6 +566,39 @@ class EpochRotatedOracle(RollingCacheOracle):
 # ---------------------------------------------------------------------------
 # Brute force over the whole history (no ring, no re-basing)
 # ---------------------------------------------------------------------------
+
+def brute_force_reprefill(pre_k, pre_v, hist_k, hist_v, q, window, n_new, n_kv_heads,
+                          theta=1e6, style=SPLIT_HALF, scale=None):
+    """Attention of the ``n_new`` newest tokens over a re-prefilled window:
+    the sequence "prefix, then the last ``window`` tokens of the history",
+    numbered 0, 1, 2, ... from its start ([TT] "Limitations": the rolling
+    context rebuilt by re-prefilling the window), causal.
+
+    pre_k, pre_v: [P][L][H_kv][D]; hist_k, hist_v: [T][L][H_kv][D];
+    q: [L][n_new][H_q][D].  Returns [L][n_new][H_q][D].
+    """
+    pre_k = np.asarray(pre_k, np.float64).reshape((-1,) + np.shape(hist_k)[1:])
+    pre_v = np.asarray(pre_v, np.float64).reshape((-1,) + np.shape(hist_v)[1:])
+    hist_k = np.asarray(hist_k, np.float64)
+    hist_v = np.asarray(hist_v, np.float64)
+    q = np.asarray(q, np.float64)
+    T, L, Hkv, D = hist_k.shape
+    G = q.shape[2] // n_kv_heads
+    sc = (1.0 / math.sqrt(D)) if not scale else scale
+    seq_k = np.concatenate([pre_k, hist_k[max(0, T - window):]])
+    seq_v = np.concatenate([pre_v, hist_v[max(0, T - window):]])
+    n = seq_k.shape[0]
+    out = np.zeros_like(q)
+    for l in range(L):
+        for h in range(q.shape[2]):
+            g = h // G
+            for j in range(n_new):
+                iq = n - n_new + j                      # the query's index in the sequence
+                K = rope(seq_k[: iq + 1, l, g], np.arange(iq + 1), theta, style)
+                qr = rope(q[l, j, h], iq, theta, style)
+                out[l, j, h] = softmax_attention(qr, K, seq_v[: iq + 1, l, g], sc)
+    return out
+
 
 def brute_force_window(hist_k, hist_v, q, capacity, n_new, n_kv_heads,
                        theta=1e6, style=SPLIT_HALF, scale=None, p0=0):
