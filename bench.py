@@ -3,13 +3,12 @@
 One step = one pass of the whole hot path over one batch of synthetic input:
 append one K/V pair per stream and layer (evicting the oldest), re-base the
 origin, and attend every layer's queries over the window.  By default the
-step is the faster of two call sequences measured on B300 for its layout:
-rkv_append + rkv_rebase + rkv_attend (pre-RoPE keys: two launches, the
-re-base being the origin update itself), or the fused rkv_step (one kernel)
-followed by rkv_rebase for stored-rotated keys with a re-basing epoch (the
-re-rotation acts once per epoch); --path picks one.  Default workload: the
-36-layer GQA 16/2 x 128 decoder, one stream, window 4096, full (steady state:
-one pair evicted per step).
+step is the fused rkv_step (one kernel: append + re-base + attend), followed
+by rkv_rebase for stored-rotated keys with a re-basing epoch (the re-rotation
+acts once per epoch), wherever the fused step applies (one new pair per
+stream, bf16); otherwise, or with --path split, rkv_append + rkv_rebase +
+rkv_attend.  Default workload: the 36-layer GQA 16/2 x 128 decoder, one
+stream, window 4096, full (steady state: one pair evicted per step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...      # the float64 CPU oracle
@@ -19,9 +18,10 @@ with CUDA events on the launching stream.  Between steps, outside the events,
 a 256 MiB buffer is written and another 256 MiB read, so every step starts on
 a cold L2 that holds no dirty lines, and a short GPU spin gives the host time
 to enqueue the whole step, so host launch latency never shows up between the
-events.  The append/attend split is timed on extra steps with an event
-between the two kernels.  ``value`` = K/V bytes read per step / event time per step (whole job:
-all ranks' bytes over the slowest rank).  Prints one JSON line (rank 0).
+events.  ``value`` = K/V bytes read per step / event time per step (whole job:
+all ranks' bytes over the slowest rank); the roofline object divides the same
+bytes by the same events' time (the step's launches).  Prints one JSON line
+(rank 0).
 """
 from __future__ import annotations
 
@@ -56,6 +56,9 @@ WORKLOAD_TEXT = {
               "per step, full window",
     "batch64": "64 streams, 36 layers, GQA 16/2 x 128, bf16, window 8192 each, fills uniform in "
                "[1, 8192], origins uniform in [0, 1e6), 1 token per stream per step",
+    "encoder750": "causal audio encoder sliding window: 32 layers, 20 heads x 64 (MHA), bf16, "
+                  "750 frames kept in 768 slots, 4 new frames per step (causal among the 4), "
+                  "full window",
 }
 
 
@@ -88,6 +91,7 @@ KERNEL_SOURCE = {
     "attend_mma": "rkv_attend_mma.cu", "attend_mma_step": "rkv_attend_mma.cu",
     "attend_mma_step_stored": "rkv_attend_mma.cu", "attend_mma_step_layer": "rkv_attend_mma.cu",
     "attend_mma_chunk": "rkv_attend_chunk.cu", "attend_fma": "rkv_attend_fma.cu",
+    "attend_tc_chunk": "rkv_attend_tc.cu",
     "rerotate": "rkv_misc.cu",
 }
 
@@ -211,7 +215,7 @@ def run_gpu(args, rank, world):
     cache = RollingKV(wl.n_streams, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
                       wl.capacity, max_chunk=c, kv_dtype=wl.kv_dtype, layout=layout,
                       rope_theta=wl.rope_theta, attend_impl=args.attend_impl, device=dev,
-                      rebase_epoch=epoch)
+                      rebase_epoch=epoch, window=wl.window or 0)
     # Steady-state windows: random contents (inputs of the path, not its work).
     gen = torch.Generator(device=dev).manual_seed(1234 + rank)
     cache.k_pool.normal_(generator=gen)
@@ -219,7 +223,7 @@ def run_gpu(args, rank, world):
     if wl.random_state:
         origins, fills = initial_states(wl)
     else:
-        origins, fills = [123_456] * wl.n_streams, [wl.capacity] * wl.n_streams
+        origins, fills = [123_456] * wl.n_streams, [wl.retained] * wl.n_streams
     for s in range(wl.n_streams):
         cache.set_stream_state(s, origins[s], fills[s])
     dt = cache.kv_dtype
@@ -247,10 +251,8 @@ def run_gpu(args, rank, world):
     # Which calls make the step.  The fused decode step (rkv_step, one launch)
     # applies to pre-RoPE keys and to stored-rotated keys with a re-basing
     # epoch (then rkv_step + rkv_rebase, whose launch acts once per epoch),
-    # one new pair, bf16.  "auto" takes the faster path measured on B300: the
-    # separate calls for pre-RoPE keys (the attention's prologue overlaps the
-    # append kernel through programmatic dependent launch, 41.4 against
-    # 43.1 us per step on qwen3b), the fused step for the epoch layout.
+    # one new pair, bf16; "auto" takes it wherever it applies (the faster path
+    # measured on B300).
     fused = step_is_fused(wl, layout, epoch, args)
 
     per_layer = fused and (args.per_layer or args.graph)
@@ -271,29 +273,27 @@ def run_gpu(args, rank, world):
             graphs[i] = g
         return graphs[i]
 
-    def step(i, ev=None, split=False):
+    def step(i, ev=None):
         q, k, v = ring[i % len(ring)]
-        if args.graph and fused and not split:
+        if args.graph and fused:
             g = graph_of(i % len(ring))      # captured outside the events
         if ev:
             ev[0].record(stream)
-        if per_layer and not split:
+        if per_layer:
             if args.graph:
                 g.replay()
             else:
                 layer_calls(q, k, v)
-        elif fused and not split:
+        elif fused:
             cache.step(k, v, q, out)
             if layout == "stored_rotated":
                 cache.rebase()
         else:
             cache.append(k, v)
             cache.rebase()
-            if ev and split:
-                ev[1].record(stream)
             cache.attend(q, out)
         if ev:
-            ev[2].record(stream)
+            ev[1].record(stream)
 
     if args.graph and fused:
         for i in range(len(ring)):
@@ -321,14 +321,14 @@ def run_gpu(args, rank, world):
         2 + (1 if layout == "stored_rotated" else 0)
 
     # Timed region: exactly `steps` whole steps, one event pair around each.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize(dev)
     fl = list(fills)
     for _ in range(n_done):
-        fl = [min(wl.capacity, f + c) for f in fl]
+        fl = [min(wl.retained, f + c) for f in fl]
     bytes_per_step = []
     rerotations = 0
     with ClockSampler(dev.index) as clk:
@@ -338,61 +338,52 @@ def run_gpu(args, rank, world):
             step(n_done, evs[i])
             n_done += 1
             if layout == "stored_rotated" and epoch:
-                lags = [g + max(0, f + c - wl.capacity) for g, f in zip(lags, fl)]
+                lags = [g + max(0, f + c - wl.retained) for g, f in zip(lags, fl)]
                 if max(lags) >= epoch:
                     rerotations += 1
                     lags = [0 if g >= epoch else g for g in lags]
-            fl = [min(wl.capacity, f + c) for f in fl]   # each step attends over fill'
+            fl = [min(wl.retained, f + c) for f in fl]   # each step attends over fill'
             bytes_per_step.append(_kv_bytes_per_step(wl, fl))
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
     if world > 1:
         dist.barrier()
-    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
 
-    # Kernel split (outside the timed region): an event between append and
-    # attend, which also keeps the attention from overlapping the append.
-    nsplit = min(args.steps, 50)
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nsplit)]
-    split_bytes = []
-    for i in range(nsplit):
-        cold()
-        step(n_done, sev[i], split=True)
-        n_done += 1
-        fl = [min(wl.capacity, f + c) for f in fl]
-        split_bytes.append(_kv_bytes_per_step(wl, fl))
-    torch.cuda.synchronize(dev)
-    attend_ms = [e[1].elapsed_time(e[2]) for e in sev]
-    append_ms = [e[0].elapsed_time(e[1]) for e in sev]
     res_fills = fl
     total_bytes = sum(bytes_per_step)
     total_ms = sum(step_ms)
     assert torch.isfinite(out).all(), "non-finite attention output"
 
     # e2e: host buffers through the public API, copies inside the timed region.
-    e2e = run_e2e(args, cache, ring, dev, wl, stream, fused) if not args.no_e2e else \
-        {"ms_per_step": float("nan"), "h2d": 0, "d2h": 0}
+    e2e = run_e2e(args, cache, ring, dev, wl, stream, fused, cold) if not args.no_e2e else \
+        {"ms_per_step": float("nan"), "ms_mean": float("nan"), "steps": 0, "h2d": 0, "d2h": 0}
 
     res = dict(total_bytes=total_bytes, total_ms=total_ms, steps=args.steps, fused=fused,
-               step_ms=step_ms, attend_ms=attend_ms, append_ms=append_ms, wall_s=wall,
-               split_bytes=split_bytes,
+               step_ms=step_ms, wall_s=wall,
                clocks=clk.summary(), launches=launches_per_step * args.steps,
                bytes_per_step=bytes_per_step, e2e=e2e, fills=res_fills,
                rerotations=rerotations if layout == "stored_rotated" and epoch else None)
     return res
 
 
+def chunk_on_tc(attend_impl):
+    """Whether chunks (c >= 2) run on the tcgen05 kernel for this attend_impl."""
+    return attend_impl == "tc"
+
+
 def step_is_fused(wl, layout, epoch, args):
     """Whether the timed step is the fused rkv_step (else the separate calls).
     The fused step applies to pre-RoPE keys and to stored-rotated keys with a
     re-basing epoch, one new pair, bf16, tensor-core kernels; "auto" takes the
-    faster path measured on B300 (the separate calls for pre-RoPE keys, the
-    fused step for the epoch layout; --per-layer and --graph are fused forms)."""
+    fused step wherever it applies (the faster path measured on B300: 39.9 us
+    against 43.7 us for the separate calls on the 36-layer decoder;
+    --per-layer and --graph are fused forms)."""
     fusable = (layout == "pre_rope" or epoch > 0) and wl.kv_dtype == "bf16" and \
         wl.n_new == 1 and args.attend_impl != "fma"
     path = "split" if args.no_fused else args.path
     if path == "auto":
-        path = "fused" if epoch > 0 or args.per_layer or args.graph else "split"
+        path = "fused"
     return fusable and path == "fused"
 
 
@@ -417,11 +408,13 @@ def _pack(ts, make):
     return flat, [flat[o:o + t.numel()].view(t.shape) for o, t in zip(offs, ts)]
 
 
-def run_e2e(args, cache, ring, dev, wl, stream, fused):
+def run_e2e(args, cache, ring, dev, wl, stream, fused, cold):
     """The step through the public API from host memory: each step's q, k and
     v sit in one pinned host buffer and go to the device in one copy (the
     library takes the three 16-byte-aligned views of the device buffer); the
-    output comes back in one copy."""
+    output comes back in one copy.  Same L2 regime as the main loop: the cold()
+    flush runs between steps, outside the events; one event pair per step,
+    at least 200 steps; the median and the mean are reported."""
     import torch
     host = []
     for q, k, v in ring[: min(len(ring), 16)]:
@@ -433,8 +426,8 @@ def run_e2e(args, cache, ring, dev, wl, stream, fused):
                                 lambda n, dt: torch.empty(n, dtype=dt, device=dev))
     out = torch.empty(dq.shape, dtype=torch.float32, device=dev)
     hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
-    steps = max(10, args.steps // 2)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    steps = max(200, args.steps // 4)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
 
     def one(i):
         dflat.copy_(host[i % len(host)], non_blocking=True)
@@ -449,17 +442,20 @@ def run_e2e(args, cache, ring, dev, wl, stream, fused):
         hout.copy_(out, non_blocking=True)
 
     for i in range(3):
+        cold()
         one(i)
     torch.cuda.synchronize(dev)
-    ev[0].record(stream)
     for i in range(steps):
+        cold()
+        evs[i][0].record(stream)
         one(i)
-    ev[1].record(stream)
+        evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    ms = ev[0].elapsed_time(ev[1]) / steps
+    per = [e[0].elapsed_time(e[1]) for e in evs]
     h2d = host[0].numel() * host[0].element_size()
     d2h = hout.numel() * hout.element_size()
-    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h}
+    return {"ms_per_step": statistics.median(per), "ms_mean": sum(per) / len(per),
+            "steps": steps, "h2d": h2d, "d2h": d2h}
 
 
 # ---------------------------------------------------------------------------
@@ -484,15 +480,15 @@ class OracleRunner:
         if self.stored and epoch:
             self.orc = O.EpochRotatedOracle(self.S, self.Ls, wl.n_q_heads, wl.n_kv_heads,
                                             wl.head_dim, wl.capacity, theta=wl.rope_theta,
-                                            epoch=epoch)
+                                            epoch=epoch, window=wl.window)
         else:
             cls = O.StoredRotatedOracle if self.stored else O.RollingCacheOracle
             self.orc = cls(self.S, self.Ls, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
-                           wl.capacity, theta=wl.rope_theta)
+                           wl.capacity, theta=wl.rope_theta, window=wl.window)
         if wl.random_state:
             origins, fills = initial_states(wl)
         else:
-            origins, fills = [123_456] * wl.n_streams, [wl.capacity] * wl.n_streams
+            origins, fills = [123_456] * wl.n_streams, [wl.retained] * wl.n_streams
         self.fills = fills
         for s in range(self.S):
             k, v = initial_window(wl, s, fills[s])
@@ -556,7 +552,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="qwen3b", choices=sorted(WORKLOAD_TEXT))
-    ap.add_argument("--attend-impl", default="auto", choices=["auto", "fma", "mma"])
+    ap.add_argument("--attend-impl", default="auto", choices=["auto", "fma", "mma", "tc"])
     ap.add_argument("--ring", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -590,7 +586,7 @@ def main():
             runner.step()
         secs = [runner.step() for _ in range(args.steps)]
         sec = sum(secs) / len(secs)
-        bps = _kv_bytes_per_step(wl, [min(wl.capacity, f + wl.n_new) for f in runner.fills])
+        bps = _kv_bytes_per_step(wl, [min(wl.retained, f + wl.n_new) for f in runner.fills])
         val = bps / sec / 1e9
         line = {
             "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s",
@@ -614,40 +610,44 @@ def main():
     res = run_gpu(args, rank, world)
     ms_local = res["total_ms"] / res["steps"]
     bytes_local = res["total_bytes"] / res["steps"]
-    att_ms = sum(res["attend_ms"]) / len(res["attend_ms"])
-    att_bytes = sum(res["split_bytes"]) / len(res["split_bytes"])
     e2e_ms_local = res["e2e"]["ms_per_step"]
-    ms, e2e_ms, att_ms, all_bytes = combine_ranks(ms_local, e2e_ms_local, att_ms, bytes_local,
-                                                  world, "cuda")
+    ms, e2e_ms, _, all_bytes = combine_ranks(ms_local, e2e_ms_local, ms_local, bytes_local,
+                                             world, "cuda")
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
     value = all_bytes / (ms * 1e-3) / 1e9
-    split = {"append_us": 1e3 * sum(res["append_ms"]) / len(res["append_ms"]),
-             "attend_us": att_ms * 1e3,
-             "timing": "rkv_append + rkv_rebase and rkv_attend timed apart on extra steps "
-                       "(an event between them)"}
+    # The roofline's kernel time is measured on the timed steps themselves, by
+    # the same events: the step's launches are the kernel(s) it names, so
+    # kernel_us <= us_per_step always holds (equality for a one-launch step).
     if res["fused"] and (args.per_layer or args.graph):
         # One launch per layer: the step's bytes over the step's time; kernel_us
         # is the average launch.
         kernel_key = "attend_mma_step_layer"
+        scope = "rkv_step_layers, one launch per layer: the step's time over its launches"
         kern_us = ms_local * 1e3 / wl.n_layers
-        achieved = bytes_local / (ms_local * 1e-3) / 1e9
     elif res["fused"]:
         # The step is one launch of the fused kernel (for stored-rotated keys
         # followed by the re-base launch, which acts once per epoch): the
         # events bracket the kernel.
         stored = _workload(args.workload)[1] == "stored_rotated"
         kernel_key = "attend_mma_step_stored" if stored else "attend_mma_step"
+        scope = "the fused step's one launch (events around it)" + \
+            ("; the re-base launch acts once per epoch" if stored else "")
         kern_us = ms_local * 1e3
-        achieved = bytes_local / (ms_local * 1e-3) / 1e9
     else:
         kernel_key = "attend_fma" if args.attend_impl == "fma" or wl.kv_dtype != "bf16" else \
-            ("attend_mma_chunk" if wl.n_new > 1 else "attend_mma")
-        kern_us = att_ms * 1e3
-        achieved = att_bytes / (att_ms * 1e-3) / 1e9
+            ("attend_mma" if wl.n_new == 1 else
+             "attend_tc_chunk" if chunk_on_tc(args.attend_impl) else "attend_mma_chunk")
+        scope = ("the step's launches: rkv_append, then the attention launched with "
+                 "programmatic dependent launch (its prologue overlaps the append); the "
+                 "attention's own share of the device time is in the committed launch list")
+        kern_us = ms_local * 1e3
+    achieved = bytes_local / (kern_us * (wl.n_layers if res["fused"] and
+                                         (args.per_layer or args.graph) else 1) * 1e-6) / 1e9
+    assert kern_us <= ms_local * 1e3 * (1 + 1e-9)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -675,9 +675,12 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "kernel": kernel_key, "traffic": _traffic(kernel_key),
-                     "kernel_us": kern_us, "split": split},
+                     "kernel_us": kern_us, "kernel_scope": scope},
         "e2e": {"value": all_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "us_per_step": e2e_ms * 1e3, "h2d_bytes_per_step": res["e2e"]["h2d"],
+                "us_per_step": e2e_ms * 1e3, "us_per_step_mean": res["e2e"]["ms_mean"] * 1e3,
+                "steps": res["e2e"]["steps"], "statistic": "median of per-step events",
+                "l2": "cold, as the main loop (flush between steps, outside the events)",
+                "h2d_bytes_per_step": res["e2e"]["h2d"],
                 "d2h_bytes_per_step": res["e2e"]["d2h"]},
         "gpu_launches": res["launches"],
         **({"rerotations_in_timed_region": res["rerotations"]}
@@ -692,7 +695,7 @@ def main():
         while len(secs) < 200 and (len(secs) < 3 or time.perf_counter() - t0 < args.cpu_budget):
             secs.append(runner.step())
         sec = sum(secs) / len(secs)
-        cb = _kv_bytes_per_step(wl, [min(wl.capacity, f + wl.n_new) for f in runner.fills])
+        cb = _kv_bytes_per_step(wl, [min(wl.retained, f + wl.n_new) for f in runner.fills])
         line["cpu_baseline"] = {
             "value": cb / sec / 1e9, "unit": "GB/s", "cores": oracle_cores(), "kind": "oracle",
             "sample": f"{len(secs)} steps of " + runner.sample_text(),

@@ -30,9 +30,14 @@
  *
  * Notation: S streams, L layers, H_q query heads, H_kv KV heads (G = H_q/H_kv
  * query heads share one KV head: head h reads KV head floor(h/G)), D head_dim,
- * W capacity (slots per stream, layer and KV head), c tokens per step.
- * Per stream the state is (origin o, fill n): retained absolute positions are
- * o .. o+n-1 and position p lives in slot p mod W.
+ * W capacity (slots per stream, layer and KV head), P pinned prefix slots
+ * (rkv_config.n_pinned, usually 0) in front of a ring of W_ring = W - P slots,
+ * W_r <= W_ring the retained window (pairs kept; W_r = W_ring unless
+ * rkv_config.window says otherwise), c tokens per step.  Per stream the state
+ * is (origin o, fill n <= W_r, npin pinned prefix pairs): retained absolute
+ * positions are o .. o+n-1 and position p lives in slot P + (p mod W_ring);
+ * prefix pair i lives in slot i.  Re-based positions: prefix pair i at i,
+ * retained pair p at npin + (p - o) (npin = 0 without pinned slots).
  */
 #ifndef RKV_H
 #define RKV_H
@@ -44,7 +49,7 @@
 extern "C" {
 #endif
 
-#define RKV_ABI_VERSION 1
+#define RKV_ABI_VERSION 2
 
 typedef struct rkv_handle rkv_handle;  /* opaque, host memory owned by the library */
 
@@ -79,8 +84,12 @@ typedef enum { RKV_PRE_ROPE = 0, RKV_STORED_ROTATED = 1 } rkv_layout;
 typedef enum { RKV_ROPE_SPLIT_HALF = 0, RKV_ROPE_INTERLEAVED = 1 } rkv_rope_style;
 
 /* Attention kernel family: AUTO picks the tensor-core kernels for bf16
- * caches and the CUDA-core kernel otherwise. */
-typedef enum { RKV_ATTEND_AUTO = 0, RKV_ATTEND_FMA = 1, RKV_ATTEND_MMA = 2 } rkv_attend_impl;
+ * caches and the CUDA-core kernel otherwise; TC runs chunks (c >= 2, c*G <=
+ * 128 rows) on the fifth-generation tensor cores (tcgen05, accumulators in
+ * tensor memory), single queries as AUTO. */
+typedef enum {
+  RKV_ATTEND_AUTO = 0, RKV_ATTEND_FMA = 1, RKV_ATTEND_MMA = 2, RKV_ATTEND_TC = 3
+} rkv_attend_impl;
 
 typedef struct {
   int32_t n_streams;     /* S, 1..1024                                    */
@@ -99,7 +108,21 @@ typedef struct {
   float softmax_scale;   /* 0 => 1/sqrt(D)                                 */
   int32_t rebase_epoch;  /* STORED_ROTATED only: 0 re-rotates at every      */
                          /* eviction; E >= 2 re-rotates once every E        */
-                         /* evictions (see rkv_rebase); E + max_chunk <= W+1 */
+                         /* evictions (see rkv_rebase); E + max_chunk <= W_r+1 */
+  int32_t window;        /* W_r, pairs retained per stream: 0 => W_ring,   */
+                         /* else 1..W_ring.  A window that is not a multiple */
+                         /* of 32 (the causal encoder's 750 frames,         */
+                         /* "audio8-asr-infinite-p150", "At a glance") is   */
+                         /* kept in a ring of W_ring >= W_r slots (768):    */
+                         /* eviction follows W_r, slots follow W_ring;      */
+                         /* max_chunk <= W_r                                */
+  int32_t n_pinned;      /* P, pinned prefix slots: 0, or a multiple of 32  */
+                         /* below W.  rkv_reset_stream then places its      */
+                         /* prefix (<= P pairs) in slots 0.. that no append */
+                         /* evicts; the window reads as "prefix, then the   */
+                         /* retained pairs", numbered from 0 (a re-prefill: */
+                         /* "audio8-asr-infinite-p150", "Limitations").    */
+                         /* Not with rebase_epoch >= 2 (RKV_ERR_UNSUPPORTED) */
 } rkv_config;
 
 typedef struct {
@@ -121,11 +144,11 @@ rkv_status rkv_required_bytes(const rkv_config* cfg, size_t* kv_pool_bytes_each,
 rkv_status rkv_create(const rkv_config* cfg, const rkv_buffers* bufs, void* stream,
                       rkv_handle** out);
 
-/* Appends n_new (1..max_chunk, <= W) pairs to every stream.
+/* Appends n_new (1..max_chunk, <= W_r) pairs to every stream.
  * k_new, v_new: device, [L][S][n_new][H_kv][D] of kv_dtype.
  * Per stream (the flowchart of "Audio8 ASR Infinite...": "evict oldest pair",
  * "shift sliding origin forward"):
- *   e = max(0, n + n_new - W); o' = o + e; n' = n + n_new - e;
+ *   e = max(0, n + n_new - W_r); o' = o + e; n' = n + n_new - e;
  *   new position o + n + j goes to slot (o + n + j) mod W in every layer and
  *   KV head.  STORED_ROTATED stores bf16/f32(R(p - o') k).
  * step_log: NULL or device int64 [S][4] receiving (o', n', e, first_slot).
@@ -223,27 +246,33 @@ rkv_status rkv_attend_static_scratch(rkv_handle* h, const void* q, float* out,
 /* Frees the handle (host memory only). */
 rkv_status rkv_destroy(rkv_handle* h);
 
-/* Utterance reset of stream s, with an optional prefix: the stream restarts at
- * `origin` holding the n_prefix pairs (k, v) -- e.g. a constant prompt
- * prepared once -- at positions origin .. origin + n_prefix - 1 (re-based
- * positions 0 .. n_prefix - 1), and its status is cleared; other streams are
- * untouched.  "Audio8 ASR Infinite..." resets the utterance state when a turn
- * completes and re-checks a prepared, audio-independent prefix on every
- * silence reset; the pages do not pin the prefix inside the rolling window, so
- * later appends evict it like any other pair.
+/* Utterance reset of stream s, with an optional prefix -- e.g. a constant
+ * prompt prepared once: "Audio8 ASR Infinite..." resets the utterance state
+ * when a turn completes, and "Reza2kn/Audio8-ASR-Infinite-Compressed" ("Linux
+ * CPU") re-checks a prepared, audio-independent prefix on every silence
+ * reset.  The stream's status is cleared; other streams are untouched.
+ *  - Without pinned slots (n_pinned = 0): the stream restarts at `origin`
+ *    holding the n_prefix pairs at positions origin .. origin + n_prefix - 1
+ *    (re-based 0 .. n_prefix - 1) as the oldest pairs of its window; later
+ *    appends evict them like any other pair.  0 <= n_prefix <= W_r.
+ *  - With P = n_pinned > 0: the prefix goes into the pinned slots 0 ..
+ *    n_prefix - 1 (re-based positions 0 .. n_prefix - 1), where no append
+ *    evicts it; the rolling window restarts empty at `origin`, its pairs at
+ *    re-based positions n_prefix + (p - o).  0 <= n_prefix <= P.
  * k, v: device, [L][n_prefix][H_kv][D] of kv_dtype, keys before rotation (the
  * call stores them rotated to 0 .. n_prefix - 1 for STORED_ROTATED), 16-byte
  * aligned; NULL allowed when n_prefix = 0 (an empty window, as
- * rkv_set_stream_state(s, origin, 0)).  0 <= s < S, origin >= 0,
- * 0 <= n_prefix <= W, else RKV_ERR_INVALID_ARG before touching the GPU.
+ * rkv_set_stream_state(s, origin, 0)).  0 <= s < S, origin >= 0, n_prefix in
+ * range, else RKV_ERR_INVALID_ARG before touching the GPU.
  * One launch on `stream`, no host synchronisation. */
 rkv_status rkv_reset_stream(rkv_handle* h, int32_t s, int64_t origin, const void* k,
                             const void* v, int32_t n_prefix, void* stream);
 
-/* Sets stream s to (origin, fill) and clears its status, enqueued on `stream`.
- * The caller must already hold that window's pairs in slots (origin+i) mod W
- * (keys rotated to i for STORED_ROTATED).  Used to seed workloads and to jump
- * the origin on an utterance reset.  origin >= 0, 0 <= fill <= W. */
+/* Sets stream s to (origin, fill) with no pinned prefix and clears its status,
+ * enqueued on `stream`.  The caller must already hold that window's pairs in
+ * slots P + ((origin+i) mod W_ring) (keys rotated to i for STORED_ROTATED).
+ * Used to seed workloads and to jump the origin on an utterance reset.
+ * origin >= 0, 0 <= fill <= W_r. */
 rkv_status rkv_set_stream_state(rkv_handle* h, int32_t s, int64_t origin, int32_t fill,
                                 void* stream);
 

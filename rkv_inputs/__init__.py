@@ -43,6 +43,11 @@ class Workload:
     k_outlier_p: float = 0.0
     k_outlier_scale: float = 1.0
     random_state: bool = False
+    window: int | None = None   # pairs retained (None: the capacity)
+
+    @property
+    def retained(self) -> int:
+        return self.capacity if self.window is None else self.window
 
     @property
     def seed(self) -> int:
@@ -64,9 +69,11 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
 
-# The five workloads: a tiny correctness case, the Audio8-ASR-0.1B decoder
-# shape, the Qwen2.5-3B-class decoder shape (single token and 6-token chunks)
-# and 64 independent streams of the latter.
+# The workloads: a tiny correctness case, the Audio8-ASR-0.1B decoder shape,
+# the Qwen2.5-3B-class decoder shape (single token and 6-token chunks), 64
+# independent streams of the latter, and the causal audio encoder's sliding
+# window (32 layers, 750 frames kept in 768 slots, 4 new frames per step,
+# width 1280 split as 20 heads of 64, one KV head per query head).
 WORKLOADS = {
     "tiny": Workload("tiny", 0, 1, 1, 2, 1, 64, 32, "f32", 1, 200),
     "audio8": Workload("audio8", 1, 1, 8, 8, 8, 64, 1024, "bf16", 1, 8192),
@@ -75,6 +82,8 @@ WORKLOADS = {
                               k_outlier_p=0.01, k_outlier_scale=2.0),
     "batch64": Workload("batch64", 4, 64, 36, 16, 2, 128, 8192, "bf16", 1, 2000,
                         random_state=True),
+    "encoder750": Workload("encoder750", 5, 1, 32, 20, 20, 64, 768, "bf16", 4, 5000,
+                           window=750),
 }
 
 

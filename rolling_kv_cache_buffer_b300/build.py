@@ -18,7 +18,7 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "librkv.so")
 INCLUDE = os.path.join(ROOT, "include")
 SOURCES = ["rkv_api.cu", "rkv_misc.cu", "rkv_attend_fma.cu", "rkv_attend_mma.cu",
-           "rkv_attend_chunk.cu", "rkv_attend_static.cu", "rkv_reset.cu"]
+           "rkv_attend_chunk.cu", "rkv_attend_tc.cu", "rkv_attend_static.cu", "rkv_reset.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -25,7 +25,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 rkv_status check_config(const rkv_config* c) {
   if (!c) return RKV_ERR_INVALID_ARG;
   if (c->n_streams < 1 || c->n_layers < 1 || c->n_kv_heads < 1 || c->n_q_heads < 1 ||
-      c->head_dim < 1 || c->capacity < 1 || c->max_chunk < 1 || c->rebase_epoch < 0)
+      c->head_dim < 1 || c->capacity < 1 || c->max_chunk < 1 || c->rebase_epoch < 0 ||
+      c->n_pinned < 0 || c->n_pinned >= c->capacity || c->n_pinned % rkv::TK ||
+      c->window < 0 || c->window > c->capacity - c->n_pinned)
     return RKV_ERR_INVALID_ARG;
   if (c->n_q_heads % c->n_kv_heads) return RKV_ERR_INVALID_ARG;
   if (!(c->rope_theta > 1.0) || !std::isfinite(c->rope_theta)) return RKV_ERR_INVALID_ARG;
@@ -35,14 +37,18 @@ rkv_status check_config(const rkv_config* c) {
   if (c->layout != RKV_PRE_ROPE && c->layout != RKV_STORED_ROTATED) return RKV_ERR_INVALID_ARG;
   if (c->rope_style != RKV_ROPE_SPLIT_HALF && c->rope_style != RKV_ROPE_INTERLEAVED)
     return RKV_ERR_INVALID_ARG;
-  if (c->attend_impl < RKV_ATTEND_AUTO || c->attend_impl > RKV_ATTEND_MMA)
+  if (c->attend_impl < RKV_ATTEND_AUTO || c->attend_impl > RKV_ATTEND_TC)
     return RKV_ERR_INVALID_ARG;
-  if (c->max_chunk > c->capacity) return RKV_ERR_CAPACITY;
+  // Retained window: by default every ring slot (those behind the pinned ones).
+  const int wr = c->window ? c->window : c->capacity - c->n_pinned;
+  if (c->max_chunk > wr) return RKV_ERR_CAPACITY;
   // Lazy re-basing: positions p - o_ref stay below 2W (the RoPE table's rows).
   if (c->rebase_epoch >= 2 &&
-      (c->layout != RKV_STORED_ROTATED || c->rebase_epoch + c->max_chunk > c->capacity + 1))
+      (c->layout != RKV_STORED_ROTATED || c->rebase_epoch + c->max_chunk > wr + 1))
     return RKV_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return RKV_ERR_UNSUPPORTED;
+  // A pinned key would need the lag in its own position too: not built.
+  if (c->n_pinned && c->rebase_epoch >= 2) return RKV_ERR_UNSUPPORTED;
   if (c->capacity % rkv::TK || c->capacity > 65536) return RKV_ERR_UNSUPPORTED;
   if (c->n_streams > kMaxStreams) return RKV_ERR_UNSUPPORTED;
   if (c->kv_dtype == RKV_F32 && c->head_dim == 128) return RKV_ERR_UNSUPPORTED;
@@ -64,6 +70,11 @@ Shape make_shape(const rkv_config* c) {
   s.D = c->head_dim;
   s.W = c->capacity;
   s.NB = c->capacity / rkv::TK;
+  s.P = c->n_pinned;
+  s.NP = c->n_pinned / rkv::TK;
+  s.Wring = c->capacity - c->n_pinned;
+  s.NBr = s.Wring / rkv::TK;
+  s.Wr = c->window ? c->window : s.Wring;
   s.bf16 = c->kv_dtype == RKV_BF16;
   s.q_bf16 = c->q_dtype == RKV_BF16;
   s.style = c->rope_style;
@@ -192,7 +203,10 @@ rkv_status rkv_create(const rkv_config* cfg, const rkv_buffers* bufs, void* stre
   if (!out || !bufs) return RKV_ERR_INVALID_ARG;
   rkv_status st = check_config(cfg);
   if (st != RKV_OK) return st;
-  if (cfg->attend_impl == RKV_ATTEND_MMA && cfg->kv_dtype != RKV_BF16) return RKV_ERR_UNSUPPORTED;
+  // The tensor-core families take bf16 caches only.
+  if ((cfg->attend_impl == RKV_ATTEND_MMA || cfg->attend_impl == RKV_ATTEND_TC) &&
+      cfg->kv_dtype != RKV_BF16)
+    return RKV_ERR_UNSUPPORTED;
   if (!bufs->k_pool || !bufs->v_pool || !bufs->state || !bufs->workspace)
     return RKV_ERR_INVALID_ARG;
   if (!aligned16(bufs->k_pool) || !aligned16(bufs->v_pool) || !aligned16(bufs->state) ||
@@ -224,7 +238,7 @@ rkv_status rkv_create(const rkv_config* cfg, const rkv_buffers* bufs, void* stre
   }
   h->has_map4 = h->sh.bf16 && make_pool_map4(&h->tmK4, h->k_pool, h->sh) &&
                 make_pool_map4(&h->tmV4, h->v_pool, h->sh);
-  if (cfg->attend_impl == RKV_ATTEND_MMA && !h->has_map4) {
+  if ((cfg->attend_impl == RKV_ATTEND_MMA || cfg->attend_impl == RKV_ATTEND_TC) && !h->has_map4) {
     delete h;
     return RKV_ERR_UNSUPPORTED;
   }
@@ -253,7 +267,7 @@ rkv_status rkv_destroy(rkv_handle* h) {
 rkv_status rkv_append(rkv_handle* h, const void* k_new, const void* v_new, int32_t n_new,
                       int64_t* step_log, void* stream) {
   if (!h || !k_new || !v_new) return RKV_ERR_INVALID_ARG;
-  if (n_new > h->sh.W) return RKV_ERR_CAPACITY;
+  if (n_new > h->sh.Wr) return RKV_ERR_CAPACITY;
   if (n_new < 1 || n_new > h->cfg.max_chunk) return RKV_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new) || (step_log && !aligned16(step_log)))
     return RKV_ERR_INVALID_ARG;
@@ -280,7 +294,7 @@ rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_be
   if (!aligned16(q) || !aligned16(out)) return RKV_ERR_INVALID_ARG;
   if (layer_begin < 0 || n_layers < 1 || layer_begin + n_layers > h->sh.L)
     return RKV_ERR_INVALID_ARG;
-  if (n_q > h->sh.W) return RKV_ERR_CAPACITY;
+  if (n_q > h->sh.Wr) return RKV_ERR_CAPACITY;
   if (n_q < 1 || n_q > h->cfg.max_chunk) return RKV_ERR_INVALID_ARG;
   rkv::AttendParams p = {};
   p.sh = h->sh;
@@ -376,11 +390,11 @@ rkv_status rkv_rebase(rkv_handle* h, void* stream) {
 
 rkv_status rkv_set_stream_state(rkv_handle* h, int32_t s, int64_t origin, int32_t fill,
                                 void* stream) {
-  if (!h || s < 0 || s >= h->sh.S || origin < 0 || fill < 0 || fill > h->sh.W)
+  if (!h || s < 0 || s >= h->sh.S || origin < 0 || fill < 0 || fill > h->sh.Wr)
     return RKV_ERR_INVALID_ARG;
   h->last_launches = 1;
   return cuda_status(
-      rkv::launch_set_state(h->state, s, origin, fill, static_cast<int>(origin % h->sh.W),
+      rkv::launch_set_state(h->state, s, origin, fill, static_cast<int>(origin % h->sh.Wring),
                             static_cast<cudaStream_t>(stream)));
 }
 

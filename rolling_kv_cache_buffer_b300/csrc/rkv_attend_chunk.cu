@@ -159,9 +159,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
   using C = ChunkCfg<D, ROTK>;
-  constexpr int TILE = C::TILE, NGRP = C::NGRP, NKB = C::NKB, HALF = C::HALF, HG = C::HG;
+  constexpr int TILE = C::TILE, NGRP = C::NGRP, NKB = C::NKB, HALF = C::HALF;
   constexpr int QSTR = C::QSTR, OSTR = C::OSTR, SLOT = C::SLOT;
-  const int W = p.sh.W, NB = p.sh.NB, G = p.sh.G, NS = p.ns, R = p.R, c = p.c;
+  const int G = p.sh.G, NS = p.ns, R = p.R, c = p.c;
   const int RG = (R + 15) >> 4;   // row groups = warps per team
   const int NTEAM = CCW / RG;     // teams (the launcher keeps RG <= CCW)
   const int R16 = RG * 16;
@@ -250,11 +250,12 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
       const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
       const int x1 = min(u.uend, re);
       const bool has_next = x1 < re;
-      // Positions of the two rows (query j = row / G at fill - c + j); rows
-      // past R see nothing.
-      const int rq0 = rr0 < R ? u.fill - c + rr0 / G : -1;
-      const int rq1 = rr1 < R ? u.fill - c + rr1 / G : -1;
-      const int rq_min = u.fill - c;          // position of the chunk's first query
+      // Positions of the two rows (query j = row / G at npin + fill - c + j,
+      // behind the pinned prefix's npin pairs); rows past R see nothing.
+      const int qbase = u.npin + u.fill - c;  // position of the chunk's first query
+      const int rq0 = rr0 < R ? qbase + rr0 / G : -1;
+      const int rq1 = rr1 < R ? qbase + rr1 / G : -1;
+      const int rq_min = qbase;
 
       // ---- A fragments for the unit: rows rotated once, R(r_j) q ----
       uint32_t qa[NKB][4];
@@ -313,19 +314,17 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j) o[kb][nt][j] = 0.f;
 
-      int r0 = -1;                     // re-based position of the block's first slot
-      for (; active && rb + jb < x1; jb += NTEAM) {
-        const int y = rb + jb;
-        if (r0 < 0) {
-          r0 = block_geo(y, u, W, NB).r0;
-        } else {
-          r0 += NTEAM * TK;              // NTEAM blocks further on along the ring
-          while (r0 >= W) r0 -= W;
-        }
-        const int wrap_at = W - r0;      // keys d >= wrap_at sit at r0 + d - W
+      const int Wg = p.sh.Wring;
+      BlockWalk wk;
+      if (active && rb + jb < x1) wk.init(rb + jb, u, p.sh);
+      for (bool first = true; active && rb + jb < x1; jb += NTEAM, first = false) {
+        if (!first) wk.advance(NTEAM, u, p.sh);   // NTEAM blocks further on
+        const BlockGeo& bg = wk.g;
+        const int r0 = bg.r0;            // re-based position of the block's first slot
+        const int wrap_at = bg.wrap_at;  // keys d >= wrap_at sit at r0 + d - W_ring
         const bool wraps = wrap_at < TK;
-        const bool allvalid = wraps ? (u.fill == W) : (r0 + TK <= u.fill);
-        const int maxpos = wraps ? W - 1 : r0 + TK - 1;
+        const bool allvalid = wraps ? (u.fill == Wg) : (r0 + TK <= bg.lim);
+        const int maxpos = wraps ? u.npin + Wg - 1 : r0 + TK - 1;
         const bool plain = allvalid && maxpos <= rq_min;   // every key seen by every row
         // A team only waits on every NTEAM-th stage, so it may reach one before
         // the stage's previous block has landed: wait for that block's release
@@ -351,9 +350,11 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
               // Keys fastest: eight lanes take keys d..d+7 of the same chunk m,
               // which the tile swizzle and the table layout spread over all banks.
               const int d = un % TK, m = un / TK;
-              const bool useB = d >= wrap_at;                  // past the ring's end
-              rotate_unit<D, STYLE>(ktw, d, m, useB ? trA + HALF : trA, useB ? -1.f : 1.f,
-                                    fine + d * HALF * 8);
+              // Past the ring's end: base R(r0 - W_ring), the stage's second
+              // row |r0 - W_ring| with its sine negated when r0 < W_ring.
+              const bool useB = d >= wrap_at;
+              rotate_unit<D, STYLE>(ktw, d, m, useB ? trA + HALF : trA,
+                                    useB && r0 < Wg ? -1.f : 1.f, fine + d * HALF * 8);
             }
             // These generic writes come before the next asynchronous copy into
             // the stage.
@@ -395,8 +396,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 s[nb][1][e] = a1;
               } else {
                 const int d = nb * 8 + 2 * cq + e;
-                const int r = r0 + d - (d >= wrap_at ? W : 0);
-                const bool in = r < u.fill;
+                const int r = r0 + d - (d >= wrap_at ? Wg : 0);
+                const bool in = r < bg.lim;
                 s[nb][0][e] = (in && r <= rq0) ? a0 : NEG_BIG;
                 s[nb][1][e] = (in && r <= rq1) ? a1 : NEG_BIG;
               }
@@ -451,7 +452,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             // V rows of keys outside the window are zeroed (they may hold anything).
             uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
             if (!allvalid) {
-              auto ok = [&](int d) { return r0 + d - (d >= wrap_at ? W : 0) < u.fill; };
+              auto ok = [&](int d) { return r0 + d - (d >= wrap_at ? Wg : 0) < bg.lim; };
               const int d0 = 16 * kk + 2 * cq;
               mlo = (ok(d0) ? 0x0000ffffu : 0u) | (ok(d0 + 1) ? 0xffff0000u : 0u);
               mhi = (ok(d0 + 8) ? 0x0000ffffu : 0u) | (ok(d0 + 9) ? 0xffff0000u : 0u);

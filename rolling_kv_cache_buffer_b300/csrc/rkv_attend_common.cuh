@@ -18,16 +18,17 @@ namespace rkv {
 
 struct UnitRef {
   int s, l, g;          // stream, layer (within the call), KV head
-  int nb;               // touched blocks per unit of this stream
+  int nb;               // blocks per unit of this stream (pinned prefix, then ring)
   int ustart, uend;     // [ustart, uend): this unit's blocks in the call's list
-  int a;                // origin mod W (slot of the oldest pair)
+  int a;                // origin mod W_ring (ring slot of the oldest retained pair)
   int fill;             // retained pairs
+  int npin;             // pinned prefix pairs
 };
 
 __device__ __forceinline__ int stream_blocks(const AttendParams& p, int s) {
   const StreamState st = p.st[s];
-  if (!state_ok(st, p.sh.W)) return 0;
-  return touched_blocks(st.ring, st.fill, p.sh.NB);
+  if (!state_ok(st, p.sh)) return 0;
+  return unit_blocks(st.ring, st.fill, st.npin, p.sh.NBr);
 }
 
 // pre[s] = first block of stream s in the call's list, pre[S] = total.  One
@@ -55,9 +56,10 @@ __device__ __forceinline__ void build_prefix(const AttendParams& p, int* pre) {
 }
 
 // As build_prefix_warp, and also caches every stream's ring start a = origin
-// mod W (-1 for a stream whose state is not valid) and fill in shared memory,
-// so later unit lookups need no global load; with `slag`, also the lag of
-// stored-rotated keys that follow a re-basing epoch (0 otherwise).
+// mod W_ring with its pinned prefix pairs (pack_an; -1 for a stream whose
+// state is not valid) and fill in shared memory, so later unit lookups need no
+// global load; with `slag`, also the lag of stored-rotated keys that follow a
+// re-basing epoch (0 otherwise).
 __device__ __forceinline__ void build_prefix_cached(const AttendParams& p, int* pre, int* sa,
                                                     int* sfill, int lane, int* slag = nullptr) {
   const int per_unit = p.L_att * p.sh.Hkv;
@@ -68,12 +70,11 @@ __device__ __forceinline__ void build_prefix_cached(const AttendParams& p, int* 
     int v = 0;
     if (s < p.sh.S) {
       const StreamState st = p.st[s];
-      const bool ok = state_ok(st, p.sh.W);
-      const int a = ok ? st.ring : -1;
-      sa[s] = a;
+      const bool ok = state_ok(st, p.sh);
+      sa[s] = ok ? pack_an(st.ring, st.npin) : -1;
       sfill[s] = ok ? st.fill : 0;
       if (slag) slag[s] = (ok && p.sh.epoch) ? st.pending : 0;
-      v = ok ? touched_blocks(a, st.fill, p.sh.NB) * per_unit : 0;
+      v = ok ? unit_blocks(st.ring, st.fill, st.npin, p.sh.NBr) * per_unit : 0;
     }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -95,9 +96,10 @@ __device__ __forceinline__ UnitRef unit_of_cached(int x, const AttendParams& p, 
   }
   UnitRef u;
   u.s = lo;
-  u.a = sa[lo];
+  u.a = sa[lo] & 0xffff;
+  u.npin = sa[lo] >> 16;
   u.fill = sfill[lo];
-  u.nb = touched_blocks(u.a, u.fill, p.sh.NB);
+  u.nb = unit_blocks(u.a, u.fill, u.npin, p.sh.NBr);
   const int xs = x - pre[lo];
   const int ul = xs / u.nb;
   u.l = ul / p.sh.Hkv;
@@ -118,7 +120,8 @@ __device__ __forceinline__ UnitRef unit_of(int x, const AttendParams& p, const i
   const StreamState st = p.st[lo];
   u.a = st.ring;
   u.fill = st.fill;
-  u.nb = touched_blocks(u.a, u.fill, p.sh.NB);
+  u.npin = st.npin;
+  u.nb = unit_blocks(u.a, u.fill, u.npin, p.sh.NBr);
   const int xs = x - pre[lo];
   const int ul = xs / u.nb;
   u.l = ul / p.sh.Hkv;
@@ -128,18 +131,84 @@ __device__ __forceinline__ UnitRef unit_of(int x, const AttendParams& p, const i
   return u;
 }
 
-// Block y of unit u: slot block index and re-based position of its first slot.
+// Block y of unit u.  Its slots blk*TK .. blk*TK+TK-1 hold, for slot d of the
+// block, re-based position r0 + d, or r0 + d - W_ring for d >= wrap_at (the
+// ring's end falls inside the block); the slots at positions below lim are
+// in the window.  Pinned prefix blocks (slots 0.., positions 0..npin-1) come
+// first; a ring block's slot P + x holds retained pair (x - a) mod W_ring, at
+// position npin + that.  Without pinned slots: blk = ring block, r0 =
+// (blk*TK - a) mod W, wrap_at = W - r0, lim = fill.
 struct BlockGeo {
-  int blk;   // slot block: slots blk*TK .. blk*TK+TK-1
-  int r0;    // (blk*TK - a) mod W; slot blk*TK+d has position r0+d, minus W if >= W
+  int blk;       // slot block
+  int r0;        // re-based position of the block's first slot
+  int wrap_at;   // slots d >= wrap_at sit at r0 + d - W_ring (>= TK: none do)
+  int lim;       // slots at positions < lim are in the window
+  int ring;      // 1 for a ring block, 0 for a pinned prefix block
 };
-__device__ __forceinline__ BlockGeo block_geo(int y, const UnitRef& u, int W, int NB) {
+__device__ __forceinline__ BlockGeo block_geo(int y, const UnitRef& u, const Shape& sh) {
   BlockGeo b;
-  b.blk = touched_block(u.a, y - u.ustart, NB);
-  int r0 = b.blk * TK - u.a;
-  b.r0 = r0 < 0 ? r0 + W : r0;
+  const int j = y - u.ustart;
+  const int npb = (u.npin + TK - 1) / TK;
+  if (j < npb) {
+    b.blk = j;
+    b.r0 = j * TK;
+    b.wrap_at = TK;
+    b.lim = u.npin;
+    b.ring = 0;
+    return b;
+  }
+  const int br = touched_block(u.a, j - npb, sh.NBr);
+  int r0 = br * TK - u.a;
+  if (r0 < 0) r0 += sh.Wring;
+  b.blk = sh.NP + br;
+  b.r0 = u.npin + r0;
+  b.wrap_at = sh.Wring - r0;
+  b.lim = u.npin + u.fill;
+  b.ring = 1;
   return b;
 }
+// Position of slot d of block b.
+__device__ __forceinline__ int slot_pos(const BlockGeo& b, int d, int Wring) {
+  return b.r0 + d - (d >= b.wrap_at ? Wring : 0);
+}
+
+// Walks the blocks of one unit: the geometry of the current block, advanced
+// by k blocks with additions and compares only (block_geo, with its
+// remainder, runs once per segment and once where the walk leaves the pinned
+// prefix for the ring).
+struct BlockWalk {
+  BlockGeo g;
+  int j;     // block index within the unit
+  int npb;   // pinned prefix blocks of the unit
+  __device__ __forceinline__ void init(int y, const UnitRef& u, const Shape& sh) {
+    j = y - u.ustart;
+    npb = (u.npin + TK - 1) / TK;
+    g = block_geo(y, u, sh);
+  }
+  // Returns the number of times the walk passed the ring's end (-1 when it
+  // jumped from the pinned prefix to the ring).
+  __device__ __forceinline__ int advance(int k, const UnitRef& u, const Shape& sh) {
+    const int j2 = j + k;
+    int wraps = 0;
+    if (j >= npb) {
+      int br = g.blk - sh.NP + k;
+      while (br >= sh.NBr) br -= sh.NBr;
+      int r0 = g.r0 - u.npin + k * TK;
+      while (r0 >= sh.Wring) { r0 -= sh.Wring; ++wraps; }
+      g.blk = sh.NP + br;
+      g.r0 = u.npin + r0;
+      g.wrap_at = sh.Wring - r0;
+    } else if (j2 < npb) {
+      g.blk = j2;
+      g.r0 = j2 * TK;
+    } else {
+      g = block_geo(u.ustart + j2, u, sh);
+      wraps = -1;
+    }
+    j = j2;
+    return wraps;
+  }
+};
 
 // The blocks one warp handles, in order: for each unit segment of the CTA's
 // range, the warp's contiguous chunk of it.
@@ -184,7 +253,7 @@ __device__ __forceinline__ void zero_empty_units(const AttendParams& p, int t, i
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
     const int s = u / per_stream;
     const StreamState st = p.st[s];
-    if (!(state_ok(st, p.sh.W) && st.fill == 0)) continue;
+    if (!(state_ok(st, p.sh) && st.fill == 0 && st.npin == 0)) continue;
     UnitRef ur;
     ur.s = s;
     ur.l = (u % per_stream) / p.sh.Hkv;
@@ -205,7 +274,8 @@ __device__ __forceinline__ void zero_empty_units_cached(const AttendParams& p, c
   const int units = p.sh.S * per_stream;
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
     const int s = u / per_stream;
-    if (!(sa[s] >= 0 && sfill[s] == 0)) continue;
+    // A valid state, no pinned prefix, no retained pair.
+    if (!(sa[s] >= 0 && (sa[s] >> 16) == 0 && sfill[s] == 0)) continue;
     UnitRef ur;
     ur.s = s;
     ur.l = (u % per_stream) / p.sh.Hkv;

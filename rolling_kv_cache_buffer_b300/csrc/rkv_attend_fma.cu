@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(NWARP * 32, 1)
   using TT = FmaTile<D, BF16>;
   constexpr int E = TT::E, TILE = TT::TILE, DPL = TT::DPL, NSW = FMA_NSW;
   constexpr int HALF = D / 2;
-  const int W = p.sh.W, NB = p.sh.NB, R = p.R, G = p.sh.G;
+  const int R = p.R, G = p.sh.G;
   const int style = p.sh.style;
   const bool rotk = !p.sh.stored_rotated;
 
@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(NWARP * 32, 1)
     int by;
     UnitRef ur;
     if (!iss.next(p, pre, by, ur)) return;
-    const BlockGeo bg = block_geo(by, ur, W, NB);
+    const BlockGeo bg = block_geo(by, ur, p.sh);
     const int ug = static_cast<int>(unit_index(p, ur));
     const uint32_t bar = smem_u32(my_bars + slot_k);
     const uint32_t kd = smem_u32(my_tiles + slot_k * 2 * TILE);
@@ -130,12 +130,13 @@ __global__ void __launch_bounds__(NWARP * 32, 1)
       for (int e = 0; e < DPL; ++e) o[r][e] = 0.f;
     }
     if (cb < ce) {
-      // Queries of this unit rotated to r_j = fill - c + j (+ the stream's lag
-      // when stored-rotated keys follow a re-basing epoch).
+      // Queries of this unit rotated to r_j = npin + fill - c + j (behind the
+      // pinned prefix; + the stream's lag when stored-rotated keys follow a
+      // re-basing epoch).
       const int lag = p.sh.epoch ? p.st[u.s].pending : 0;
       for (int idx = lane; idx < R * HALF; idx += 32) {
         const int row = idx / HALF, i = idx % HALF;
-        const int rq = max(u.fill - p.c + row / G, 0) + lag;
+        const int rq = max(u.npin + u.fill - p.c + row / G, 0) + lag;
         const size_t qo = row_offset(p, u, row);
         const int d1 = pair_d1(i, D, style), d2 = pair_d2(i, D, style);
         const float a = load_elem(p.q, qo + d1, p.sh.q_bf16), b = load_elem(p.q, qo + d2, p.sh.q_bf16);
@@ -155,10 +156,9 @@ __global__ void __launch_bounds__(NWARP * 32, 1)
       if (!dead) {
         const uint8_t* kt = my_tiles + st * 2 * TILE;
         const uint8_t* vt = kt + TILE;
-        const BlockGeo bg = block_geo(y, u, W, NB);
-        int r = bg.r0 + lane;
-        if (r >= W) r -= W;
-        const bool valid = r < u.fill;
+        const BlockGeo bg = block_geo(y, u, p.sh);
+        const int r = slot_pos(bg, lane, p.sh.Wring);   // this lane's key position
+        const bool valid = r < bg.lim;
         // ---- scores: lane = key ----
         float acc[RMAX];
 #pragma unroll
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(NWARP * 32, 1)
 #pragma unroll
         for (int rr = 0; rr < RMAX; ++rr) {
           if (rr < R) {
-            const int rq = u.fill - p.c + rr / G;
+            const int rq = u.npin + u.fill - p.c + rr / G;
             const bool vis = valid && r <= rq;
             const float sc = vis ? acc[rr] * p.scale_log2 : NEG_BIG;
             const float mnew = fmaxf(m[rr], warp_max(sc));

@@ -58,8 +58,12 @@ namespace rkv {
 namespace {
 
 constexpr int NCW = RKV_MMA_NCW;              // consumer warps
-constexpr int MMA_THREADS = (NCW + 1) * 32;   // + the producer warp
 constexpr int CONS_THREADS = NCW * 32;
+// Threads of a CTA: the producer warp, the consumer warps and, in a fused
+// step, one side warp that writes the step's new pairs and publishes the new
+// stream states (off the consumers' path to their first block).
+template <bool FUSED>
+constexpr int mma_threads() { return (1 + NCW + (FUSED ? 1 : 0)) * 32; }
 constexpr int MMA_MAX_STAGES = 16;
 constexpr int BAR_CONS = 1;                   // named barrier of the consumer warps
 constexpr int BAR_PREFIX = 2;                 // the producer warp's block prefix is ready
@@ -95,9 +99,13 @@ __host__ __device__ constexpr size_t mma_smem_bytes(int stage, int fixed, int ns
   return 1024 + (size_t)ns * stage + (size_t)fixed + (size_t)ns * 16 + (size_t)(4 * S + 1) * 4 +
          (rx ? 16 + 16 + (size_t)rx : 0);
 }
-// Cluster merge: rank 0 receives rank 1's NCW warp partials.
+// Cluster merge: rank 0 receives rank 1's partial, already combined over its
+// warps: per consumer thread, m and l of its head and its 4 (D/16) / NCW
+// output elements (see the segment end), stored element-major.
 template <int D>
-constexpr int rx_floats() { return NCW * (16 + 32 * (D / 4)); }
+constexpr int rx_per_thread() { return 2 + (4 * (D / 16)) / NCW; }
+template <int D>
+constexpr int rx_floats() { return rx_per_thread<D>() * CONS_THREADS; }
 
 __device__ __forceinline__ void rot(float& x, float& y, float c, float s) {
   const float a = x * c - y * s;
@@ -145,23 +153,23 @@ __device__ __forceinline__ void rot_pair2(uint32_t& x, uint32_t& y, float4 cs) {
 
 // Fused decode step: what rkv_append of one pair would leave in a stream's
 // state, from the state the step starts from (the bookkeeping of the append
-// kernel: e = max(0, n + 1 - W), o' = o + e, n' = n + 1 - e; stored-rotated
+// kernel: e = max(0, n + 1 - Wr), o' = o + e, n' = n + 1 - e; stored-rotated
 // keys with a re-basing epoch E also carry their lag, which must be below E
 // before the append and grows by e).
 struct StepState {
   bool ok;
-  int e, n2, ring2;   // evictions, fill and origin mod W after the append
-  int new_slot;       // slot of the new pair
+  int e, n2, ring2;   // evictions, fill and origin mod W_ring after the append
+  int new_slot;       // slot of the new pair (behind the P pinned slots)
   int lag2;           // lag after the append (epoch), else 0
 };
 __device__ __forceinline__ StepState step_state(const StreamState& st, const Shape& sh) {
-  const int W = sh.W;
+  const int Wg = sh.Wring;
   StepState r;
-  r.ok = state_ok(st, W) && (!sh.stored_rotated || (sh.epoch && st.pending < sh.epoch));
-  r.e = max(0, st.fill + 1 - W);
+  r.ok = state_ok(st, sh) && (!sh.stored_rotated || (sh.epoch && st.pending < sh.epoch));
+  r.e = max(0, st.fill + 1 - sh.Wr);
   r.n2 = st.fill + 1 - r.e;
-  r.ring2 = st.ring + r.e < W ? st.ring + r.e : st.ring + r.e - W;
-  r.new_slot = st.ring + st.fill < W ? st.ring + st.fill : st.ring + st.fill - W;
+  r.ring2 = st.ring + r.e < Wg ? st.ring + r.e : st.ring + r.e - Wg;
+  r.new_slot = sh.P + (st.ring + st.fill < Wg ? st.ring + st.fill : st.ring + st.fill - Wg);
   r.lag2 = sh.epoch ? st.pending + r.e : 0;
   return r;
 }
@@ -178,11 +186,12 @@ __device__ __forceinline__ void build_prefix_step(const AttendParams& p, int* pr
     const int s = base + lane;
     int v = 0;
     if (s < p.sh.S) {
-      const StepState ss = step_state(p.st[s], p.sh);
-      sa[s] = ss.ok ? ss.ring2 : -1;
+      const StreamState st = p.st[s];
+      const StepState ss = step_state(st, p.sh);
+      sa[s] = ss.ok ? pack_an(ss.ring2, st.npin) : -1;
       sfill[s] = ss.ok ? ss.n2 - 1 : 0;
       slag[s] = ss.ok ? ss.lag2 : 0;
-      v = ss.ok ? touched_blocks(ss.ring2, ss.n2 - 1, p.sh.NB) * per_unit : 0;
+      v = ss.ok ? unit_blocks(ss.ring2, ss.n2 - 1, st.npin, p.sh.NBr) * per_unit : 0;
     }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -198,10 +207,11 @@ __device__ __forceinline__ void build_prefix_step(const AttendParams& p, int* pr
 // unit): the new pair goes into its slot in the pools (this step's attention
 // takes it from the inputs and never reads that slot), and a unit whose window
 // holds only the new pair gets v_new as its output.  Reads the post-append
-// geometry from the CTA's cache (sa = ring start after the append, or -1 for
-// a bad state; sfill = fill after the append minus the new pair), so the new
-// pair's slot is (sa + sfill) mod W.  STORED: stored-rotated keys (with a
-// re-basing epoch), whose new key goes in rotated.
+// geometry from the CTA's cache (sa = ring start after the append with the
+// pinned prefix pairs, or -1 for a bad state; sfill = fill after the append
+// minus the new pair), so the new pair's slot is P + (a + sfill) mod W_ring.
+// STORED: stored-rotated keys (with a re-basing epoch), whose new key goes in
+// rotated.
 template <int D, bool STORED>
 __device__ __forceinline__ void step_prepass(const AttendParams& p, const int* sa,
                                              const int* sfill, const int* slag, int w, int nw,
@@ -212,10 +222,11 @@ __device__ __forceinline__ void step_prepass(const AttendParams& p, const int* s
   const int t = lane, nt = 32;   // one warp per unit
   for (int u = blockIdx.x + gridDim.x * w; u < units; u += gridDim.x * nw) {
     const int s = u / per_stream;
-    const int a = sa[s];
-    if (a < 0) continue;
+    if (sa[s] < 0) continue;
+    const int a = sa[s] & 0xffff, npin = sa[s] >> 16;
     int new_slot = a + sfill[s];
-    if (new_slot >= p.sh.W) new_slot -= p.sh.W;
+    if (new_slot >= p.sh.Wring) new_slot -= p.sh.Wring;
+    new_slot += p.sh.P;
     const int l = (u % per_stream) / p.sh.Hkv, g = u % p.sh.Hkv;
     const size_t src = (((size_t)l * p.sh.S + s) * p.sh.Hkv + g) * D;
     const size_t dst =
@@ -224,7 +235,7 @@ __device__ __forceinline__ void step_prepass(const AttendParams& p, const int* s
     if constexpr (STORED) {
       // Stored-rotated keys (with an epoch): the new key goes in rotated to
       // its position from o_ref, n' - 1 + lag', four pairs per lane.
-      const size_t trow = (size_t)(sfill[s] + slag[s]) * (D / 2);
+      const size_t trow = (size_t)(npin + sfill[s] + slag[s]) * (D / 2);
       for (int i = t; i < D / 8; i += nt) {
         float ka[4], kb[4];
         float2 cs[4];
@@ -243,7 +254,7 @@ __device__ __forceinline__ void step_prepass(const AttendParams& p, const int* s
           static_cast<uint8_t*>(kv ? p.v_pool : p.k_pool) + dst * esz) + q;
       *to = *from;
     }
-    if (sfill[s] == 0) {   // only the new pair: softmax over one key gives v_new
+    if (sfill[s] == 0 && npin == 0) {   // only the new pair: softmax over one key gives v_new
       UnitRef ur;
       ur.s = s; ur.l = l; ur.g = g;
       for (int i = t; i < p.sh.G * D; i += nt) {
@@ -254,15 +265,53 @@ __device__ __forceinline__ void step_prepass(const AttendParams& p, const int* s
   }
 }
 
+// The fused step's publish: every CTA reads the old states in its prologue and
+// keeps what it needs in shared memory; once all have, the last CTA past this
+// point writes the new ones (the append's bookkeeping), one stream per lane of
+// the calling warp, on the step's last launch only.
+__device__ __forceinline__ void step_publish(const AttendParams& p, int lane) {
+  int last = 0;
+  if (lane == 0) {
+    __threadfence();
+    last = atomicAdd(p.step_ticket, 1) == static_cast<int>(gridDim.x) - 1;
+    if (last) __threadfence();
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  for (int s2 = lane; s2 < p.sh.S; s2 += 32) {
+    const StreamState st = p.st[s2];
+    const StepState ss = step_state(st, p.sh);
+    StreamState ns = st;
+    if (ss.ok) {
+      ns.origin = st.origin + ss.e;
+      ns.fill = ss.n2;
+      ns.ring = ss.ring2;
+      ns.pending = ss.lag2;
+      ns.last_new = 1;
+    } else if (ns.status == 0) {
+      ns.status = STATUS_DEVICE_STATE;
+    }
+    p.st[s2] = ns;
+    if (p.log) {
+      long long* lg = p.log + 4 * (size_t)s2;
+      lg[0] = ss.ok ? ns.origin : st.origin;
+      lg[1] = ss.ok ? ns.fill : st.fill;
+      lg[2] = ss.ok ? ss.e : -1;
+      lg[3] = ss.ok ? ss.new_slot : -1;
+    }
+  }
+  if (lane == 0) *p.step_ticket = 0;
+}
+
 template <int D, bool ROTK, int STYLE, bool FUSED, bool CL>
-__global__ void __launch_bounds__(MMA_THREADS, 1)
+__global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
     attend_mma_decode(const __grid_constant__ AttendParams p,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
   using C = MmaCfg<D, ROTK>;
   constexpr int TILE = C::TILE, NGRP = C::NGRP, NKB = C::NKB, HALF = C::HALF, HG = C::HG;
   constexpr int QSTR = C::QSTR;
-  const int W = p.sh.W, NB = p.sh.NB, G = p.sh.G, NS = p.ns;
+  const int G = p.sh.G, NS = p.ns;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -290,9 +339,10 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
   // Cluster merge (CL): the pair of CTAs that shares a unit meets here.
   uint64_t* rx_bar = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(slag + p.sh.S) + 15) & ~uintptr_t(15));
-  float* rslots = reinterpret_cast<float*>(rx_bar + 2);            // [NCW][SLOT] rank 1's slots
+  float* rslots = reinterpret_cast<float*>(rx_bar + 2);            // rank 1's partial
   volatile int* abort_flag = flag + 1;
 
+  constexpr int NTHR = mma_threads<FUSED>();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Prologue that reads nothing the previous kernel of the stream writes: the
   // barriers and the R(d) table (written once when the handle was created).
@@ -314,11 +364,11 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     flag[2] = 0;
   }
   if constexpr (ROTK) {
-    if (warp > 0) {
+    if (warp > 0 && warp <= NCW) {
       load_fine<D, STYLE>(p, fine, tid - 32, CONS_THREADS);
       // The constant steps of the query bases: R(-NPAIR*TK), the NPAIR-th
       // power of table row TK with its sine negated (rows stop below 2W, and
-      // TK < 2W always), and R(W) (row W).
+      // TK < 2W always), and R(W_ring) (row W_ring).
       for (int i = tid - 32; i < 2 * HALF; i += CONS_THREADS) {
         const int k = i % HALF;
         if (i < HALF) {
@@ -328,7 +378,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             a = make_float2(a.x * c.x - a.y * c.y, a.x * c.y + a.y * c.x);
           srow[k] = make_float2(a.x, -a.y);
         } else {
-          Wrow[k] = __ldg(p.table + (size_t)W * HALF + k);
+          Wrow[k] = __ldg(p.table + (size_t)p.sh.Wring * HALF + k);
         }
       }
     }
@@ -358,9 +408,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     else
       build_prefix_cached(p, pre, sa, sfill, lane, slag);
     __syncwarp();
-    named_bar_arrive(BAR_PREFIX, MMA_THREADS);
+    named_bar_arrive(BAR_PREFIX, NTHR);
   } else {
-    named_bar_sync(BAR_PREFIX, MMA_THREADS);
+    named_bar_sync(BAR_PREFIX, NTHR);
   }
   const int T = pre[p.sh.S];
   const int P = min(static_cast<int>(gridDim.x), T);
@@ -371,8 +421,15 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     // ------------------------------------------------------------------ producer
     if (lane == 0)
       flag[2] = produce<D, ROTK, NO_ROWS>(p, &tmK, &tmV, stages, full, empty, mdone, pre, sa,
-                                          sfill, rb, re, abort_flag, FUSED ? 1 : 0);
+                                          sfill, rb, re, abort_flag);
     __syncwarp();
+    if constexpr (CL) cluster_wait();
+  } else if (FUSED && warp == NCW + 1) {
+    // ------------------------------------------------------------------ side warp
+    // The step's new pairs into their slots (every unit once over the grid),
+    // then, on the step's last launch, the new stream states.
+    step_prepass<D, !ROTK>(p, sa, sfill, slag, 0, 1, lane);
+    if (p.publish) step_publish(p, lane);
     if constexpr (CL) cluster_wait();
   } else {
     // ------------------------------------------------------------------ consumers
@@ -432,57 +489,13 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     for (int i = ct; i < (8 - G) * D; i += CONS_THREADS)
       qs[(G + i / D) * QSTR + i % D] = 0.f;
     if (rb < re) stage_unit(unit_of_cached(rb, p, pre, sa, sfill));
-    if constexpr (FUSED)
-      step_prepass<D, !ROTK>(p, sa, sfill, slag, cw, NCW, lane);
-    else
-      zero_empty_units_cached(p, sa, sfill, ct, CONS_THREADS);
+    if constexpr (!FUSED) zero_empty_units_cached(p, sa, sfill, ct, CONS_THREADS);
     if (rb < re) {
       unstage_q();
       if constexpr (FUSED) unstage_new();
     }
     named_bar_sync(BAR_CONS, CONS_THREADS);
     if constexpr (CL) cluster_wait();   // long after both CTAs arrived
-    if constexpr (FUSED) {
-      // Every CTA reads the old states in its prologue and keeps what it needs
-      // in shared memory; once all have, the last CTA past this point
-      // publishes the new ones (the append's bookkeeping), one stream per
-      // lane of the last consumer warp, on the step's last launch only.
-      if (cw == NCW - 1 && p.publish) {
-        int last = 0;
-        if (lane == 0) {
-          __threadfence();
-          last = atomicAdd(p.step_ticket, 1) == static_cast<int>(gridDim.x) - 1;
-          if (last) __threadfence();
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          for (int s2 = lane; s2 < p.sh.S; s2 += 32) {
-            const StreamState st = p.st[s2];
-            const StepState ss = step_state(st, p.sh);
-            StreamState ns = st;
-            if (ss.ok) {
-              ns.origin = st.origin + ss.e;
-              ns.fill = ss.n2;
-              ns.ring = ss.ring2;
-              ns.pending = ss.lag2;
-              ns.last_new = 1;
-            } else if (ns.status == 0) {
-              ns.status = STATUS_DEVICE_STATE;
-            }
-            p.st[s2] = ns;
-            if (p.log) {
-              long long* lg = p.log + 4 * (size_t)s2;
-              lg[0] = ss.ok ? ns.origin : st.origin;
-              lg[1] = ss.ok ? ns.fill : st.fill;
-              lg[2] = ss.ok ? ss.e : -1;
-              lg[3] = ss.ok ? ss.new_slot : -1;
-            }
-          }
-          if (lane == 0) *p.step_ticket = 0;
-        }
-      }
-    }
-
     // Dims of the thread's A-fragment elements: k-block kb, j in {0,1,2,3}:
     //   dim 16kb + (j>>1)*8 + 2cq + (j&1)
     auto qdim = [&](int kb, int j) { return 16 * kb + (j >> 1) * 8 + 2 * cq + (j & 1); };
@@ -495,7 +508,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
     for (int x = rb; x < re;) {
       const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
       const int x1 = min(u.uend, re);
-      const int rq = u.fill - 1 + (FUSED ? 1 : 0);   // the query's re-based position
+      // The query's re-based position, behind the pinned prefix's npin pairs.
+      const int rq = u.npin + u.fill - 1 + (FUSED ? 1 : 0);
       // The next segment's query (and new pair): copied now, converted once
       // this segment is done with `qs` (and `kvn`).
       const bool has_next = x1 < re;
@@ -557,18 +571,24 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       // The warp's query base R(r_q - r0) as a row of (cos, sin) per pair
       // (lane t holds pairs 2t and 2t+1 of `qrow`): seeded from the table for
       // the warp's first block of the segment, then stepped from block to
-      // block by R(-NPAIR*TK), and by R(W) where the ring wraps.
+      // block by R(-NPAIR*TK), and by R(W_ring) where the ring wraps; seeded
+      // again from the table where the blocks jump (pinned prefix to ring).
       float4 seed = make_float4(0.f, 0.f, 0.f, 0.f);
       bool seeded = true;
       float2* my_row = qrow + cw * HALF;
+      auto table_row = [&](int r) {    // R(r_q - r) for this lane's two pairs
+        const int m0 = rq - r;
+        const int am = m0 < 0 ? -m0 : m0;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (2 * lane < HALF) {
+          v = __ldg(reinterpret_cast<const float4*>(p.table + (size_t)am * HALF) + lane);
+          if (m0 < 0) { v.y = -v.y; v.w = -v.w; }
+        }
+        return v;
+      };
       if constexpr (ROTK) {
         if (rb + jb < x1) {
-          const int m0 = rq - block_geo(rb + jb, u, W, NB).r0;
-          const int am = m0 < 0 ? -m0 : m0;
-          if (2 * lane < HALF) {
-            seed = __ldg(reinterpret_cast<const float4*>(p.table + (size_t)am * HALF) + lane);
-            if (m0 < 0) { seed.y = -seed.y; seed.w = -seed.w; }
-          }
+          seed = table_row(block_geo(rb + jb, u, p.sh).r0);
           seeded = false;
         }
       }
@@ -581,27 +601,35 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
                           a.z * b.z - a.w * b.w, a.z * b.w + a.w * b.z);
         }
       };
+      const int Wg = p.sh.Wring;
+      BlockWalk wk;
+      if (rb + jb < x1) wk.init(rb + jb, u, p.sh);
       for (; rb + jb < x1; jb += NPAIR) {
-        const int y = rb + jb;
-        if (r0 < 0) {
-          r0 = block_geo(y, u, W, NB).r0;
-        } else {
-          r0 += NPAIR * TK;              // NPAIR blocks further on along the ring
+        if (r0 >= 0) {
+          // NPAIR blocks further on: the query base turns by R(-NPAIR*TK), and
+          // by R(W_ring) each time the ring's end is passed; where the blocks
+          // jump (pinned prefix to ring) it is seeded from the table again.
+          const int wraps = wk.advance(NPAIR, u, p.sh);
           if constexpr (ROTK) {
-            __syncwarp();
-            cmul_row(my_row, srow);
-          }
-          while (r0 >= W) {
-            r0 -= W;
-            if constexpr (ROTK) {
+            if (wraps >= 0) {
               __syncwarp();
-              cmul_row(my_row, Wrow);
+              cmul_row(my_row, srow);
+              for (int i = 0; i < wraps; ++i) {
+                __syncwarp();
+                cmul_row(my_row, Wrow);
+              }
+            } else {
+              const float4 v = table_row(wk.g.r0);
+              __syncwarp();
+              if (2 * lane < HALF) reinterpret_cast<float4*>(my_row)[lane] = v;
             }
           }
         }
-        const int wrap_at = W - r0;      // keys d >= wrap_at sit at r0 + d - W
+        const BlockGeo& bg = wk.g;
+        r0 = bg.r0;
+        const int wrap_at = bg.wrap_at;  // keys d >= wrap_at sit at r0 + d - W_ring
         const bool wraps = wrap_at < TK;
-        const bool allvalid = wraps ? (u.fill == W) : (r0 + TK <= u.fill);
+        const bool allvalid = wraps ? (u.fill == Wg) : (r0 + TK <= bg.lim);
         const bool plain = allvalid && !wraps;   // every key visible, one base
         {
           const int st_i = stage, st_r = round;
@@ -726,8 +754,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
               for (int e = 0; e < 2; ++e) {
                 const int d = hh * TKH + nb * 8 + 2 * cq + e;
                 const bool wr = ROTK && d >= wrap_at;
-                const int r = r0 + d - (d >= wrap_at ? W : 0);
-                const bool vis = allvalid || r < u.fill;
+                const int r = r0 + d - (d >= wrap_at ? Wg : 0);
+                const bool vis = allvalid || r < bg.lim;
                 s[nb][e] = vis ? (wr ? accs[2 + e] : accs[e]) * p.scale_log2 : NEG_BIG;
               }
             }
@@ -766,7 +794,7 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             // V rows of keys outside the window are zeroed (they may hold anything).
             uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
             if (!allvalid) {
-              auto ok = [&](int d) { return r0 + d - (d >= wrap_at ? W : 0) < u.fill; };
+              auto ok = [&](int d) { return r0 + d - (d >= wrap_at ? Wg : 0) < bg.lim; };
               const int d0 = hh * TKH + 2 * cq;
               mlo = (ok(d0) ? 0x0000ffffu : 0u) | (ok(d0 + 1) ? 0xffff0000u : 0u);
               mhi = (ok(d0 + 8) ? 0x0000ffffu : 0u) | (ok(d0 + 9) ? 0xffff0000u : 0u);
@@ -800,14 +828,17 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
       // Once every consumer is done with the stages (the producer issues
       // nothing more until the merge is over), each warp leaves (m, l, O^T)
       // of its blocks in its slot, in the stage memory; after one more barrier
-      // every thread combines the slots for its output elements.  In a
-      // 2-CTA cluster that splits the unit, rank 1 writes its slots straight
-      // into rank 0's receive area (asynchronous stores that complete bytes on
-      // rank 0's barrier) and is done; rank 0 combines all 2*NCW slots.
+      // every thread combines the NCW slots for its output elements into this
+      // CTA's partial.  In a 2-CTA cluster that splits the unit, rank 1 sends
+      // its partial (per thread: m, l and its few elements) straight into rank
+      // 0's receive area (asynchronous stores that complete bytes on rank 0's
+      // barrier) and is done; rank 0 folds it into its own and writes the
+      // output.  Otherwise the partial is the output (whole unit) or goes to
+      // the unit's ticket merge in global memory.
       named_bar_sync(BAR_CONS, CONS_THREADS);
       const bool whole = (x == u.ustart) && (x1 == u.uend);
-      const bool ship = CL && !whole && x != u.ustart;      // rank 1: slots go to rank 0
-      const bool receive = CL && !whole && x == u.ustart;   // rank 0: waits for them
+      const bool ship = CL && !whole && x != u.ustart;      // rank 1: partial goes to rank 0
+      const bool receive = CL && !whole && x == u.ustart;   // rank 0: waits for it
       // The CTA that finishes the unit adds the fused step's new pair.
       const bool add_new = FUSED && (CL ? x == u.ustart : x1 == u.uend);
       {
@@ -824,74 +855,90 @@ __global__ void __launch_bounds__(MMA_THREADS, 1)
             if (lane == 0) mx[cw] = dot * p.scale_log2;
           }
         }
-        if (ship) {
-          const uint32_t peer = cluster_rank() ^ 1u;
-          const uint32_t dst = map_to_rank(smem_u32(rslots + cw * C::SLOT), peer);
-          const uint32_t bar = map_to_rank(smem_u32(rx_bar), peer);
-          if (cq == 0) {
-            st_async_f32(dst + 4u * g, m_run, bar);
-            st_async_f32(dst + 4u * (8 + g), lsum, bar);
-          }
+        float* my = slots + cw * C::SLOT;
+        if (cq == 0) { my[g] = m_run; my[8 + g] = lsum; }
 #pragma unroll
-          for (int i = 0; i < C::FR; ++i)
-            st_async_f32(dst + 4u * (16 + 32 * i + lane), o[i >> 2][i & 3], bar);
-        } else {
-          float* my = slots + cw * C::SLOT;
-          if (cq == 0) { my[g] = m_run; my[8 + g] = lsum; }
-#pragma unroll
-          for (int i = 0; i < C::FR; ++i) my[16 + 32 * i + lane] = o[i >> 2][i & 3];
-        }
+        for (int i = 0; i < C::FR; ++i) my[16 + 32 * i + lane] = o[i >> 2][i & 3];
       }
       named_bar_sync(BAR_CONS, CONS_THREADS);
       if (has_next) unstage_q();
       const int R = p.R;   // == G for decode
-      bool got = true;
-      if (receive) {
-        got = false;
-        for (uint32_t i = 0; i < WAIT_LIMIT && !got; ++i)
-          got = mbar_try_wait_cluster(smem_u32(rx_bar), 0);
-        if (!got && ct == 0) {
-          *abort_flag = 1;
-          p.st[u.s].status = STATUS_DEVICE_STATE;
-        }
-      }
-      if (!ship && got) {
-        // Thread ct takes fragment element i of lane lf for i = ct/32, ct/32 +
-        // NCW, ...: head h = 2(lf & 3) + (i & 1) is the same for all of them.
+      {
+        // Thread ct takes fragment elements i = ct/32, ct/32 + NCW, ... of lane
+        // lf: head h = 2(lf & 3) + (i & 1) is the same for all of them.
+        constexpr int NE = C::FR / NCW;       // output elements per thread
         const int lf = ct & 31, i0 = ct >> 5;
         const int h = 2 * (lf & 3) + (i0 & 1);
-        const int nsl = receive ? 2 * NCW : NCW;
-        auto slot = [&](int w) { return w < NCW ? slots + w * C::SLOT : rslots + (w - NCW) * C::SLOT; };
-        float M = add_new ? mx[h] : NEG_BIG;
-        for (int w = 0; w < nsl; ++w) M = fmaxf(M, slot(w)[h]);
-        float sc[2 * NCW];
-        float L = 0.f;
+        float M = NEG_BIG;
 #pragma unroll
-        for (int w = 0; w < 2 * NCW; ++w) {
-          sc[w] = 0.f;
-          if (w < nsl) {
-            sc[w] = exp2f(slot(w)[h] - M);
-            L += sc[w] * slot(w)[8 + h];
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, slots[w * C::SLOT + h]);
+        float sc[NCW], L = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+          sc[w] = exp2f(slots[w * C::SLOT + h] - M);
+          L += sc[w] * slots[w * C::SLOT + 8 + h];
+        }
+        float v[NE];
+        int dd[NE];
+#pragma unroll
+        for (int k = 0; k < NE; ++k) {
+          const int i = i0 + k * NCW;
+          dd[k] = 16 * (i >> 2) + (lf >> 2) + (((i >> 1) & 1) << 3);
+          float a = 0.f;
+#pragma unroll
+          for (int w = 0; w < NCW; ++w) a += sc[w] * slots[w * C::SLOT + 16 + 32 * i + lf];
+          v[k] = a;
+        }
+        if (ship) {
+          const uint32_t peer = cluster_rank() ^ 1u;
+          const uint32_t dst = map_to_rank(smem_u32(rslots + ct), peer);
+          const uint32_t bar = map_to_rank(smem_u32(rx_bar), peer);
+          st_async_f32(dst, M, bar);
+          st_async_f32(dst + 4u * CONS_THREADS, L, bar);
+#pragma unroll
+          for (int k = 0; k < NE; ++k) st_async_f32(dst + 4u * (2 + k) * CONS_THREADS, v[k], bar);
+        } else {
+          bool got = true;
+          if (receive) {
+            got = false;
+            for (uint32_t i = 0; i < WAIT_LIMIT && !got; ++i)
+              got = mbar_try_wait_cluster(smem_u32(rx_bar), 0);
+            if (!got && ct == 0) {
+              *abort_flag = 1;
+              p.st[u.s].status = STATUS_DEVICE_STATE;
+            }
+            if (got) {
+              // Rank 1's partial of the same elements.
+              const float M1 = rslots[ct], L1 = rslots[CONS_THREADS + ct];
+              const float Mx = fmaxf(M, M1);
+              const float s0 = exp2f(M - Mx), s1 = exp2f(M1 - Mx);
+              L = s0 * L + s1 * L1;
+#pragma unroll
+              for (int k = 0; k < NE; ++k) v[k] = s0 * v[k] + s1 * rslots[(2 + k) * CONS_THREADS + ct];
+              M = Mx;
+            }
           }
-        }
-        const float scn = add_new ? exp2f(mx[h] - M) : 0.f;
-        L += scn;
-        float* part = nullptr;
-        if (!whole && !CL) {
-          part = p.partials + (size_t)(2 * b + (x == rb ? 0 : 1)) * p.slot_floats;
-          if (lf < 4 && i0 < 2 && h < R) { part[h] = M; part[R + h] = L; }
-        }
-        for (int i = i0; i < C::FR; i += NCW) {
-          const int d = 16 * (i >> 2) + (lf >> 2) + (((i >> 1) & 1) << 3);
-          float v = scn * (add_new ? kvn[D + d] : 0.f);
+          if (add_new) {
+            // The new pair: score mx[h], value v_new.
+            const float Mx = fmaxf(M, mx[h]);
+            const float s0 = exp2f(M - Mx), sn = exp2f(mx[h] - Mx);
+            L = s0 * L + sn;
 #pragma unroll
-          for (int w = 0; w < 2 * NCW; ++w)
-            if (w < nsl) v += sc[w] * slot(w)[16 + 32 * i + lf];
-          if (h < R) {
-            if (whole || receive)
-              p.out[row_offset(p, u, h) + d] = L > 0.f ? v / L : 0.f;
-            else
-              part[2 * R + h * D + d] = v;
+            for (int k = 0; k < NE; ++k) v[k] = s0 * v[k] + sn * kvn[D + dd[k]];
+            M = Mx;
+          }
+          if (got && h < R) {
+            if (whole || receive) {
+              const float inv = L > 0.f ? 1.f / L : 0.f;
+              float* out = p.out + row_offset(p, u, h);
+#pragma unroll
+              for (int k = 0; k < NE; ++k) out[dd[k]] = v[k] * inv;
+            } else {
+              float* part = p.partials + (size_t)(2 * b + (x == rb ? 0 : 1)) * p.slot_floats;
+              if (lf < 4 && i0 < 2) { part[h] = M; part[R + h] = L; }
+#pragma unroll
+              for (int k = 0; k < NE; ++k) part[2 * R + h * D + dd[k]] = v[k];
+            }
           }
         }
       }
@@ -1008,7 +1055,7 @@ static cudaError_t launch_mma_k(const AttendParams& p0, const CUtensorMap& tk,
   // Programmatic dependent launch: the prologue overlaps the previous kernel.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(MMA_THREADS);
+  cfg.blockDim = dim3(mma_threads<FUSED>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];

@@ -26,14 +26,12 @@ struct PipeCfg {
 };
 
 // Which table rows a block's stage carries (r0 = re-based position of the
-// block's first slot, fill = the stream's fill):
-//   QUERY_BASES: row |fill-1-r0| (the query's offset from the block; the
-//     consumer flips the sine when negative) and, when the block holds the
-//     ring's end, row fill-1-r0+W;
-//   KEY_BASES: row r0 and, when the block holds the ring's end, row W-r0 (the
-//     consumer flips its sine to get R(r0-W));
+// block's first slot):
+//   KEY_BASES: row r0 and, when the block holds the ring's end, row
+//     |r0 - W_ring| (the consumer flips its sine when r0 < W_ring, to get
+//     R(r0 - W_ring));
 //   NO_ROWS: none (the consumers derive the rows themselves).
-enum TableRows { QUERY_BASES = 0, KEY_BASES = 1, NO_ROWS = 2 };
+enum TableRows { KEY_BASES = 1, NO_ROWS = 2 };
 
 // 16-byte chunk `grp` of key row `row` (0..TK-1) of a block tile: the tile is
 // D/64 boxes of TK rows x 128 bytes, 128-byte swizzled.
@@ -61,6 +59,25 @@ __device__ __forceinline__ uint32_t fine_chunk(int d, int k) {
 template <int D>
 __device__ __forceinline__ uint32_t fine_chunk_keys(int d, int k) {
   return static_cast<uint32_t>((k ^ (d & 7)) << 4);
+}
+
+// The rotation warps of the tcgen05 chunk kernel read the same table with
+// eight lanes on eight consecutive keys d and one chunk j of pairs (2j, 2j+1)
+// as (cos, sin, cos, sin): chunk j of row d sits at position j ^ (d mod 8) of
+// its row, so those eight reads hit eight different 16-byte bank groups.
+__device__ __forceinline__ uint32_t fine_chunk_rot(int d, int j) {
+  return static_cast<uint32_t>((j ^ (d & 7)) << 4);
+}
+// Threads t0, t0+nt, ... fill that table from rows 0..TK-1 of the global one.
+template <int D>
+__device__ __forceinline__ void load_fine_rot(const AttendParams& p, uint8_t* fine, int t0,
+                                              int nt) {
+  constexpr int HALF = D / 2;
+  for (int idx = t0; idx < TK * HALF / 2; idx += nt) {
+    const int d = idx / (HALF / 2), j = idx % (HALF / 2);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p.table + (size_t)d * HALF) + j);
+    *reinterpret_cast<float4*>(fine + d * HALF * 8 + fine_chunk_rot(d, j)) = v;
+  }
 }
 
 // Threads t0, t0+nt, ... fill the fine table from rows 0..TK-1 of the global
@@ -101,16 +118,14 @@ __device__ __forceinline__ void prefetch_states(const AttendParams& p) {
 // The producer loop, run by lane 0 of warp 0 over blocks [rb, re).  Returns
 // the number of stages it filled.  Stops early (status set, *abort raised) if
 // a wait runs out.
-// rq_off: the query sits at fill - 1 + rq_off (1 in a fused step, where the
-// cached fill counts the window's pairs other than the new one).
 template <int D, bool ROTK, int ROWS>
 __device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap* tmK,
                                        const CUtensorMap* tmV, uint8_t* stages, uint64_t* full,
                                        uint64_t* empty, uint64_t* mdone, const int* pre,
                                        const int* sa, const int* sfill, int rb, int re,
-                                       volatile int* abort_flag, int rq_off = 0) {
+                                       volatile int* abort_flag) {
   using C = PipeCfg<D, ROTK>;
-  const int W = p.sh.W, NB = p.sh.NB, NS = p.ns;
+  const int NS = p.ns;
   int stage = 0, round = 0, issued = 0, seg = 0;
   bool stop = false;
   const uint64_t pol = l2_evict_first_policy();   // every K/V row is read once
@@ -125,10 +140,22 @@ __device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap*
     }
     const int x1 = min(u.uend, re);
     const int ug = static_cast<int>(unit_index(p, u));
-    int blk = touched_block(u.a, x - u.ustart, NB);
-    int r0 = blk * TK - u.a;
-    if (r0 < 0) r0 += W;
-    for (; x < x1; ++x) {
+    // Block geometry stepped in scalars (the producer is one thread that must
+    // keep the ring full): j = block within the unit, the pinned prefix's npb
+    // blocks first (slot block j, positions from 0), then the ring blocks
+    // (slot block NP + br, first slot at position npin + r0r).
+    const int Wg = p.sh.Wring, NBr = p.sh.NBr;
+    const int npb = (u.npin + TK - 1) / TK;
+    int j = x - u.ustart;
+    int br = u.a / TK, r0r = 0;
+    if (j >= npb) br = touched_block(u.a, j - npb, NBr);
+    r0r = br * TK - u.a;
+    if (r0r < 0) r0r += Wg;
+    for (; x < x1; ++x, ++j) {
+      const bool ring = j >= npb;
+      const int blk = ring ? p.sh.NP + br : j;
+      const int r0 = ring ? u.npin + r0r : j * TK;
+      const int wrap_at = ring ? Wg - r0r : TK;
       if (*abort_flag) { stop = true; break; }
       if (round > 0 &&
           !mbar_wait_or_abort(smem_u32(empty + stage), (round - 1) & 1, abort_flag)) {
@@ -139,7 +166,7 @@ __device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap*
       }
       const uint32_t bar = smem_u32(full + stage);
       const uint32_t dst = smem_u32(stages + (size_t)stage * C::STAGE);
-      const bool wraps = W - r0 < TK;
+      const bool wraps = wrap_at < TK;
       uint32_t bytes = 2 * C::TILE;
       if constexpr (ROTK && ROWS != NO_ROWS) bytes += wraps ? 2 * C::TROW : C::TROW;
       mbar_arrive_expect_tx(bar, bytes);
@@ -147,24 +174,18 @@ __device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap*
       tma_load_4d_hint(dst, tmK, 0, blk * TK, 0, ug, bar, pol);
       tma_load_4d_hint(dst + C::TILE, tmV, 0, blk * TK, 0, ug, bar, pol);
       if constexpr (ROTK && ROWS != NO_ROWS) {
-        int rowA, rowB;
-        if constexpr (ROWS == QUERY_BASES) {
-          const int mA = u.fill - 1 + rq_off - r0;
-          rowA = mA < 0 ? -mA : mA;
-          rowB = mA + W;
-        } else {
-          rowA = r0;
-          rowB = W - r0;
-        }
+        const int rowA = r0, rowB = r0 >= Wg ? r0 - Wg : Wg - r0;
         bulk_load(dst + 2 * C::TILE, p.table + (size_t)rowA * C::HALF, C::TROW, bar);
         if (wraps)
           bulk_load(dst + 2 * C::TILE + C::TROW, p.table + (size_t)rowB * C::HALF, C::TROW, bar);
       }
       ++issued;
       if (++stage == NS) { stage = 0; ++round; }
-      if (++blk == NB) blk = 0;
-      r0 += TK;
-      if (r0 >= W) r0 -= W;
+      if (ring) {
+        if (++br == NBr) br = 0;
+        r0r += TK;
+        if (r0r >= Wg) r0r -= Wg;
+      }
     }
   }
   return issued;

@@ -54,7 +54,7 @@ extern "C" rkv_status rkv_attend_static_scratch(rkv_handle* h, const void* q, fl
     return RKV_ERR_INVALID_ARG;
   if (layer_begin < 0 || n_layers < 1 || layer_begin + n_layers > h->sh.L)
     return RKV_ERR_INVALID_ARG;
-  if (n_q > h->sh.W) return RKV_ERR_CAPACITY;
+  if (n_q > h->sh.Wr) return RKV_ERR_CAPACITY;
   if (n_q < 1 || n_q > h->cfg.max_chunk) return RKV_ERR_INVALID_ARG;
 
   // Sizes first: a call that needs more scratch than the array holds is

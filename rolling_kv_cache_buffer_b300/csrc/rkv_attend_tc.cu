@@ -1,0 +1,781 @@
+// rkv_attend_tc.cu -- chunk attention on the fifth-generation tensor cores
+// (tcgen05, accumulators in tensor memory) for steps that insert c >= 2 tokens
+// per stream: bf16 caches, R = c*G <= 128 query rows per (stream, layer, KV
+// head) unit, D 64 or 128.
+//
+// What it computes is the attention over the window with exact re-basing of
+// "Audio8 ASR Infinite: What It Actually Takes to Listen Forever" ("Inside the
+// Rolling KV Cache and Exact RoPE Re-Basing"), causal among the chunk: query j
+// sits at r_j = npin + fill - c + j and sees the keys at positions r <= r_j,
+//   out_j = sum_{r <= r_j} softmax(<R(r_j) q_j, R(r) k_r> * scale) v_r.
+//
+// Per unit the rows (query j, head) form one M = 128 tile (rows >= R are
+// zero), so S = Q K^T and O = P V are dense contractions issued as tcgen05.mma
+// (kind::f16, bf16 operands, f32 accumulation in tensor memory):
+//  * Q: [128 rows x D] bf16 in shared memory, K-major, 128-byte swizzle,
+//    rotated once per unit by R(r_j) (plus the lag of stored-rotated keys
+//    that follow a re-basing epoch);
+//  * a key block (TK = 32 slots, one TMA box per tile, 128-byte swizzle) is
+//    the B operand of S = Q K^T as it lands (stored-rotated keys) or after
+//    the staging warps have turned each key in place to its position, R(r0+d)
+//    = R(r0) R(d) composed in f32 (pre-RoPE keys), rounded to bf16;
+//  * S (128 lanes x 32 columns f32, two buffers) is read by the softmax warps,
+//    one row per thread: causal and window masks, running maximum with a lazy
+//    rescale (O and l are rescaled only when the maximum grows by more than
+//    2^8, which keeps every exponent below 2^8 and every partial sum exact
+//    to f32 rounding), P = 2^(s - m) rounded to bf16 and written back to
+//    tensor memory (two bf16 per column);
+//  * O += P V takes P from tensor memory and the V tile from shared memory as
+//    an MN-major operand (dims contiguous per key).
+// The unit's split partials (m, l, O rows) merge across CTAs through global
+// memory: the last CTA to take the unit's ticket combines them.
+//
+// Roles (one persistent CTA per SM, 10 warps): warp 0 the TMA producer (the
+// stage ring of rkv_attend_pipe.cuh), warps 1-4 the softmax warps (warp w owns
+// tensor-memory lanes 32 (w mod 4) .. +31), warp 5 the MMA issuer (one lane;
+// the warp allocates and frees the tensor memory), warps 6-9 the staging
+// warps (they zero the V rows of slots outside the window and, for pre-RoPE
+// keys, rotate the K tile).  Every wait is bounded and falls back to the
+// stream's status word.
+#include "rkv_attend_pipe.cuh"
+
+namespace rkv {
+
+namespace {
+
+constexpr int TC_SMW = 4;                       // softmax warps
+constexpr int TC_RW = 4;                        // staging (rotation) warps
+constexpr int W_SM0 = 1, W_MMA = 1 + TC_SMW, W_ROT0 = W_MMA + 1;
+constexpr int TC_THREADS = (W_ROT0 + TC_RW) * 32;
+constexpr int TC_MAX_STAGES = 12;
+constexpr int TC_ROWS = 128;                    // M of every product
+constexpr int TBAR_PREFIX = 2;                  // named barrier: block prefix ready
+constexpr int TBAR_SM = 3;                      // named barrier of the softmax warps
+constexpr float TC_TAU = 8.f;                   // lazy rescale threshold (log2 units)
+// Tensor memory columns: S[2] (f32), P[2] (bf16 pairs), O (f32, D columns).
+constexpr int TM_S = 0, TM_P = 64, TM_O = 128, TM_COLS = 256;
+
+template <int D, bool ROTK>
+struct TcCfg : PipeCfg<D, ROTK> {
+  static constexpr int QT = TC_ROWS * D * 2;    // Q tile bytes (D/64 boxes of 16 KB)
+};
+
+__host__ __device__ constexpr size_t tc_smem_bytes(int stage, int fine, int qt, int ns, int S) {
+  // stages, Q tile, R(d) table, 3 barriers per stage, 9 more barriers, the
+  // tensor memory address (16 B), flags (16 B), the per-stream cache.
+  return 1024 + (size_t)ns * stage + (size_t)qt + (size_t)fine + (size_t)ns * 24 + 9 * 8 + 16 +
+         16 + (size_t)(4 * S + 1) * 4;
+}
+
+// ---- tcgen05 wrappers ------------------------------------------------------
+// Shared-memory matrix descriptor: start address, leading / stride byte
+// offsets, the sm_100 descriptor version (bit 46) and 128-byte swizzling.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B, A
+// K-major, B K-major (tb = 0) or MN-major (tb = 1), M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int tb) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)tb << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                          int acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+               ::"r"(d), "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id,
+                                          int acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+               ::"r"(d), "r"(a), "l"(b), "r"(id), "r"(acc));
+}
+// The mbarrier completes once every tcgen05 operation this thread issued
+// before it has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 32 columns of this warp's 32 lanes: thread t gets lane (base + t).
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// Byte offset of element (row, col) of a K-major, 128-byte-swizzled tile of
+// `rows` x 64 bf16 per box (col < 64 within the box).
+__device__ __forceinline__ uint32_t swz128(int row, int col) {
+  return static_cast<uint32_t>(row * 128 + ((((col * 2) >> 4) ^ (row & 7)) << 4) +
+                               ((col * 2) & 15));
+}
+
+// Packed f32 pairs (the sm_100+ f32x2 pipe).
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 f2_make(float a, float b) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(f2 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+  f2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// Two rotary pairs (x0, y0), (x1, y1) -- X = (x0, x1), Y = (y0, y1) -- turned
+// by R(base + d): the base's (cos, sin) of both pairs b = (c0, s0, c1, s1)
+// composed with R(d)'s f (angle addition), then x' = x c - y s, y' = y c + x s.
+__device__ __forceinline__ void rot2_composed(f2& X, f2& Y, float4 b, float4 f) {
+  const f2 Bc = f2_make(b.x, b.z), Bs = f2_make(b.y, b.w);
+  const f2 Fc = f2_make(f.x, f.z), Fs = f2_make(f.y, f.w);
+  const f2 NBs = f2_make(-b.y, -b.w);
+  const f2 Cc = f2_fma(NBs, Fs, f2_mul(Bc, Fc));
+  const f2 Ss = f2_fma(Bc, Fs, f2_mul(Bs, Fc));
+  float s0, s1;
+  f2_split(Ss, s0, s1);
+  const f2 NSs = f2_make(-s0, -s1);
+  const f2 Xr = f2_fma(Y, NSs, f2_mul(X, Cc));
+  const f2 Yr = f2_fma(X, Ss, f2_mul(Y, Cc));
+  X = Xr;
+  Y = Yr;
+}
+
+// Staging warps: for every block of the CTA's share, in order, wait for its
+// tiles, zero the V rows of slots outside the window (they may hold anything,
+// and 0 * NaN would reach the output through P V), turn each key of the K
+// tile in place to its position (pre-RoPE keys) -- slot d of the block at
+// r0 + d, or r0 + d - W_ring past the ring's end -- and hand the stage on.  R(r0 + d) is the block's base row
+// R(r0) (or R(r0 - W_ring): the stage's second row |r0 - W_ring|, its sine
+// negated when r0 < W_ring) composed with R(d) from the resident table.  Item
+// `it` of a block is key d = it mod TK and group g = it / TK of eight rotary
+// pairs: eight consecutive lanes take eight keys of one group, so their
+// 16-byte reads of the swizzled tile and of the table fall in eight
+// different bank groups and the base row is a broadcast.
+template <int D, int STYLE, bool ROTK>
+__device__ __forceinline__ void stage_tiles(const AttendParams& p, uint8_t* stages,
+                                             const uint8_t* fine, uint64_t* full, uint64_t* rotd,
+                                             const int* pre, const int* sa, const int* sfill,
+                                             int rb, int re, volatile int* abort_flag, int rt) {
+  using C = PipeCfg<D, ROTK>;
+  constexpr int HALF = D / 2, NG = D / 16, ITEMS = TK * NG;
+  constexpr int RT = TC_RW * 32;
+  constexpr int VCH = D / 8;   // 16-byte chunks of a V row
+  const int NS = p.ns, Wg = p.sh.Wring;
+  const int lane = rt & 31;
+  int stage = 0, round = 0;
+  for (int x = rb; x < re;) {
+    const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
+    const int x1 = min(u.uend, re);
+    BlockWalk wk;
+    wk.init(x, u, p.sh);
+    for (bool first = true; x < x1; ++x, first = false) {
+      if (!first) wk.advance(1, u, p.sh);
+      // Every block passes through here in order, so the full barrier of a
+      // stage is never more than one phase ahead of this wait.
+      const bool bad = !mbar_wait_or_abort(smem_u32(full + stage), round & 1, abort_flag);
+      if (__any_sync(0xffffffffu, bad)) {
+        if (lane == 0 && !*abort_flag) {
+          *abort_flag = 1;
+          p.st[u.s].status = STATUS_DEVICE_STATE;
+        }
+        return;
+      }
+      uint8_t* kt = stages + (size_t)stage * C::STAGE;
+      const int wrap_at = wk.g.wrap_at;
+      // Slots outside the window may hold anything (NaN included): their V
+      // rows are zeroed, since the product P V would turn 0 * NaN into NaN.
+      // (Their K rows only reach masked scores.)
+      const bool allvalid = wrap_at < TK ? (u.fill == Wg) : (wk.g.r0 + TK <= wk.g.lim);
+      if (!allvalid) {
+        for (int it = rt; it < TK * VCH; it += RT) {
+          const int d = it % TK, ch = it / TK;
+          if (slot_pos(wk.g, d, Wg) >= wk.g.lim)
+            *reinterpret_cast<uint4*>(kt + C::TILE + tile_swz(d, ch)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if constexpr (ROTK) {
+      const float4* base = reinterpret_cast<const float4*>(kt + 2 * C::TILE);   // R(r0)
+      const float4* basew = base + HALF / 2;                                  // |r0 - W_ring|
+      const bool neg = wk.g.r0 < Wg;
+#pragma unroll
+      for (int k0 = 0; k0 < (ITEMS + RT - 1) / RT; ++k0) {
+        const int it = rt + k0 * RT;
+        if (it >= ITEMS) break;
+        const int d = it & (TK - 1), g = it / TK;
+        const bool wr = d >= wrap_at;
+        const float4* bp = (wr ? basew : base) + 4 * g;
+        const uint8_t* frow = fine + d * HALF * 8;
+        const uint32_t offA = STYLE == 0 ? tile_swz(d, g) : tile_swz(d, 2 * g);
+        const uint32_t offB = STYLE == 0 ? tile_swz(d, HALF / 8 + g) : tile_swz(d, 2 * g + 1);
+        const uint4 A = *reinterpret_cast<const uint4*>(kt + offA);
+        const uint4 B = *reinterpret_cast<const uint4*>(kt + offB);
+        uint32_t w[8] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {   // pairs 8g + 2k and 8g + 2k + 1
+          float4 bb = bp[k];
+          if (wr && neg) { bb.y = -bb.y; bb.w = -bb.w; }
+          const float4 ff =
+              *reinterpret_cast<const float4*>(frow + fine_chunk_rot(d, 4 * g + k));
+          // Split-half: x of the two pairs in word k of A, y in word k of B.
+          // Interleaved: pair 8g + 2k + e is word 2k + e of A|B as (x, y).
+          uint32_t& u0 = STYLE == 0 ? w[k] : w[2 * k];
+          uint32_t& u1 = STYLE == 0 ? w[4 + k] : w[2 * k + 1];
+          f2 X = STYLE == 0 ? f2_make(bf_lo(u0), bf_hi(u0)) : f2_make(bf_lo(u0), bf_lo(u1));
+          f2 Y = STYLE == 0 ? f2_make(bf_lo(u1), bf_hi(u1)) : f2_make(bf_hi(u0), bf_hi(u1));
+          rot2_composed(X, Y, bb, ff);
+          float x0, x1v, y0, y1;
+          f2_split(X, x0, x1v);
+          f2_split(Y, y0, y1);
+          if (STYLE == 0) {
+            u0 = pack_bf2(x0, x1v);
+            u1 = pack_bf2(y0, y1);
+          } else {
+            u0 = pack_bf2(x0, y0);
+            u1 = pack_bf2(x1v, y1);
+          }
+        }
+        *reinterpret_cast<uint4*>(kt + offA) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(kt + offB) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      }
+      // The tensor cores read the tile through the async proxy.
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(rotd + stage));
+      if (++stage == NS) { stage = 0; ++round; }
+    }
+  }
+}
+
+}  // namespace
+
+template <int D, bool ROTK, int STYLE>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    attend_tc_chunk(const __grid_constant__ AttendParams p,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV) {
+  using C = TcCfg<D, ROTK>;
+  constexpr int HALF = D / 2, NKS = D / 16;   // k-steps of the QK product
+  const int G = p.sh.G, NS = p.ns, R = p.R, c = p.c;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  uint8_t* stages = smem;                                        // [NS][STAGE]
+  uint8_t* qt = stages + (size_t)NS * C::STAGE;                  // Q tile, 1024-aligned
+  uint8_t* fine = qt + C::QT;                                    // R(d) table (pre-RoPE)
+  uint64_t* full = reinterpret_cast<uint64_t*>(fine + C::FINE);  // [NS]
+  uint64_t* empty = full + NS;                                   // [NS] stage consumed
+  uint64_t* rotd = empty + NS;                                   // [NS] keys rotated
+  uint64_t* sfull = rotd + NS;                                   // [2] S buffer written
+  uint64_t* sfree = sfull + 2;                                   // [2] S buffer read
+  uint64_t* pready = sfree + 2;                                  // [2] P buffer written
+  uint64_t* qready = pready + 2;                                 // Q tile of the segment
+  uint64_t* ofin = qready + 1;                                   // every product of a segment
+  uint64_t* mdone = ofin + 1;                                    // a segment's products issued
+  uint32_t* tm_base = reinterpret_cast<uint32_t*>(mdone + 1);    // tensor memory address
+  int* flag = reinterpret_cast<int*>(tm_base + 4);               // ticket, abort, issued
+  int* pre = flag + 4;                                           // [S+1] block prefix
+  int* sa = pre + p.sh.S + 1;                                    // [S] ring start | npin
+  int* sfill = sa + p.sh.S;                                      // [S] fill
+  int* slag = sfill + p.sh.S;                                    // [S] lag (epoch)
+  volatile int* abort_flag = flag + 1;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(full + i), 1);
+      mbar_init(smem_u32(empty + i), 1);      // the MMA issuer's commit
+      mbar_init(smem_u32(rotd + i), TC_RW);   // every rotation warp
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(sfull + i), 1);
+      mbar_init(smem_u32(sfree + i), TC_SMW);
+      mbar_init(smem_u32(pready + i), TC_SMW);
+    }
+    mbar_init(smem_u32(qready), TC_SMW);
+    mbar_init(smem_u32(ofin), 1);
+    mbar_init(smem_u32(mdone), 1);
+    fence_mbar_init();
+    flag[1] = 0;
+    flag[2] = 0;
+  }
+  if (warp == W_MMA) {
+    // The MMA warp owns the tensor memory: TM_COLS columns for the CTA.
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(tm_base)), "r"(TM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if constexpr (ROTK) {
+    if (warp >= W_ROT0) load_fine_rot<D>(p, fine, tid - 32 * W_ROT0, TC_RW * 32);
+  }
+  prefetch_queries(p, D);
+  prefetch_states(p);
+  pdl_wait();      // from here on: stream state, pools, queries, outputs
+  pdl_trigger();   // a kernel launched next may start its own prologue
+  tc_fence_before();
+  if (warp == 0) {
+    build_prefix_cached(p, pre, sa, sfill, lane, slag);
+    __syncwarp();
+    named_bar_arrive(TBAR_PREFIX, TC_THREADS);
+  } else {
+    named_bar_sync(TBAR_PREFIX, TC_THREADS);
+  }
+  tc_fence_after();
+  const uint32_t tmem = *tm_base;
+  const int T = pre[p.sh.S];
+  const int P = min(static_cast<int>(gridDim.x), T);
+  const int b = static_cast<int>(blockIdx.x);
+  const int rb = b < P ? range_start(b, T, P) : 0, re = b < P ? range_start(b + 1, T, P) : 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0)
+      flag[2] = produce<D, ROTK, ROTK ? KEY_BASES : NO_ROWS>(
+          p, &tmK, &tmV, stages, full, empty, mdone, pre, sa, sfill, rb, re, abort_flag);
+    __syncwarp();
+  } else if (warp >= W_ROT0) {
+    // ------------------------------------------------------------- staging warps
+    stage_tiles<D, STYLE, ROTK>(p, stages, fine, full, rotd, pre, sa, sfill, rb, re, abort_flag,
+                                tid - 32 * W_ROT0);
+  } else if (warp == W_MMA) {
+    // --------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_bf16(TC_ROWS, TK, 0);
+      const uint32_t id_pv = idesc_bf16(TC_ROWS, D, 1);
+      const uint32_t q_s = smem_u32(qt);
+      uint64_t* ready = rotd;   // tiles staged (keys rotated, outside V rows zeroed)
+      int jj = 0, seg = 0;
+      bool dead = false;
+      for (int x = rb; x < re && !dead; ++seg) {
+        const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
+        const int x1 = min(u.uend, re);
+        if (!mbar_wait_or_abort(smem_u32(qready), seg & 1, abort_flag)) { dead = true; break; }
+        tc_fence_after();
+        const int j0 = jj;
+        for (; x < x1; ++x, ++jj) {
+          const int s = jj % NS, r = jj / NS, bsl = jj & 1;
+          if (!mbar_wait_or_abort(smem_u32(ready + s), r & 1, abort_flag)) { dead = true; break; }
+          if (jj >= 2 && !mbar_wait_or_abort(smem_u32(sfree + bsl), ((jj >> 1) - 1) & 1,
+                                             abort_flag)) { dead = true; break; }
+          tc_fence_after();
+          // S[bsl] = Q K^T over D in k-steps of 16 (32 bytes of a 128-byte row).
+          const uint32_t k_s = smem_u32(stages + (size_t)s * C::STAGE);
+#pragma unroll
+          for (int ks = 0; ks < NKS; ++ks) {
+            const uint64_t a = sdesc(q_s + (ks >> 2) * (TC_ROWS * 128) + (ks & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc(k_s + (ks >> 2) * (TK * 128) + (ks & 3) * 32, 16, 1024);
+            tc_mma_ss(tmem + TM_S + bsl * TK, a, bd, id_qk, ks > 0);
+          }
+          tc_commit(smem_u32(sfull + bsl));
+          if (jj > j0) {
+            // O += P V for the previous block, once its P is in tensor memory.
+            const int jp = jj - 1, sp = jp % NS, bp = jp & 1;
+            if (!mbar_wait_or_abort(smem_u32(pready + bp), (jp >> 1) & 1, abort_flag)) {
+              dead = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t v_s = smem_u32(stages + (size_t)sp * C::STAGE + C::TILE);
+#pragma unroll
+            for (int ks = 0; ks < TK / 16; ++ks) {
+              const uint64_t bd = sdesc(v_s + ks * 16 * 128, TK * 128, 1024);
+              tc_mma_ts(tmem + TM_O, tmem + TM_P + bp * (TK / 2) + ks * 8, bd, id_pv,
+                        (jp > j0 || ks > 0) ? 1 : 0);
+            }
+            tc_commit(smem_u32(empty + sp));
+          }
+        }
+        if (dead) break;
+        if (jj > j0) {
+          const int jp = jj - 1, sp = jp % NS, bp = jp & 1;
+          if (!mbar_wait_or_abort(smem_u32(pready + bp), (jp >> 1) & 1, abort_flag)) {
+            dead = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t v_s = smem_u32(stages + (size_t)sp * C::STAGE + C::TILE);
+#pragma unroll
+          for (int ks = 0; ks < TK / 16; ++ks) {
+            const uint64_t bd = sdesc(v_s + ks * 16 * 128, TK * 128, 1024);
+            tc_mma_ts(tmem + TM_O, tmem + TM_P + bp * (TK / 2) + ks * 8, bd, id_pv,
+                      (jp > j0 || ks > 0) ? 1 : 0);
+          }
+          tc_commit(smem_u32(empty + sp));
+        }
+        tc_commit(smem_u32(ofin));
+        // The producer may go on with the next segment (its epilogue leaves
+        // the stages alone).
+        mbar_arrive(smem_u32(mdone));
+      }
+      if (dead) {
+        if (!*abort_flag) {
+          *abort_flag = 1;
+          if (rb < re) p.st[unit_of_cached(rb, p, pre, sa, sfill).s].status = STATUS_DEVICE_STATE;
+        }
+        // Nothing leaves while products are in flight: one last commit, waited on.
+        tc_commit(smem_u32(ofin));
+      }
+      flag[3] = seg;
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    // Control flow is the same in all four warps (every decision below is
+    // warp-uniform and the segment structure is shared), so the named
+    // barriers of a split unit's merge are always reached by all of them,
+    // also after a wait ran out (then the work is skipped, the barriers not).
+    const int q4 = warp & 3;                  // tensor-memory lane quarter
+    const int row = 32 * q4 + lane;           // this thread's row of every tile
+    const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
+    const int st = tid - 32 * W_SM0;          // 0..127
+    const bool warp_rows = 32 * q4 < R;       // the warp holds real rows
+    zero_empty_units_cached(p, sa, sfill, st, TC_SMW * 32);
+    int jj = 0, seg = 0;
+    bool dead = false;
+    auto waited = [&](uint64_t* bar, int parity) {   // false (and dead) if it ran out
+      if (dead) return false;
+      if (__any_sync(0xffffffffu, !mbar_wait_or_abort(smem_u32(bar), parity, abort_flag))) {
+        dead = true;
+        if (lane == 0) *abort_flag = 1;   // the other roles stop waiting
+      }
+      return !dead;
+    };
+    for (int x = rb; x < re; ++seg) {
+      const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
+      const int x1 = min(u.uend, re);
+      const bool whole = (x == u.ustart) && (x1 == u.uend);
+      // A split unit's partial goes to slot 0 (the CTA's first segment) or 1.
+      const int kslot = x == rb ? 0 : 1;
+      const int qbase = u.npin + u.fill - c;  // position of the chunk's first query
+      const int rq = row < R ? qbase + row / G : -1;
+      // ---- this segment's Q tile: row = (query j, head), rotated to r_j ----
+      // (plus the lag of stored-rotated keys that follow a re-basing epoch);
+      // rows >= R are zero.  Eight rotary pairs per pass: split-half pairs
+      // (i, i + D/2) from two 16-byte chunks, interleaved ones from one.
+      {
+        const size_t qo = row < R ? row_offset(p, u, row) : 0;
+        const float2* t = p.table + (size_t)(row < R ? rq + slag[u.s] : 0) * HALF;
+        auto load8 = [&](int d0, float (&v)[8]) {
+          if (row >= R) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+          } else if (p.sh.q_bf16) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(
+                static_cast<const uint16_t*>(p.q) + qo + d0));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { v[2 * i] = bf_lo(ww[i]); v[2 * i + 1] = bf_hi(ww[i]); }
+          } else {
+            const float4* f = reinterpret_cast<const float4*>(
+                static_cast<const float*>(p.q) + qo + d0);
+            const float4 a = __ldg(f), bq = __ldg(f + 1);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = bq.x; v[5] = bq.y; v[6] = bq.z; v[7] = bq.w;
+          }
+        };
+        auto store8 = [&](int d0, const float (&v)[8]) {
+          const uint4 w = make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]),
+                                     pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
+          *reinterpret_cast<uint4*>(qt + (d0 >> 6) * (TC_ROWS * 128) + swz128(row, d0 & 63)) = w;
+        };
+        if constexpr (STYLE == 0) {
+#pragma unroll 1
+          for (int i0 = 0; i0 < HALF; i0 += 8) {
+            float xa[8], xb[8];
+            load8(i0, xa);
+            load8(i0 + HALF, xb);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float2 cs = row < R ? __ldg(t + i0 + i) : make_float2(1.f, 0.f);
+              const float a = xa[i], bq = xb[i];
+              xa[i] = a * cs.x - bq * cs.y;
+              xb[i] = bq * cs.x + a * cs.y;
+            }
+            store8(i0, xa);
+            store8(i0 + HALF, xb);
+          }
+        } else {
+#pragma unroll 1
+          for (int d0 = 0; d0 < D; d0 += 8) {
+            float xv[8];
+            load8(d0, xv);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 cs = row < R ? __ldg(t + d0 / 2 + i) : make_float2(1.f, 0.f);
+              const float a = xv[2 * i], bq = xv[2 * i + 1];
+              xv[2 * i] = a * cs.x - bq * cs.y;
+              xv[2 * i + 1] = bq * cs.x + a * cs.y;
+            }
+            store8(d0, xv);
+          }
+        }
+      }
+      // The tensor cores read the Q tile through the async proxy.
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(qready));
+
+      float m = NEG_BIG, l = 0.f;
+      const int j0 = jj;
+      BlockWalk wk;
+      wk.init(x, u, p.sh);
+      const int Wg = p.sh.Wring;
+      for (bool first = true; x < x1; ++x, ++jj, first = false) {
+        if (!first) wk.advance(1, u, p.sh);
+        const BlockGeo& bg = wk.g;
+        const int bsl = jj & 1;
+        if (!waited(sfull + bsl, (jj >> 1) & 1)) continue;
+        tc_fence_after();
+        uint32_t sr[32];
+        if (warp_rows) tc_ld32(tmem + lane_addr + TM_S + bsl * TK, sr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(sfree + bsl));
+        // Scores in log2 units; masked: outside the window or after the row.
+        float sv[32];
+        float bm = NEG_BIG;
+#pragma unroll
+        for (int d = 0; d < 32; ++d) {
+          const int r = slot_pos(bg, d, Wg);
+          const bool vis = row < R && r < bg.lim && r <= rq;
+          sv[d] = vis ? __uint_as_float(sr[d]) * p.scale_log2 : NEG_BIG;
+          bm = fmaxf(bm, sv[d]);
+        }
+        // Lazy rescale: the running maximum moves only when a score exceeds
+        // it by more than TC_TAU; O and l are then rescaled.  O is quiet once
+        // the previous block's product has completed (its stage's commit).
+        const bool grow = bm > m + TC_TAU;
+        const float mnew = grow ? bm : m;
+        if (__any_sync(0xffffffffu, grow && jj > j0)) {
+          const int jp = jj - 1;
+          if (!waited(empty + jp % NS, (jp / NS) & 1)) continue;
+          tc_fence_after();
+          const float sc = exp2f(m - mnew);
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t ov[16];
+            tc_ld16(tmem + lane_addr + TM_O + c0, ov);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * sc);
+            tc_st16(tmem + lane_addr + TM_O + c0, ov);
+          }
+        }
+        if (grow) l *= exp2f(m - mnew);
+        m = mnew;
+        uint32_t pw[16];
+        float psum = 0.f;
+#pragma unroll
+        for (int d = 0; d < 32; d += 2) {
+          const float p0 = sv[d] > 0.5f * NEG_BIG ? exp2f(sv[d] - m) : 0.f;
+          const float p1 = sv[d + 1] > 0.5f * NEG_BIG ? exp2f(sv[d + 1] - m) : 0.f;
+          psum += p0 + p1;
+          pw[d >> 1] = pack_bf2(p0, p1);
+        }
+        l += psum;
+        // P[bsl] was last read by the product of block jj - 2: wait for it.
+        if (jj >= 2) {
+          const int jq = jj - 2;
+          if (!waited(empty + jq % NS, (jq / NS) & 1)) continue;
+          tc_fence_after();
+        }
+        if (warp_rows) tc_st16(tmem + lane_addr + TM_P + bsl * (TK / 2), pw);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(pready + bsl));
+      }
+      // ---- segment end: O row from tensor memory, then the unit's output ----
+      if (waited(ofin, seg & 1)) {
+        tc_fence_after();
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t ov[32];
+          if (warp_rows) tc_ld32(tmem + lane_addr + TM_O + c0, ov);
+          if (row < R) {
+            if (whole) {
+              const float inv = l > 0.f ? 1.f / l : 0.f;
+              float* o = p.out + row_offset(p, u, row) + c0;
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(o + i) =
+                    make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
+                                __uint_as_float(ov[i + 2]) * inv,
+                                __uint_as_float(ov[i + 3]) * inv);
+            } else {
+              // Split unit: this CTA's partial (m, l, unnormalised O) of the row.
+              float* pp = p.partials + (size_t)(2 * b + kslot) * p.slot_floats;
+              if (c0 == 0) { pp[row] = m; pp[R + row] = l; }
+#pragma unroll
+              for (int i = 0; i < 32; ++i) pp[2 * R + row * D + c0 + i] = __uint_as_float(ov[i]);
+            }
+          }
+        }
+        tc_fence_before();
+      }
+      if (!whole) {
+        // The last CTA of the unit to take its ticket merges the partials.
+        named_bar_sync(TBAR_SM, TC_SMW * 32);
+        if (st == 0) {
+          __threadfence();
+          flag[0] = atomicAdd(&p.unit_tickets[unit_index(p, u)], 1);
+          __threadfence();
+        }
+        named_bar_sync(TBAR_SM, TC_SMW * 32);
+        const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
+        if (flag[0] == b1 - b0) {
+          const int rs0 = range_start(b0, T, P);
+          for (int idx = st; idx < R * D; idx += TC_SMW * 32) {
+            const int h = idx / D, d = idx % D;
+            float M = NEG_BIG;
+            for (int bb = b0; bb <= b1; ++bb) {
+              const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
+              M = fmaxf(M, __ldcg(p.partials + (size_t)(2 * bb + k) * p.slot_floats + h));
+            }
+            float num = 0.f, den = 0.f;
+            for (int bb = b0; bb <= b1; ++bb) {
+              const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
+              const float* pp = p.partials + (size_t)(2 * bb + k) * p.slot_floats;
+              const float sc = exp2f(__ldcg(pp + h) - M);
+              den += sc * __ldcg(pp + R + h);
+              num += sc * __ldcg(pp + 2 * R + h * D + d);
+            }
+            p.out[row_offset(p, u, h) + d] = den > 0.f ? num / den : 0.f;
+          }
+          if (st == 0) p.unit_tickets[unit_index(p, u)] = 0;
+        }
+        named_bar_sync(TBAR_SM, TC_SMW * 32);
+      }
+      x = x1;
+    }
+    if (dead && lane == 0 && !*abort_flag) {
+      *abort_flag = 1;
+      if (rb < re) p.st[unit_of_cached(rb, p, pre, sa, sfill).s].status = STATUS_DEVICE_STATE;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == W_MMA) {
+    // After an abort: no product may be in flight when the memory is freed.
+    if (*abort_flag && lane == 0) mbar_wait(smem_u32(ofin), (flag[3]) & 1);
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                 ::"r"(tmem), "r"(TM_COLS));
+  }
+  if (tid == 0 && *abort_flag) {
+    const int issued = flag[2];
+    for (int j = max(0, issued - NS); j < issued; ++j)
+      mbar_wait(smem_u32(full + (j % NS)), (j / NS) & 1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Launch
+// ---------------------------------------------------------------------------
+template <int D, bool ROTK>
+static int tc_stages(int S) {
+  using C = TcCfg<D, ROTK>;
+  int ns = TC_MAX_STAGES;
+  while (ns > 2 && tc_smem_bytes(C::STAGE, C::FINE, C::QT, ns, S) > (size_t)SMEM_LIMIT) --ns;
+  return ns;
+}
+
+bool attend_tc_supported(const Shape& sh, int c) {
+  if (!(sh.bf16 && (sh.D == 64 || sh.D == 128) && c >= 2 && c * sh.G <= TC_ROWS)) return false;
+  const bool rotk = !sh.stored_rotated;
+  if (sh.D == 128)
+    return rotk ? tc_stages<128, true>(sh.S) >= 4 : tc_stages<128, false>(sh.S) >= 4;
+  return rotk ? tc_stages<64, true>(sh.S) >= 4 : tc_stages<64, false>(sh.S) >= 4;
+}
+
+template <int D, bool ROTK, int STYLE>
+static cudaError_t launch_tc_k(const AttendParams& p0, const CUtensorMap& tk,
+                               const CUtensorMap& tv, int grid, cudaStream_t s) {
+  using C = TcCfg<D, ROTK>;
+  AttendParams p = p0;
+  p.ns = tc_stages<D, ROTK>(p.sh.S);
+  const size_t smem = tc_smem_bytes(C::STAGE, C::FINE, C::QT, p.ns, p.sh.S);
+  if (smem > (size_t)SMEM_LIMIT) return cudaErrorNotSupported;
+  auto kern = attend_tc_chunk<D, ROTK, STYLE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, tk, tv);
+}
+
+template <int D>
+static cudaError_t launch_tc_d(const AttendParams& p, const CUtensorMap& tk,
+                               const CUtensorMap& tv, int grid, cudaStream_t s) {
+  const bool rotk = !p.sh.stored_rotated;
+  if (p.sh.style == 0)
+    return rotk ? launch_tc_k<D, true, 0>(p, tk, tv, grid, s)
+                : launch_tc_k<D, false, 0>(p, tk, tv, grid, s);
+  return rotk ? launch_tc_k<D, true, 1>(p, tk, tv, grid, s)
+              : launch_tc_k<D, false, 1>(p, tk, tv, grid, s);
+}
+
+cudaError_t launch_attend_tc(const AttendParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                             int grid, cudaStream_t s) {
+  if (!attend_tc_supported(p.sh, p.c)) return cudaErrorNotSupported;
+  if (p.sh.D == 128) return launch_tc_d<128>(p, tk, tv, grid, s);
+  return launch_tc_d<64>(p, tk, tv, grid, s);
+}
+
+}  // namespace rkv

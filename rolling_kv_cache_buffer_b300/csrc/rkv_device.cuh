@@ -15,15 +15,17 @@ namespace rkv {
 
 // One stream's device state (32 bytes).  origin = absolute position of the
 // oldest retained pair, fill = retained pairs; retained positions are
-// origin .. origin+fill-1 and position p sits in slot p mod W.
+// origin .. origin+fill-1 and position p sits in slot P + (p mod W_ring) (P
+// pinned slots in front of a ring of W_ring = W - P slots; P = 0 unless the
+// handle pins a prefix).  npin pinned prefix pairs sit in slots 0..npin-1.
 struct StreamState {
   long long origin;
   int fill;
   int status;     // 0, or an rkv_status code (sticky until rkv_set_stream_state)
   int pending;    // stored-rotated: evictions not yet re-based (the lag, with an epoch)
   int last_new;   // pairs inserted by the last append
-  int ring;       // origin mod W (slot of the oldest pair), kept by every state writer
-  int pad1;
+  int ring;       // origin mod W_ring (ring slot of the oldest pair), kept by every writer
+  int npin;       // pinned prefix pairs (0 without pinned slots)
 };
 static_assert(sizeof(StreamState) == 32, "state layout");
 
@@ -256,9 +258,11 @@ __device__ __forceinline__ int pair_d2(int i, int D, int style) {
   return style ? 2 * i + 1 : i + D / 2;
 }
 
-__device__ __forceinline__ int state_ok(const StreamState& s, int W) {
-  return s.status == 0 && s.origin >= 0 && s.fill >= 0 && s.fill <= W && s.ring >= 0 &&
-         s.ring < W;
+// A usable stream state: no status set, 0 <= fill <= Wr (the retained window),
+// 0 <= ring < Wring (the ring's slots) and 0 <= npin <= P (the pinned slots).
+__device__ __forceinline__ int state_ok(const StreamState& s, int Wring, int Wr, int P) {
+  return s.status == 0 && s.origin >= 0 && s.fill >= 0 && s.fill <= Wr && s.ring >= 0 &&
+         s.ring < Wring && s.npin >= 0 && s.npin <= P;
 }
 
 // ----------------------------------------------------------------------------
@@ -279,6 +283,15 @@ __host__ __device__ __forceinline__ int touched_blocks(int a, int n, int NB) {
 __host__ __device__ __forceinline__ int touched_block(int a, int j, int NB) {
   return (a / TK + j) % NB;
 }
+// Blocks of one (stream, layer, KV head) unit: the ceil(npin / TK) blocks of
+// the pinned prefix (slots 0..), then the ring blocks the window of n pairs
+// starting at ring slot a touches.
+__host__ __device__ __forceinline__ int unit_blocks(int a, int n, int npin, int NBr) {
+  return (npin + TK - 1) / TK + touched_blocks(a, n, NBr);
+}
+// The cached per-stream word of the attention kernels: ring start a and pinned
+// prefix pairs npin (both < 2^16), or -1 for a stream whose state is not usable.
+__host__ __device__ __forceinline__ int pack_an(int a, int npin) { return a | (npin << 16); }
 // First block index of CTA b when T blocks are shared by P CTAs.
 __host__ __device__ __forceinline__ int range_start(int b, int T, int P) {
   return static_cast<int>((static_cast<long long>(b) * T) / P);

@@ -30,13 +30,20 @@ struct FastDiv {
 
 // Geometry every kernel needs.
 struct Shape {
-  int S, L, Hq, Hkv, G, D, W, NB;  // NB = W / TK
+  int S, L, Hq, Hkv, G, D, W, NB;  // W = slots per (stream, layer, KV head), NB = W / TK
+  int P, NP;                       // pinned prefix slots 0..P-1, NP = P / TK blocks
+  int Wring, NBr;                  // ring slots P..W-1: Wring = W - P, NBr = Wring / TK
+  int Wr;                          // retained window (pairs kept), Wr <= Wring
   int bf16;                        // K/V pools hold bf16 (else f32)
   int q_bf16;                      // queries are bf16 (else f32)
   int style;                       // 0 split-half, 1 interleaved
   int stored_rotated;              // 1: keys kept rotated to (p - origin)
   int epoch;                       // stored-rotated lazy re-basing period E (0: every eviction)
 };
+
+__device__ __forceinline__ int state_ok(const StreamState& s, const Shape& sh) {
+  return state_ok(s, sh.Wring, sh.Wr, sh.P);
+}
 
 // Workspace carve-up (byte offsets from the workspace base).
 struct WsLayout {
@@ -116,6 +123,10 @@ bool attend_mma_supported(const Shape& sh, int c);
 cudaError_t launch_attend_chunk(const AttendParams& p, const CUtensorMap& tk,
                                 const CUtensorMap& tv, int grid, cudaStream_t s);
 bool attend_chunk_supported(const Shape& sh, int c);
+// Chunk attention on the tcgen05 tensor cores (c >= 2, c*G <= 128 rows).
+cudaError_t launch_attend_tc(const AttendParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                             int grid, cudaStream_t s);
+bool attend_tc_supported(const Shape& sh, int c);
 size_t attend_fma_smem(const Shape& sh, int R);
 size_t attend_mma_smem(const Shape& sh, int c);
 

@@ -36,8 +36,10 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
   // Stored-rotated: re-based before this append (every eviction), or, with an
   // epoch E, lagging by fewer than E evictions.
   const bool rebased = !sh.stored_rotated || (sh.epoch ? st.pending < sh.epoch : st.pending == 0);
-  const bool ok = state_ok(st, W) && c >= 1 && c <= W && rebased;
-  const int e = max(0, st.fill + c - W);
+  // Evict just enough of the oldest pairs that at most Wr (the retained
+  // window, <= the W slots) stay.
+  const bool ok = state_ok(st, sh) && c >= 1 && c <= sh.Wr && rebased;
+  const int e = max(0, st.fill + c - sh.Wr);
   // Keys are stored rotated to p - o_ref: o_ref = o2 (every eviction) or
   // o2 - lag2 (epoch), lag2 = the evictions since the last re-rotation.
   const int lag2 = sh.epoch ? st.pending + e : 0;
@@ -53,8 +55,15 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
     l = static_cast<int>(p.div_c.div(lj));
     j = lj - l * c;
   };
-  // New pair j goes to slot first_slot + j (mod W); the state keeps origin mod W.
-  const int first_slot = st.ring + st.fill < W ? st.ring + st.fill : st.ring + st.fill - W;
+  // New pair j goes to ring slot first_ring + j (mod W_ring), i.e. slot P +
+  // that (P pinned slots in front of the ring); the state keeps origin mod
+  // W_ring.
+  const int Wg = sh.Wring;
+  const int first_ring = st.ring + st.fill < Wg ? st.ring + st.fill : st.ring + st.fill - Wg;
+  const int first_slot = sh.P + first_ring;
+  // Stored-rotated keys: a pinned prefix of npin pairs sits at positions
+  // 0..npin-1 in front of the retained ones.
+  const int npin = st.npin;
 
   if (!sh.stored_rotated) {
     // Pre-RoPE: a plain copy of each row in 16-byte chunks.  Each thread loads
@@ -91,7 +100,7 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
         const int kv = kvrow >= rows;
         int l, j, g;
         split_row(kvrow - kv * rows, l, j, g);
-        const int slot = first_slot + j < W ? first_slot + j : first_slot + j - W;
+        const int slot = sh.P + (first_ring + j < Wg ? first_ring + j : first_ring + j - Wg);
         const size_t dst = ((((size_t)s * sh.L + l) * Hkv + g) * W + slot) * D;
         uint8_t* to = static_cast<uint8_t*>(kv ? p.v_pool : p.k_pool) + dst * esz;
         reinterpret_cast<uint4*>(to)[q] = v[t];
@@ -108,14 +117,14 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
       int l, j, g;
       split_row(row, l, j, g);
       const long long pos = first + j;
-      const int slot = first_slot + j < W ? first_slot + j : first_slot + j - W;
+      const int slot = sh.P + (first_ring + j < Wg ? first_ring + j : first_ring + j - Wg);
       const size_t src = ((((size_t)l * sh.S + s) * c + j) * Hkv + g) * D;
       const size_t dst = ((((size_t)s * sh.L + l) * Hkv + g) * W + slot) * D;
       float ka[4], kb[4], va[4], vb[4];
       load_pairs(p.k_new, src, i, D, sh.style, bf, ka, kb);
       load_pairs(p.v_new, src, i, D, sh.style, bf, va, vb);
       float2 cs[4];
-      load_cs4(p.table, (size_t)(pos - o2 + lag2) * (D / 2), i, cs);
+      load_cs4(p.table, (size_t)(npin + pos - o2 + lag2) * (D / 2), i, cs);
       rotate4(ka, kb, cs, 1.f);
       store_pairs(p.k_pool, dst, i, D, sh.style, bf, ka, kb);
       store_pairs(p.v_pool, dst, i, D, sh.style, bf, va, vb);
@@ -136,7 +145,7 @@ __global__ void __launch_bounds__(APPEND_THREADS) append_kernel(const AppendPara
     if (ok) {
       ns.origin = o2;
       ns.fill = n2;
-      ns.ring = st.ring + e < W ? st.ring + e : st.ring + e - W;
+      ns.ring = st.ring + e < Wg ? st.ring + e : st.ring + e - Wg;
       ns.pending = sh.stored_rotated ? (sh.epoch ? lag2 : e) : 0;
       ns.last_new = c;
     } else if (ns.status == 0) {
@@ -208,7 +217,7 @@ __global__ void __launch_bounds__(256, 3) rerotate_kernel(const RerotParams p) {
   const int s = blockIdx.y;
   const StreamState st = p.st[s];
   const int W = sh.W, D = sh.D;
-  const bool work = sh.stored_rotated && state_ok(st, W) &&
+  const bool work = sh.stored_rotated && state_ok(st, sh) &&
                     (sh.epoch ? st.pending >= sh.epoch : st.pending > 0);
   // Every CTA of the stream reads the same state (it changes only after the
   // last CTA's ticket below), so either all take a ticket or none does.
@@ -250,8 +259,10 @@ __global__ void __launch_bounds__(256, 3) rerotate_kernel(const RerotParams p) {
     for (int j = 0; j < NB; ++j) {
       row[j] = nullptr;
       if (lg < LH) {
+        // Retained pair r (oldest first) of the ring behind the P pinned
+        // slots; a pinned prefix keeps its positions and is never turned.
         const int r = rem >> cshift;
-        const int slot = st.ring + r < W ? st.ring + r : st.ring + r - W;
+        const int slot = sh.P + (st.ring + r < sh.Wring ? st.ring + r : st.ring + r - sh.Wring);
         row[j] = pool + (sbase + (size_t)lg * W + slot) * D;
 #pragma unroll
         for (int k = 0; k < NW; ++k) {

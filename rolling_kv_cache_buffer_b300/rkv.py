@@ -21,7 +21,7 @@ RKV_OK, RKV_ERR_INVALID_ARG, RKV_ERR_UNSUPPORTED, RKV_ERR_CAPACITY, RKV_ERR_CUDA
 RKV_BF16, RKV_F32 = 0, 1
 RKV_PRE_ROPE, RKV_STORED_ROTATED = 0, 1
 RKV_ROPE_SPLIT_HALF, RKV_ROPE_INTERLEAVED = 0, 1
-RKV_ATTEND_AUTO, RKV_ATTEND_FMA, RKV_ATTEND_MMA = 0, 1, 2
+RKV_ATTEND_AUTO, RKV_ATTEND_FMA, RKV_ATTEND_MMA, RKV_ATTEND_TC = 0, 1, 2, 3
 
 
 class rkv_config(ctypes.Structure):
@@ -31,6 +31,7 @@ class rkv_config(ctypes.Structure):
         ("max_chunk", c_int32), ("kv_dtype", c_int32), ("q_dtype", c_int32),
         ("layout", c_int32), ("rope_style", c_int32), ("attend_impl", c_int32),
         ("rope_theta", c_double), ("softmax_scale", c_float), ("rebase_epoch", c_int32),
+        ("window", c_int32), ("n_pinned", c_int32),
     ]
 
 
@@ -173,17 +174,18 @@ def rkv_last_launch_count(h) -> int:
 _DT = {"bf16": RKV_BF16, "f32": RKV_F32}
 _LAYOUT = {"pre_rope": RKV_PRE_ROPE, "stored_rotated": RKV_STORED_ROTATED}
 _STYLE = {"split_half": RKV_ROPE_SPLIT_HALF, "interleaved": RKV_ROPE_INTERLEAVED}
-_IMPL = {"auto": RKV_ATTEND_AUTO, "fma": RKV_ATTEND_FMA, "mma": RKV_ATTEND_MMA}
+_IMPL = {"auto": RKV_ATTEND_AUTO, "fma": RKV_ATTEND_FMA, "mma": RKV_ATTEND_MMA,
+         "tc": RKV_ATTEND_TC}
 
 
 def make_config(n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, capacity, max_chunk=1,
                 kv_dtype="bf16", q_dtype=None, layout="pre_rope", rope_style="split_half",
                 rope_theta=1e6, softmax_scale=0.0, attend_impl="auto",
-                rebase_epoch=0) -> rkv_config:
+                rebase_epoch=0, window=0, n_pinned=0) -> rkv_config:
     return rkv_config(n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, capacity, max_chunk,
                       _DT[kv_dtype], _DT[q_dtype or kv_dtype], _LAYOUT[layout],
                       _STYLE[rope_style], _IMPL[attend_impl], float(rope_theta),
-                      float(softmax_scale), int(rebase_epoch))
+                      float(softmax_scale), int(rebase_epoch), int(window), int(n_pinned))
 
 
 class RollingKV:
@@ -192,12 +194,14 @@ class RollingKV:
     def __init__(self, n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, capacity,
                  max_chunk=1, kv_dtype="bf16", q_dtype=None, layout="pre_rope",
                  rope_style="split_half", rope_theta=1e6, softmax_scale=0.0,
-                 attend_impl="auto", device="cuda", rebase_epoch=0):
+                 attend_impl="auto", device="cuda", rebase_epoch=0, window=0, n_pinned=0):
         import torch
         self.torch = torch
         self.cfg = make_config(n_streams, n_layers, n_q_heads, n_kv_heads, head_dim, capacity,
                                max_chunk, kv_dtype, q_dtype, layout, rope_style, rope_theta,
-                               softmax_scale, attend_impl, rebase_epoch)
+                               softmax_scale, attend_impl, rebase_epoch, window, n_pinned)
+        self.P = n_pinned
+        self.Wr = window or capacity - n_pinned
         pool_b, state_b, ws_b = rkv_required_bytes(self.cfg)
         self.kv_dtype = torch.bfloat16 if kv_dtype == "bf16" else torch.float32
         self.q_dtype = torch.bfloat16 if (q_dtype or kv_dtype) == "bf16" else torch.float32

@@ -14,12 +14,13 @@ def make_cache(wl, layout="pre_rope", attend_impl="auto", max_chunk=None, style=
     return RollingKV(n_streams or wl.n_streams, wl.n_layers, wl.n_q_heads, wl.n_kv_heads,
                      wl.head_dim, wl.capacity, max_chunk=max_chunk or wl.n_new,
                      kv_dtype=wl.kv_dtype, layout=layout, rope_style=style,
-                     rope_theta=wl.rope_theta, attend_impl=attend_impl)
+                     rope_theta=wl.rope_theta, attend_impl=attend_impl,
+                     window=wl.window or 0)
 
 
 def make_oracle(wl, cls=O.RollingCacheOracle, style="split_half", n_layers=None, n_streams=None):
     return cls(n_streams or wl.n_streams, n_layers or wl.n_layers, wl.n_q_heads, wl.n_kv_heads,
-               wl.head_dim, wl.capacity, theta=wl.rope_theta, style=style)
+               wl.head_dim, wl.capacity, theta=wl.rope_theta, style=style, window=wl.window)
 
 
 def dev(x, dtype):

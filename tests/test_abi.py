@@ -31,8 +31,8 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_abi_version_and_struct_size():
-    assert R.rkv_abi_version() == 1
-    assert ctypes.sizeof(R.rkv_config) == 64
+    assert R.rkv_abi_version() == 2
+    assert ctypes.sizeof(R.rkv_config) == 72
     assert ctypes.sizeof(R.rkv_buffers) == 40
 
 
@@ -67,6 +67,11 @@ def test_required_bytes_closed_form(name):
     (dict(rebase_epoch=-1), R.rkv.RKV_ERR_INVALID_ARG),
     (dict(rebase_epoch=64), R.rkv.RKV_ERR_INVALID_ARG),                       # pre-RoPE
     (dict(layout="stored_rotated", rebase_epoch=4096, max_chunk=2), R.rkv.RKV_ERR_INVALID_ARG),
+    (dict(capacity=768, window=769), R.rkv.RKV_ERR_INVALID_ARG),              # window > slots
+    (dict(capacity=768, window=-1), R.rkv.RKV_ERR_INVALID_ARG),
+    (dict(capacity=768, window=4, max_chunk=5), R.rkv.RKV_ERR_CAPACITY),      # chunk > window
+    (dict(layout="stored_rotated", capacity=768, window=750, rebase_epoch=751),
+     R.rkv.RKV_ERR_INVALID_ARG),                                               # E + c > W_r + 1
 ])
 def test_config_rejected(kw, status):
     with pytest.raises(R.RkvError) as e:
@@ -80,6 +85,15 @@ def test_rebase_epoch_bounds_accepted():
     R.rkv_required_bytes(_cfg(layout="stored_rotated", rebase_epoch=4090, max_chunk=7))
     R.rkv_required_bytes(_cfg(layout="stored_rotated", rebase_epoch=0))
     R.rkv_required_bytes(_cfg(layout="stored_rotated", rebase_epoch=1))   # 1 = every eviction
+    R.rkv_required_bytes(_cfg(layout="stored_rotated", capacity=768, window=750,
+                              rebase_epoch=750))
+
+
+def test_window_accepted():
+    # the encoder's 750-frame window in 768 slots, four frames per step
+    pool, _, _ = R.rkv_required_bytes(_cfg(n_layers=32, n_q_heads=20, n_kv_heads=20,
+                                          head_dim=64, capacity=768, window=750, max_chunk=4))
+    assert pool == 32 * 20 * 768 * 64 * 2
 
 
 def test_create_rejects_null_and_misaligned_buffers_without_gpu():

@@ -14,8 +14,9 @@ def _args(**kw):
 
 def test_auto_path_per_layout():
     q = WORKLOADS["qwen3b"]
-    # Pre-RoPE keys: the separate calls (faster on B300); the fused forms on request.
-    assert not bench.step_is_fused(q, "pre_rope", 0, _args())
+    # Pre-RoPE keys: the fused step (faster on B300); the separate calls on request.
+    assert bench.step_is_fused(q, "pre_rope", 0, _args())
+    assert not bench.step_is_fused(q, "pre_rope", 0, _args(path="split"))
     assert bench.step_is_fused(q, "pre_rope", 0, _args(path="fused"))
     assert bench.step_is_fused(q, "pre_rope", 0, _args(per_layer=True))
     assert bench.step_is_fused(q, "pre_rope", 0, _args(graph=True))
