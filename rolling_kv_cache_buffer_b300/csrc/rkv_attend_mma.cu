@@ -505,6 +505,14 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
     const int pi = cw >> 1, hh = cw & 1;
     int jb = pi, stage = pi, round = 0;   // the pair's next block and its stage (NS >= NPAIR)
     bool dead = false;
+    // The first pass through the loop is a dry run of the segment end: no
+    // block, nothing written (neither the slots, which alias the stages the
+    // producer is filling, nor outputs, partials, tickets, the partner CTA or
+    // the merge-done barrier), while the first tiles are still on their way.
+    // It brings the merge's code into the instruction caches, so that the
+    // real merge at the end of the stream does not fetch it from memory.
+    bool dry = rb < re;
+#pragma unroll 1
     for (int x = rb; x < re;) {
       const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
       const int x1 = min(u.uend, re);
@@ -513,7 +521,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
       // The next segment's query (and new pair): copied now, converted once
       // this segment is done with `qs` (and `kvn`).
       const bool has_next = x1 < re;
-      if (has_next) stage_unit(unit_of_cached(x1, p, pre, sa, sfill));
+      if (has_next && !dry) stage_unit(unit_of_cached(x1, p, pre, sa, sfill));
 
       // The raw query of head g (dims of the thread's A fragments), from `qs`.
       auto load_qf = [&](float (&qr)[NKB][4]) {
@@ -536,7 +544,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
           o[kb][j] = 0.f;
           qa[kb][j] = 0u;
         }
-      if constexpr (!ROTK) {
+      if (!ROTK && !dry) {
         // Stored-rotated keys sit at r (+ the stream's lag, with a re-basing
         // epoch) already: one base, R(r_q + lag) q.
         const int lag = slag[u.s];
@@ -587,7 +595,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
         return v;
       };
       if constexpr (ROTK) {
-        if (rb + jb < x1) {
+        if (rb + jb < x1 && !dry) {
           seed = table_row(block_geo(rb + jb, u, p.sh).r0);
           seeded = false;
         }
@@ -603,8 +611,8 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
       };
       const int Wg = p.sh.Wring;
       BlockWalk wk;
-      if (rb + jb < x1) wk.init(rb + jb, u, p.sh);
-      for (; rb + jb < x1; jb += NPAIR) {
+      if (rb + jb < x1 && !dry) wk.init(rb + jb, u, p.sh);
+      for (; !dry && rb + jb < x1; jb += NPAIR) {
         if (r0 >= 0) {
           // NPAIR blocks further on: the query base turns by R(-NPAIR*TK), and
           // by R(W_ring) each time the ring's end is passed; where the blocks
@@ -855,13 +863,15 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
             if (lane == 0) mx[cw] = dot * p.scale_log2;
           }
         }
-        float* my = slots + cw * C::SLOT;
-        if (cq == 0) { my[g] = m_run; my[8 + g] = lsum; }
+        if (!dry) {
+          float* my = slots + cw * C::SLOT;
+          if (cq == 0) { my[g] = m_run; my[8 + g] = lsum; }
 #pragma unroll
-        for (int i = 0; i < C::FR; ++i) my[16 + 32 * i + lane] = o[i >> 2][i & 3];
+          for (int i = 0; i < C::FR; ++i) my[16 + 32 * i + lane] = o[i >> 2][i & 3];
+        }
       }
       named_bar_sync(BAR_CONS, CONS_THREADS);
-      if (has_next) unstage_q();
+      if (has_next && !dry) unstage_q();
       const int R = p.R;   // == G for decode
       {
         // Thread ct takes fragment elements i = ct/32, ct/32 + NCW, ... of lane
@@ -889,7 +899,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
           for (int w = 0; w < NCW; ++w) a += sc[w] * slots[w * C::SLOT + 16 + 32 * i + lf];
           v[k] = a;
         }
-        if (ship) {
+        if (ship && !dry) {
           const uint32_t peer = cluster_rank() ^ 1u;
           const uint32_t dst = map_to_rank(smem_u32(rslots + ct), peer);
           const uint32_t bar = map_to_rank(smem_u32(rx_bar), peer);
@@ -899,7 +909,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
           for (int k = 0; k < NE; ++k) st_async_f32(dst + 4u * (2 + k) * CONS_THREADS, v[k], bar);
         } else {
           bool got = true;
-          if (receive) {
+          if (receive && !dry) {
             got = false;
             for (uint32_t i = 0; i < WAIT_LIMIT && !got; ++i)
               got = mbar_try_wait_cluster(smem_u32(rx_bar), 0);
@@ -927,7 +937,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
             for (int k = 0; k < NE; ++k) v[k] = s0 * v[k] + sn * kvn[D + dd[k]];
             M = Mx;
           }
-          if (got && h < R) {
+          if (got && h < R && !dry) {
             if (whole || receive) {
               const float inv = L > 0.f ? 1.f / L : 0.f;
               float* out = p.out + row_offset(p, u, h);
@@ -942,7 +952,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
           }
         }
       }
-      if (!whole && !CL) {
+      if (!whole && !CL && !dry) {
         // Publish this CTA's partial (one release by one thread after the
         // barrier); the last CTA of the unit to arrive merges them all.
         named_bar_sync(BAR_CONS, CONS_THREADS);
@@ -983,6 +993,10 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
       // asynchronous copies into the same memory.
       fence_proxy_async();
       named_bar_sync(BAR_CONS, CONS_THREADS);
+      if (dry) {   // the real pass over the same segment
+        dry = false;
+        continue;
+      }
       if (ct == 0) mbar_arrive(smem_u32(mdone));
       if constexpr (FUSED) {
         if (has_next) unstage_new();
