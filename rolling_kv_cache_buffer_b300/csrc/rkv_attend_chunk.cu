@@ -547,26 +547,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         named_bar_sync(CBAR_CONS, CCONS);
         const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
         if (flag[0] == b1 - b0) {
-          const int rs0 = range_start(b0, T, P);
-          for (int idx = ct; idx < R * D; idx += CCONS) {
-            const int row = idx / D, d = idx % D;
-            float M = NEG_BIG;
-#pragma unroll 8
-            for (int bb = b0; bb <= b1; ++bb) {
-              const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
-              M = fmaxf(M, __ldcg(p.partials + (size_t)(2 * bb + k) * p.slot_floats + row));
-            }
-            float num = 0.f, den = 0.f;
-#pragma unroll 8
-            for (int bb = b0; bb <= b1; ++bb) {
-              const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
-              const float* pp = p.partials + (size_t)(2 * bb + k) * p.slot_floats;
-              const float sc = exp2f(__ldcg(pp + row) - M);
-              den += sc * __ldcg(pp + R + row);
-              num += sc * __ldcg(pp + 2 * R + row * D + d);
-            }
-            p.out[row_offset(p, u, row) + d] = den > 0.f ? num / den : 0.f;
-          }
+          merge_unit_partials<16>(p, u, T, P, ct, CCONS);
           if (ct == 0) p.unit_tickets[unit_index(p, u)] = 0;
         }
       }

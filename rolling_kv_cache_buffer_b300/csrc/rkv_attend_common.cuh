@@ -287,6 +287,60 @@ __device__ __forceinline__ void zero_empty_units_cached(const AttendParams& p, c
   }
 }
 
+// The last CTA of a split unit combines the unit's partials (m, l and the
+// unnormalised O of each row, one slot per CTA segment) into its output:
+//   out = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k,   M = max_k m_k.
+// Thread t of nt takes elements t, t + nt, ... Q at a time, so that the loads
+// of one pass over the partials are independent of one another (a few L2
+// round trips in all, not two per element).
+template <int Q>
+__device__ __forceinline__ void merge_unit_partials(const AttendParams& p, const UnitRef& u,
+                                                    int T, int P, int t, int nt) {
+  const int R = p.R, D = p.sh.D, RD = R * D;
+  const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
+  const int rs0 = range_start(b0, T, P);
+  // CTA b0 holds the unit in its second slot when its range starts before it.
+  const float* first =
+      p.partials + (size_t)(2 * b0 + (rs0 < u.ustart ? 1 : 0)) * p.slot_floats;
+  auto part = [&](int b) {
+    return b == b0 ? first : p.partials + (size_t)(2 * b) * p.slot_floats;
+  };
+  for (int i0 = t; i0 < RD; i0 += Q * nt) {
+    float M[Q], num[Q], den[Q];
+    int h[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      h[q] = min(i0 + q * nt, RD - 1) / D;
+      M[q] = NEG_BIG;
+      num[q] = 0.f;
+      den[q] = 0.f;
+    }
+#pragma unroll 4
+    for (int b = b0; b <= b1; ++b) {
+      const float* pp = part(b);
+#pragma unroll
+      for (int q = 0; q < Q; ++q) M[q] = fmaxf(M[q], __ldcg(pp + h[q]));
+    }
+#pragma unroll 2
+    for (int b = b0; b <= b1; ++b) {
+      const float* pp = part(b);
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        const int e = min(i0 + q * nt, RD - 1);
+        const float w = exp2f(__ldcg(pp + h[q]) - M[q]);
+        den[q] += w * __ldcg(pp + R + h[q]);
+        num[q] += w * __ldcg(pp + 2 * R + e);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      const int e = i0 + q * nt;
+      if (e < RD)
+        p.out[row_offset(p, u, h[q]) + (e - h[q] * D)] = den[q] > 0.f ? num[q] / den[q] : 0.f;
+    }
+  }
+}
+
 // Segment end.  `mrg` holds NWARP warp partials of `wstride` floats, each
 // [m(R) | l(R) | o(R*D)] with m in log2 units.  All CTA threads call this
 // right after a __syncthreads.  Writes the unit's output when the segment is
@@ -336,25 +390,7 @@ __device__ __forceinline__ void finish_segment(const AttendParams& p, const Unit
   const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
   if (*flag != b1 - b0) return;  // another CTA finishes this unit
   __threadfence();
-  const int rs0 = range_start(b0, T, P);
-  for (int idx = threadIdx.x; idx < R * D; idx += nthr) {
-    const int row = idx / D, d = idx % D;
-    float M = NEG_BIG;
-    for (int b = b0; b <= b1; ++b) {
-      const int k = (b == b0 && rs0 < u.ustart) ? 1 : 0;
-      const float* pp = p.partials + (size_t)(2 * b + k) * p.slot_floats;
-      M = fmaxf(M, __ldcg(pp + row));
-    }
-    float num = 0.f, den = 0.f;
-    for (int b = b0; b <= b1; ++b) {
-      const int k = (b == b0 && rs0 < u.ustart) ? 1 : 0;
-      const float* pp = p.partials + (size_t)(2 * b + k) * p.slot_floats;
-      const float sc = exp2f(__ldcg(pp + row) - M);
-      den += sc * __ldcg(pp + R + row);
-      num += sc * __ldcg(pp + 2 * R + row * D + d);
-    }
-    p.out[row_offset(p, u, row) + d] = den > 0.f ? num / den : 0.f;
-  }
+  merge_unit_partials<16>(p, u, T, P, threadIdx.x, nthr);
   if (threadIdx.x == 0) p.unit_tickets[unit_index(p, u)] = 0;
 }
 

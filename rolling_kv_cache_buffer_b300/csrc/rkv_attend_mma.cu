@@ -964,28 +964,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
         named_bar_sync(BAR_CONS, CONS_THREADS);
         const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
         if (flag[0] == b1 - b0) {
-          const int rs0 = range_start(b0, T, P);
-          for (int idx = ct; idx < R * D; idx += CONS_THREADS) {
-            const int h = idx / D, d = idx % D;
-            float M = NEG_BIG;
-            // Unrolled so that the partials' loads overlap instead of paying
-            // one L2 round trip each.
-#pragma unroll 8
-            for (int bb = b0; bb <= b1; ++bb) {
-              const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
-              M = fmaxf(M, __ldcg(p.partials + (size_t)(2 * bb + k) * p.slot_floats + h));
-            }
-            float num = 0.f, den = 0.f;
-#pragma unroll 8
-            for (int bb = b0; bb <= b1; ++bb) {
-              const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
-              const float* pp = p.partials + (size_t)(2 * bb + k) * p.slot_floats;
-              const float sc = exp2f(__ldcg(pp + h) - M);
-              den += sc * __ldcg(pp + R + h);
-              num += sc * __ldcg(pp + 2 * R + h * D + d);
-            }
-            p.out[row_offset(p, u, h) + d] = den > 0.f ? num / den : 0.f;
-          }
+          merge_unit_partials<8>(p, u, T, P, ct, CONS_THREADS);
           if (ct == 0) p.unit_tickets[unit_index(p, u)] = 0;
         }
       }

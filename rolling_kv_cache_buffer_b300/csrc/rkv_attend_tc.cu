@@ -52,8 +52,16 @@ constexpr int TC_ROWS = 128;                    // M of every product
 constexpr int TBAR_PREFIX = 2;                  // named barrier: block prefix ready
 constexpr int TBAR_SM = 3;                      // named barrier of the softmax warps
 constexpr float TC_TAU = 8.f;                   // lazy rescale threshold (log2 units)
-// Tensor memory columns: S[2] (f32), P[2] (bf16 pairs), O (f32, D columns).
-constexpr int TM_S = 0, TM_P = 64, TM_O = 128, TM_COLS = 256;
+// A step of the softmax and of the products covers up to TC_KB key blocks
+// (128 keys): S = Q K^T of the step's blocks lands side by side in one S
+// buffer, the softmax reads it in two passes (maximum, then P), and O += P V
+// takes the step's blocks one after the other.
+constexpr int TC_KB = 4;
+// Tensor memory columns: S[2] (f32, TC_KB * TK each), P[2] (bf16 pairs,
+// TC_KB * TK / 2 each), O (f32, D columns).
+constexpr int TM_SW = TC_KB * TK, TM_PW = TC_KB * TK / 2;
+constexpr int TM_S = 0, TM_P = 2 * TM_SW, TM_O = TM_P + 2 * TM_PW, TM_COLS = 512;
+static_assert(TM_O + 128 <= TM_COLS, "tensor memory columns");
 
 template <int D, bool ROTK>
 struct TcCfg : PipeCfg<D, ROTK> {
@@ -140,6 +148,13 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16])
       "r"(r[15])
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 2^x on the special-function unit (relative error about 2^-22; -inf gives 0):
+// the softmax weights are rounded to bf16 right after.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 // Byte offset of element (row, col) of a K-major, 128-byte-swizzled tile of
 // `rows` x 64 bf16 per box (col < 64 within the box).
@@ -393,64 +408,70 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t id_pv = idesc_bf16(TC_ROWS, D, 1);
       const uint32_t q_s = smem_u32(qt);
       uint64_t* ready = rotd;   // tiles staged (keys rotated, outside V rows zeroed)
-      int jj = 0, seg = 0;
+      int jj = 0, t = 0, seg = 0;   // blocks and steps over the CTA, segments
       bool dead = false;
-      for (int x = rb; x < re && !dead; ++seg) {
-        const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
-        const int x1 = min(u.uend, re);
-        if (!mbar_wait_or_abort(smem_u32(qready), seg & 1, abort_flag)) { dead = true; break; }
+      auto wait = [&](uint64_t* bar, int parity) {
+        if (!dead && !mbar_wait_or_abort(smem_u32(bar), parity, abort_flag)) dead = true;
+        return !dead;
+      };
+      // O += P V over the n blocks of step tp (first block jb), P from the
+      // step's P buffer; each block's stage is released by the commit after
+      // its products.
+      auto issue_pv = [&](int jb, int n, int tp, bool first) {
+        if (!wait(pready + (tp & 1), (tp >> 1) & 1)) return;
         tc_fence_after();
-        const int j0 = jj;
-        for (; x < x1; ++x, ++jj) {
-          const int s = jj % NS, r = jj / NS, bsl = jj & 1;
-          if (!mbar_wait_or_abort(smem_u32(ready + s), r & 1, abort_flag)) { dead = true; break; }
-          if (jj >= 2 && !mbar_wait_or_abort(smem_u32(sfree + bsl), ((jj >> 1) - 1) & 1,
-                                             abort_flag)) { dead = true; break; }
-          tc_fence_after();
-          // S[bsl] = Q K^T over D in k-steps of 16 (32 bytes of a 128-byte row).
-          const uint32_t k_s = smem_u32(stages + (size_t)s * C::STAGE);
-#pragma unroll
-          for (int ks = 0; ks < NKS; ++ks) {
-            const uint64_t a = sdesc(q_s + (ks >> 2) * (TC_ROWS * 128) + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc(k_s + (ks >> 2) * (TK * 128) + (ks & 3) * 32, 16, 1024);
-            tc_mma_ss(tmem + TM_S + bsl * TK, a, bd, id_qk, ks > 0);
-          }
-          tc_commit(smem_u32(sfull + bsl));
-          if (jj > j0) {
-            // O += P V for the previous block, once its P is in tensor memory.
-            const int jp = jj - 1, sp = jp % NS, bp = jp & 1;
-            if (!mbar_wait_or_abort(smem_u32(pready + bp), (jp >> 1) & 1, abort_flag)) {
-              dead = true;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t v_s = smem_u32(stages + (size_t)sp * C::STAGE + C::TILE);
-#pragma unroll
-            for (int ks = 0; ks < TK / 16; ++ks) {
-              const uint64_t bd = sdesc(v_s + ks * 16 * 128, TK * 128, 1024);
-              tc_mma_ts(tmem + TM_O, tmem + TM_P + bp * (TK / 2) + ks * 8, bd, id_pv,
-                        (jp > j0 || ks > 0) ? 1 : 0);
-            }
-            tc_commit(smem_u32(empty + sp));
-          }
-        }
-        if (dead) break;
-        if (jj > j0) {
-          const int jp = jj - 1, sp = jp % NS, bp = jp & 1;
-          if (!mbar_wait_or_abort(smem_u32(pready + bp), (jp >> 1) & 1, abort_flag)) {
-            dead = true;
-            break;
-          }
-          tc_fence_after();
+        for (int i = 0; i < n; ++i) {
+          const int sp = (jb + i) % NS;
           const uint32_t v_s = smem_u32(stages + (size_t)sp * C::STAGE + C::TILE);
 #pragma unroll
           for (int ks = 0; ks < TK / 16; ++ks) {
             const uint64_t bd = sdesc(v_s + ks * 16 * 128, TK * 128, 1024);
-            tc_mma_ts(tmem + TM_O, tmem + TM_P + bp * (TK / 2) + ks * 8, bd, id_pv,
-                      (jp > j0 || ks > 0) ? 1 : 0);
+            tc_mma_ts(tmem + TM_O, tmem + TM_P + (tp & 1) * TM_PW + i * (TK / 2) + ks * 8, bd,
+                      id_pv, (first && i == 0 && ks == 0) ? 0 : 1);
           }
           tc_commit(smem_u32(empty + sp));
         }
+      };
+      for (int x = rb; x < re && !dead; ++seg) {
+        const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
+        const int x1 = min(u.uend, re);
+        if (!wait(qready, seg & 1)) break;
+        tc_fence_after();
+        int pj = 0, pn = 0;   // the previous step's first block and block count
+        bool first = true;    // the segment's first product into O
+        while (x < x1 && !dead) {
+          const int nb = min(TC_KB, x1 - x), bs = t & 1;
+          // The S buffer was read by the softmax of step t - 2.
+          if (t >= 2 && !wait(sfree + bs, ((t >> 1) - 1) & 1)) break;
+          // S = Q K^T of each block over D in k-steps of 16 (32 bytes of a
+          // 128-byte row), into the block's 32 columns of the buffer.
+          for (int i = 0; i < nb; ++i) {
+            const int sb = (jj + i) % NS;
+            if (!wait(ready + sb, ((jj + i) / NS) & 1)) break;
+            tc_fence_after();
+            const uint32_t k_s = smem_u32(stages + (size_t)sb * C::STAGE);
+#pragma unroll
+            for (int ks = 0; ks < NKS; ++ks) {
+              const uint64_t a = sdesc(q_s + (ks >> 2) * (TC_ROWS * 128) + (ks & 3) * 32, 16, 1024);
+              const uint64_t bd = sdesc(k_s + (ks >> 2) * (TK * 128) + (ks & 3) * 32, 16, 1024);
+              tc_mma_ss(tmem + TM_S + bs * TM_SW + i * TK, a, bd, id_qk, ks > 0);
+            }
+          }
+          if (dead) break;
+          tc_commit(smem_u32(sfull + bs));
+          if (pn > 0) {
+            issue_pv(pj, pn, t - 1, first);
+            first = false;
+          }
+          pj = jj;
+          pn = nb;
+          jj += nb;
+          x += nb;
+          ++t;
+        }
+        if (dead) break;
+        if (pn > 0) issue_pv(pj, pn, t - 1, first);
+        if (dead) break;
         tc_commit(smem_u32(ofin));
         // The producer may go on with the next segment (its epilogue leaves
         // the stages alone).
@@ -479,7 +500,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int st = tid - 32 * W_SM0;          // 0..127
     const bool warp_rows = 32 * q4 < R;       // the warp holds real rows
     zero_empty_units_cached(p, sa, sfill, st, TC_SMW * 32);
-    int jj = 0, seg = 0;
+    int jj = 0, t = 0, seg = 0;   // blocks and steps over the CTA, segments
+    int jl1 = -1, jl2 = -1;       // the last blocks of the two previous steps
     bool dead = false;
     auto waited = [&](uint64_t* bar, int parity) {   // false (and dead) if it ran out
       if (dead) return false;
@@ -565,41 +587,78 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (lane == 0) mbar_arrive(smem_u32(qready));
 
       float m = NEG_BIG, l = 0.f;
-      const int j0 = jj;
+      const int t0 = t;
       BlockWalk wk;
       wk.init(x, u, p.sh);
       const int Wg = p.sh.Wring;
-      for (bool first = true; x < x1; ++x, ++jj, first = false) {
-        if (!first) wk.advance(1, u, p.sh);
-        const BlockGeo& bg = wk.g;
-        const int bsl = jj & 1;
-        if (!waited(sfull + bsl, (jj >> 1) & 1)) continue;
-        tc_fence_after();
-        uint32_t sr[32];
-        if (warp_rows) tc_ld32(tmem + lane_addr + TM_S + bsl * TK, sr);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(sfree + bsl));
-        // Scores in log2 units; masked: outside the window or after the row.
-        float sv[32];
-        float bm = NEG_BIG;
+      // Scores of one block in log2 units; masked (-inf): outside the window
+      // or after the row.  A block that holds no ring end, lies inside the
+      // window and ends at or before the chunk's first query needs no mask.
+      auto scores = [&](const BlockGeo& g, const uint32_t (&sr)[32], float (&sv)[32]) {
+        if (g.wrap_at >= TK && g.r0 + TK <= g.lim && g.r0 + TK - 1 <= qbase) {
 #pragma unroll
-        for (int d = 0; d < 32; ++d) {
-          const int r = slot_pos(bg, d, Wg);
-          const bool vis = row < R && r < bg.lim && r <= rq;
-          sv[d] = vis ? __uint_as_float(sr[d]) * p.scale_log2 : NEG_BIG;
-          bm = fmaxf(bm, sv[d]);
+          for (int d = 0; d < 32; ++d) sv[d] = __uint_as_float(sr[d]) * p.scale_log2;
+        } else {
+#pragma unroll
+          for (int d = 0; d < 32; ++d) {
+            const int r = slot_pos(g, d, Wg);
+            const bool vis = row < R && r < g.lim && r <= rq;
+            sv[d] = vis ? __uint_as_float(sr[d]) * p.scale_log2 : -INFINITY;
+          }
+        }
+      };
+      auto load_s = [&](int col, uint32_t (&sr)[32]) {
+        if (warp_rows) {
+          tc_ld32(tmem + lane_addr + col, sr);
+        } else {
+#pragma unroll
+          for (int d = 0; d < 32; ++d) sr[d] = 0u;
+        }
+      };
+      for (bool first = true; x < x1; first = false) {
+        const int nb = min(TC_KB, x1 - x), bs = t & 1;
+        if (!first) wk.advance(TC_KB, u, p.sh);
+        const int jl = jj + nb - 1;   // the step's last block
+        auto next = [&]() {
+          x += nb;
+          jj += nb;
+          ++t;
+          jl2 = jl1;
+          jl1 = jl;
+        };
+        if (!waited(sfull + bs, (t >> 1) & 1)) { next(); continue; }
+        tc_fence_after();
+        // Pass 1: the step's maximum.
+        float bm = -INFINITY;
+        {
+          BlockWalk w = wk;
+#pragma unroll 1
+          for (int i = 0; i < nb; ++i) {
+            if (i) w.advance(1, u, p.sh);
+            uint32_t sr[32];
+            float sv[32];
+            load_s(TM_S + bs * TM_SW + i * TK, sr);
+            scores(w.g, sr, sv);
+            float mx[16];
+#pragma unroll
+            for (int d = 0; d < 16; ++d) mx[d] = fmaxf(sv[d], sv[d + 16]);
+#pragma unroll
+            for (int k = 8; k >= 1; k >>= 1)
+#pragma unroll
+              for (int d = 0; d < k; ++d) mx[d] = fmaxf(mx[d], mx[d + k]);
+            bm = fmaxf(bm, mx[0]);
+          }
         }
         // Lazy rescale: the running maximum moves only when a score exceeds
         // it by more than TC_TAU; O and l are then rescaled.  O is quiet once
-        // the previous block's product has completed (its stage's commit).
+        // the previous step's products have completed (the commit after its
+        // last block).
         const bool grow = bm > m + TC_TAU;
         const float mnew = grow ? bm : m;
-        if (__any_sync(0xffffffffu, grow && jj > j0)) {
-          const int jp = jj - 1;
-          if (!waited(empty + jp % NS, (jp / NS) & 1)) continue;
+        if (__any_sync(0xffffffffu, grow && t > t0)) {
+          if (!waited(empty + (jj - 1) % NS, ((jj - 1) / NS) & 1)) { next(); continue; }
           tc_fence_after();
-          const float sc = exp2f(m - mnew);
+          const float sc = ex2(m - mnew);
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 16) {
             uint32_t ov[16];
@@ -609,28 +668,45 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tc_st16(tmem + lane_addr + TM_O + c0, ov);
           }
         }
-        if (grow) l *= exp2f(m - mnew);
+        if (grow) l *= ex2(m - mnew);
         m = mnew;
-        uint32_t pw[16];
-        float psum = 0.f;
-#pragma unroll
-        for (int d = 0; d < 32; d += 2) {
-          const float p0 = sv[d] > 0.5f * NEG_BIG ? exp2f(sv[d] - m) : 0.f;
-          const float p1 = sv[d + 1] > 0.5f * NEG_BIG ? exp2f(sv[d + 1] - m) : 0.f;
-          psum += p0 + p1;
-          pw[d >> 1] = pack_bf2(p0, p1);
-        }
-        l += psum;
-        // P[bsl] was last read by the product of block jj - 2: wait for it.
-        if (jj >= 2) {
-          const int jq = jj - 2;
-          if (!waited(empty + jq % NS, (jq / NS) & 1)) continue;
+        // The P buffer was last read by the products of step t - 2: wait for
+        // the commit after its last block.
+        if (t >= 2) {
+          if (!waited(empty + jl2 % NS, (jl2 / NS) & 1)) { next(); continue; }
           tc_fence_after();
         }
-        if (warp_rows) tc_st16(tmem + lane_addr + TM_P + bsl * (TK / 2), pw);
+        // Pass 2: P = 2^(s - m) (masked scores give 2^-inf = 0; m is always
+        // finite), rounded to bf16, two per column of the P buffer.
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          BlockWalk w = wk;
+#pragma unroll 1
+          for (int i = 0; i < nb; ++i) {
+            if (i) w.advance(1, u, p.sh);
+            uint32_t sr[32];
+            float sv[32];
+            load_s(TM_S + bs * TM_SW + i * TK, sr);
+            scores(w.g, sr, sv);
+            uint32_t pw[16];
+#pragma unroll
+            for (int d = 0; d < 32; d += 2) {
+              const float p0 = ex2(sv[d] - m);
+              const float p1 = ex2(sv[d + 1] - m);
+              ps[(d >> 1) & 3] += p0 + p1;
+              pw[d >> 1] = pack_bf2(p0, p1);
+            }
+            if (warp_rows) tc_st16(tmem + lane_addr + TM_P + bs * TM_PW + i * (TK / 2), pw);
+          }
+        }
+        l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(pready + bsl));
+        if (lane == 0) {
+          mbar_arrive(smem_u32(sfree + bs));
+          mbar_arrive(smem_u32(pready + bs));
+        }
+        next();
       }
       // ---- segment end: O row from tensor memory, then the unit's output ----
       if (waited(ofin, seg & 1)) {
@@ -670,24 +746,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         named_bar_sync(TBAR_SM, TC_SMW * 32);
         const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
         if (flag[0] == b1 - b0) {
-          const int rs0 = range_start(b0, T, P);
-          for (int idx = st; idx < R * D; idx += TC_SMW * 32) {
-            const int h = idx / D, d = idx % D;
-            float M = NEG_BIG;
-            for (int bb = b0; bb <= b1; ++bb) {
-              const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
-              M = fmaxf(M, __ldcg(p.partials + (size_t)(2 * bb + k) * p.slot_floats + h));
-            }
-            float num = 0.f, den = 0.f;
-            for (int bb = b0; bb <= b1; ++bb) {
-              const int k = (bb == b0 && rs0 < u.ustart) ? 1 : 0;
-              const float* pp = p.partials + (size_t)(2 * bb + k) * p.slot_floats;
-              const float sc = exp2f(__ldcg(pp + h) - M);
-              den += sc * __ldcg(pp + R + h);
-              num += sc * __ldcg(pp + 2 * R + h * D + d);
-            }
-            p.out[row_offset(p, u, h) + d] = den > 0.f ? num / den : 0.f;
-          }
+          merge_unit_partials<8>(p, u, T, P, st, TC_SMW * 32);
           if (st == 0) p.unit_tickets[unit_index(p, u)] = 0;
         }
         named_bar_sync(TBAR_SM, TC_SMW * 32);
@@ -729,10 +788,13 @@ static int tc_stages(int S) {
 
 bool attend_tc_supported(const Shape& sh, int c) {
   if (!(sh.bf16 && (sh.D == 64 || sh.D == 128) && c >= 2 && c * sh.G <= TC_ROWS)) return false;
+  // The softmax's waits on a stage's release assume that no stage is reused
+  // within two steps: at least 2 TC_KB + 1 stages.
   const bool rotk = !sh.stored_rotated;
+  constexpr int need = 2 * TC_KB + 1;
   if (sh.D == 128)
-    return rotk ? tc_stages<128, true>(sh.S) >= 4 : tc_stages<128, false>(sh.S) >= 4;
-  return rotk ? tc_stages<64, true>(sh.S) >= 4 : tc_stages<64, false>(sh.S) >= 4;
+    return rotk ? tc_stages<128, true>(sh.S) >= need : tc_stages<128, false>(sh.S) >= need;
+  return rotk ? tc_stages<64, true>(sh.S) >= need : tc_stages<64, false>(sh.S) >= need;
 }
 
 template <int D, bool ROTK, int STYLE>
