@@ -43,9 +43,11 @@ namespace rkv {
 
 namespace {
 
-constexpr int TC_SMW = 4;                       // softmax warps
+constexpr int TC_SMW = 4;                       // softmax warps of one group
+constexpr int TC_SMG = 2;                       // softmax groups (one stream of steps each)
 constexpr int TC_RW = 4;                        // staging (rotation) warps
-constexpr int W_SM0 = 1, W_MMA = 1 + TC_SMW, W_ROT0 = W_MMA + 1;
+constexpr int W_SM0 = 1, W_MMA = 1 + TC_SMG * TC_SMW, W_ROT0 = W_MMA + 1;
+constexpr int TC_SMT = TC_SMG * TC_SMW * 32;    // softmax threads
 constexpr int TC_THREADS = (W_ROT0 + TC_RW) * 32;
 constexpr int TC_MAX_STAGES = 12;
 constexpr int TC_ROWS = 128;                    // M of every product
@@ -53,15 +55,19 @@ constexpr int TBAR_PREFIX = 2;                  // named barrier: block prefix r
 constexpr int TBAR_SM = 3;                      // named barrier of the softmax warps
 constexpr float TC_TAU = 8.f;                   // lazy rescale threshold (log2 units)
 // A step of the softmax and of the products covers up to TC_KB key blocks
-// (128 keys): S = Q K^T of the step's blocks lands side by side in one S
+// (64 keys): S = Q K^T of the step's blocks lands side by side in one S
 // buffer, the softmax reads it in two passes (maximum, then P), and O += P V
-// takes the step's blocks one after the other.
-constexpr int TC_KB = 4;
+// takes the step's blocks one after the other.  Steps alternate between two
+// streams, each with its own S, P and O in tensor memory and its own group
+// of softmax warps (its own running maximum and sum), so that one group's
+// softmax overlaps the other's; the two are combined row by row at the end
+// of a segment.
+constexpr int TC_KB = 2;
 // Tensor memory columns: S[2] (f32, TC_KB * TK each), P[2] (bf16 pairs,
-// TC_KB * TK / 2 each), O (f32, D columns).
+// TC_KB * TK / 2 each), O[2] (f32, D columns each), one of each per stream.
 constexpr int TM_SW = TC_KB * TK, TM_PW = TC_KB * TK / 2;
 constexpr int TM_S = 0, TM_P = 2 * TM_SW, TM_O = TM_P + 2 * TM_PW, TM_COLS = 512;
-static_assert(TM_O + 128 <= TM_COLS, "tensor memory columns");
+static_assert(TM_O + 2 * 128 <= TM_COLS, "tensor memory columns");
 
 template <int D, bool ROTK>
 struct TcCfg : PipeCfg<D, ROTK> {
@@ -426,8 +432,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int ks = 0; ks < TK / 16; ++ks) {
             const uint64_t bd = sdesc(v_s + ks * 16 * 128, TK * 128, 1024);
-            tc_mma_ts(tmem + TM_O, tmem + TM_P + (tp & 1) * TM_PW + i * (TK / 2) + ks * 8, bd,
-                      id_pv, (first && i == 0 && ks == 0) ? 0 : 1);
+            tc_mma_ts(tmem + TM_O + (tp & 1) * D, tmem + TM_P + (tp & 1) * TM_PW + i * (TK / 2) +
+                      ks * 8, bd, id_pv, (first && i == 0 && ks == 0) ? 0 : 1);
           }
           tc_commit(smem_u32(empty + sp));
         }
@@ -437,8 +443,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int x1 = min(u.uend, re);
         if (!wait(qready, seg & 1)) break;
         tc_fence_after();
-        int pj = 0, pn = 0;   // the previous step's first block and block count
-        bool first = true;    // the segment's first product into O
+        int pj = 0, pn = 0;          // the previous step's first block and block count
+        bool first[2] = {true, true};   // each stream's first product into its O
         while (x < x1 && !dead) {
           const int nb = min(TC_KB, x1 - x), bs = t & 1;
           // The S buffer was read by the softmax of step t - 2.
@@ -460,8 +466,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (dead) break;
           tc_commit(smem_u32(sfull + bs));
           if (pn > 0) {
-            issue_pv(pj, pn, t - 1, first);
-            first = false;
+            issue_pv(pj, pn, t - 1, first[(t - 1) & 1]);
+            first[(t - 1) & 1] = false;
           }
           pj = jj;
           pn = nb;
@@ -470,7 +476,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           ++t;
         }
         if (dead) break;
-        if (pn > 0) issue_pv(pj, pn, t - 1, first);
+        if (pn > 0) issue_pv(pj, pn, t - 1, first[(t - 1) & 1]);
         if (dead) break;
         tc_commit(smem_u32(ofin));
         // The producer may go on with the next segment (its epilogue leaves
@@ -497,9 +503,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int q4 = warp & 3;                  // tensor-memory lane quarter
     const int row = 32 * q4 + lane;           // this thread's row of every tile
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
-    const int st = tid - 32 * W_SM0;          // 0..127
+    const int st = tid - 32 * W_SM0;          // 0 .. TC_SMT - 1
+    const int grp = st / (TC_SMW * 32);       // the stream of steps this warp takes
     const bool warp_rows = 32 * q4 < R;       // the warp holds real rows
-    zero_empty_units_cached(p, sa, sfill, st, TC_SMW * 32);
+    zero_empty_units_cached(p, sa, sfill, st, TC_SMT);
     int jj = 0, t = 0, seg = 0;   // blocks and steps over the CTA, segments
     int jl1 = -1, jl2 = -1;       // the last blocks of the two previous steps
     bool dead = false;
@@ -523,7 +530,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       // (plus the lag of stored-rotated keys that follow a re-basing epoch);
       // rows >= R are zero.  Eight rotary pairs per pass: split-half pairs
       // (i, i + D/2) from two 16-byte chunks, interleaved ones from one.
-      {
+      // The first group stages it.
+      if (grp == 0) {
         const size_t qo = row < R ? row_offset(p, u, row) : 0;
         const float2* t = p.table + (size_t)(row < R ? rq + slag[u.s] : 0) * HALF;
         auto load8 = [&](int d0, float (&v)[8]) {
@@ -580,14 +588,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             store8(d0, xv);
           }
         }
+        // The tensor cores read the Q tile through the async proxy.
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(qready));
       }
-      // The tensor cores read the Q tile through the async proxy.
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(qready));
 
       float m = NEG_BIG, l = 0.f;
       const int t0 = t;
+      int nmine = 0;   // this group's steps in the segment
       BlockWalk wk;
       wk.init(x, u, p.sh);
       const int Wg = p.sh.Wring;
@@ -626,8 +635,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           jl2 = jl1;
           jl1 = jl;
         };
+        if (bs != grp) { next(); continue; }   // the other stream's step
+        ++nmine;
         if (!waited(sfull + bs, (t >> 1) & 1)) { next(); continue; }
         tc_fence_after();
+        // A warp without real rows only keeps step with its group (its
+        // arrivals below); its lanes of S, P and O are never used.
+        if (warp_rows) {
         // Pass 1: the step's maximum.
         float bm = -INFINITY;
         {
@@ -639,43 +653,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             float sv[32];
             load_s(TM_S + bs * TM_SW + i * TK, sr);
             scores(w.g, sr, sv);
-            float mx[16];
+            float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-            for (int d = 0; d < 16; ++d) mx[d] = fmaxf(sv[d], sv[d + 16]);
-#pragma unroll
-            for (int k = 8; k >= 1; k >>= 1)
-#pragma unroll
-              for (int d = 0; d < k; ++d) mx[d] = fmaxf(mx[d], mx[d + k]);
-            bm = fmaxf(bm, mx[0]);
+            for (int d = 4; d < 32; ++d) mx[d & 3] = fmaxf(mx[d & 3], sv[d]);
+            bm = fmaxf(bm, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
           }
         }
-        // Lazy rescale: the running maximum moves only when a score exceeds
-        // it by more than TC_TAU; O and l are then rescaled.  O is quiet once
-        // the previous step's products have completed (the commit after its
-        // last block).
-        const bool grow = bm > m + TC_TAU;
-        const float mnew = grow ? bm : m;
-        if (__any_sync(0xffffffffu, grow && t > t0)) {
-          if (!waited(empty + (jj - 1) % NS, ((jj - 1) / NS) & 1)) { next(); continue; }
-          tc_fence_after();
-          const float sc = ex2(m - mnew);
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 16) {
-            uint32_t ov[16];
-            tc_ld16(tmem + lane_addr + TM_O + c0, ov);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * sc);
-            tc_st16(tmem + lane_addr + TM_O + c0, ov);
-          }
-        }
-        if (grow) l *= ex2(m - mnew);
-        m = mnew;
-        // The P buffer was last read by the products of step t - 2: wait for
-        // the commit after its last block.
+        // This stream's previous step (t - 2): its products read the P buffer
+        // and wrote O; both are quiet once the commit after its last block
+        // has completed.
         if (t >= 2) {
           if (!waited(empty + jl2 % NS, (jl2 / NS) & 1)) { next(); continue; }
           tc_fence_after();
         }
+        // Lazy rescale: the running maximum moves only when a score exceeds
+        // it by more than TC_TAU; O and l are then rescaled (O holds products
+        // of this segment once the stream had a step in it before).
+        const bool grow = bm > m + TC_TAU;
+        const float mnew = grow ? bm : m;
+        if (__any_sync(0xffffffffu, grow && t >= t0 + 2)) {
+          const float sc = ex2(m - mnew);
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t ov[16];
+            tc_ld16(tmem + lane_addr + TM_O + bs * D + c0, ov);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * sc);
+            tc_st16(tmem + lane_addr + TM_O + bs * D + c0, ov);
+          }
+        }
+        if (grow) l *= ex2(m - mnew);
+        m = mnew;
         // Pass 2: P = 2^(s - m) (masked scores give 2^-inf = 0; m is always
         // finite), rounded to bf16, two per column of the P buffer.
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
@@ -696,10 +704,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               ps[(d >> 1) & 3] += p0 + p1;
               pw[d >> 1] = pack_bf2(p0, p1);
             }
-            if (warp_rows) tc_st16(tmem + lane_addr + TM_P + bs * TM_PW + i * (TK / 2), pw);
+            tc_st16(tmem + lane_addr + TM_P + bs * TM_PW + i * (TK / 2), pw);
           }
         }
         l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -708,48 +717,75 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         next();
       }
-      // ---- segment end: O row from tensor memory, then the unit's output ----
-      if (waited(ofin, seg & 1)) {
-        tc_fence_after();
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t ov[32];
-          if (warp_rows) tc_ld32(tmem + lane_addr + TM_O + c0, ov);
+      // ---- segment end: the two streams' rows combined, then the output ----
+      // Each group publishes (m, l, steps) of its rows (in the Q tile, idle
+      // until the next segment's), then group g writes columns
+      // [g D/2, (g + 1) D/2) of every row:
+      //   O = w_a O_a + w_b O_b,  l = w_a l_a + w_b l_b,  w = 2^(m - M),
+      // M = max(m_a, m_b), a stream without steps in the segment left out.
+      const bool fin = waited(ofin, seg & 1);
+      tc_fence_after();
+      float* xch = reinterpret_cast<float*>(qt);   // [2][3][128]
+      xch[grp * 384 + row] = m;
+      xch[grp * 384 + 128 + row] = l;
+      xch[grp * 384 + 256 + row] = static_cast<float>(nmine);
+      named_bar_sync(TBAR_SM, TC_SMT);
+      if (fin) {
+        const float ma = xch[row], la = xch[128 + row];
+        const float mb = xch[384 + row], lb = xch[512 + row];
+        const bool ha = xch[256 + row] > 0.f, hb = xch[640 + row] > 0.f;
+        const float M = ha && hb ? fmaxf(ma, mb) : (ha ? ma : mb);
+        const float wa = ha ? ex2(ma - M) : 0.f, wb = hb ? ex2(mb - M) : 0.f;
+        const float L = wa * la + wb * lb;
+        constexpr int DH = D / 2;
+#pragma unroll 1
+        for (int c0 = grp * DH; c0 < (grp + 1) * DH; c0 += 16) {
+          uint32_t oa[16], ob[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) oa[i] = ob[i] = 0u;
+          if (warp_rows && ha) tc_ld16(tmem + lane_addr + TM_O + c0, oa);
+          if (warp_rows && hb) tc_ld16(tmem + lane_addr + TM_O + D + c0, ob);
+          float ov[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            ov[i] = (ha ? wa * __uint_as_float(oa[i]) : 0.f) +
+                    (hb ? wb * __uint_as_float(ob[i]) : 0.f);
           if (row < R) {
             if (whole) {
-              const float inv = l > 0.f ? 1.f / l : 0.f;
+              const float inv = L > 0.f ? 1.f / L : 0.f;
               float* o = p.out + row_offset(p, u, row) + c0;
 #pragma unroll
-              for (int i = 0; i < 32; i += 4)
+              for (int i = 0; i < 16; i += 4)
                 *reinterpret_cast<float4*>(o + i) =
-                    make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
-                                __uint_as_float(ov[i + 2]) * inv,
-                                __uint_as_float(ov[i + 3]) * inv);
+                    make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv, ov[i + 3] * inv);
             } else {
               // Split unit: this CTA's partial (m, l, unnormalised O) of the row.
               float* pp = p.partials + (size_t)(2 * b + kslot) * p.slot_floats;
-              if (c0 == 0) { pp[row] = m; pp[R + row] = l; }
+              if (c0 == 0) { pp[row] = M; pp[R + row] = L; }
 #pragma unroll
-              for (int i = 0; i < 32; ++i) pp[2 * R + row * D + c0 + i] = __uint_as_float(ov[i]);
+              for (int i = 0; i < 16; ++i) pp[2 * R + row * D + c0 + i] = ov[i];
             }
           }
         }
         tc_fence_before();
       }
+      // The exchange area is the next segment's Q tile.
+      named_bar_sync(TBAR_SM, TC_SMT);
       if (!whole) {
         // The last CTA of the unit to take its ticket merges the partials.
-        named_bar_sync(TBAR_SM, TC_SMW * 32);
+        named_bar_sync(TBAR_SM, TC_SMT);
         if (st == 0) {
           __threadfence();
           flag[0] = atomicAdd(&p.unit_tickets[unit_index(p, u)], 1);
           __threadfence();
         }
-        named_bar_sync(TBAR_SM, TC_SMW * 32);
+        named_bar_sync(TBAR_SM, TC_SMT);
         const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
         if (flag[0] == b1 - b0) {
-          merge_unit_partials<8>(p, u, T, P, st, TC_SMW * 32);
+          merge_unit_partials<8>(p, u, T, P, st, TC_SMT);
           if (st == 0) p.unit_tickets[unit_index(p, u)] = 0;
         }
-        named_bar_sync(TBAR_SM, TC_SMW * 32);
+        named_bar_sync(TBAR_SM, TC_SMT);
       }
       x = x1;
     }
@@ -788,10 +824,11 @@ static int tc_stages(int S) {
 
 bool attend_tc_supported(const Shape& sh, int c) {
   if (!(sh.bf16 && (sh.D == 64 || sh.D == 128) && c >= 2 && c * sh.G <= TC_ROWS)) return false;
-  // The softmax's waits on a stage's release assume that no stage is reused
-  // within two steps: at least 2 TC_KB + 1 stages.
+  // A softmax group waits on the release of its previous step's last stage;
+  // that stage must not be reused by the next three steps (the other
+  // stream's step may complete meanwhile): at least 3 TC_KB + 1 stages.
   const bool rotk = !sh.stored_rotated;
-  constexpr int need = 2 * TC_KB + 1;
+  constexpr int need = 3 * TC_KB + 1;
   if (sh.D == 128)
     return rotk ? tc_stages<128, true>(sh.S) >= need : tc_stages<128, false>(sh.S) >= need;
   return rotk ? tc_stages<64, true>(sh.S) >= need : tc_stages<64, false>(sh.S) >= need;
