@@ -367,9 +367,13 @@ def run_gpu(args, rank, world):
     return res
 
 
-def chunk_on_tc(attend_impl):
-    """Whether chunks (c >= 2) run on the tcgen05 kernel for this attend_impl."""
-    return attend_impl == "tc"
+TC_AUTO_MIN_ROWS = 32   # the library's choice under "auto": chunks of c*G >= 32 rows
+
+
+def chunk_on_tc(attend_impl, rows):
+    """Whether a chunk of `rows` = c*G query rows per KV head runs on the
+    tcgen05 kernel for this attend_impl (the library's own rule)."""
+    return attend_impl == "tc" or (attend_impl == "auto" and rows >= TC_AUTO_MIN_ROWS)
 
 
 def step_is_fused(wl, layout, epoch, args):
@@ -640,7 +644,8 @@ def main():
     else:
         kernel_key = "attend_fma" if args.attend_impl == "fma" or wl.kv_dtype != "bf16" else \
             ("attend_mma" if wl.n_new == 1 else
-             "attend_tc_chunk" if chunk_on_tc(args.attend_impl) else "attend_mma_chunk")
+             "attend_tc_chunk" if chunk_on_tc(args.attend_impl, wl.n_new * wl.n_q_heads // wl.n_kv_heads)
+             else "attend_mma_chunk")
         scope = ("the step's launches: rkv_append, then the attention launched with "
                  "programmatic dependent launch (its prologue overlaps the append); the "
                  "attention's own share of the device time is in the committed launch list")
@@ -676,12 +681,15 @@ def main():
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
                      "kernel": kernel_key, "traffic": _traffic(kernel_key),
                      "kernel_us": kern_us, "kernel_scope": scope},
-        "e2e": {"value": all_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                "us_per_step": e2e_ms * 1e3, "us_per_step_mean": res["e2e"]["ms_mean"] * 1e3,
-                "steps": res["e2e"]["steps"], "statistic": "median of per-step events",
-                "l2": "cold, as the main loop (flush between steps, outside the events)",
-                "h2d_bytes_per_step": res["e2e"]["h2d"],
-                "d2h_bytes_per_step": res["e2e"]["d2h"]},
+        "e2e": ({"value": all_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                 "us_per_step": e2e_ms * 1e3, "us_per_step_mean": res["e2e"]["ms_mean"] * 1e3,
+                 "steps": res["e2e"]["steps"], "statistic": "median of per-step events",
+                 "l2": "cold, as the main loop (flush between steps, outside the events)",
+                 "h2d_bytes_per_step": res["e2e"]["h2d"],
+                 "d2h_bytes_per_step": res["e2e"]["d2h"]}
+                if res["e2e"]["steps"] else
+                {"value": None, "unit": "GB/s", "skipped": "--no-e2e",
+                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}),
         "gpu_launches": res["launches"],
         **({"rerotations_in_timed_region": res["rerotations"]}
            if res["rerotations"] is not None else {}),

@@ -51,19 +51,27 @@ inline int attend_grid(const rkv_handle* h, int n_layers) {
   return sms;
 }
 
+// Chunks of at least this many rows (c*G) run on tcgen05 under RKV_ATTEND_AUTO:
+// below it most of the 128-row tile is padding and the mma.sync kernel wins
+// (measured on B300: 6 x 8 rows 113 us against 130 us; 4 x 1 rows 145 us
+// against 98 us).
+constexpr int kTcAutoMinRows = 32;
+
 // Picks and launches the attention kernel for p.c queries per stream: the
 // tensor-core kernels for bf16 caches (single query on mma.sync; a chunk on
-// tcgen05 with RKV_ATTEND_TC, else on mma.sync for c*G <= 96 rows) unless the
-// handle asks for the CUDA-core kernel, which serves f32 caches and c*G <= 16.
+// tcgen05 with RKV_ATTEND_TC, or with RKV_ATTEND_AUTO from kTcAutoMinRows
+// rows, else on mma.sync for c*G <= 96 rows) unless the handle asks for the
+// CUDA-core kernel, which serves f32 caches and c*G <= 16.
 // RKV_ERR_UNSUPPORTED when no kernel takes the call.
 inline rkv_status launch_attend_any(const rkv_handle* h, const AttendParams& p, int grid,
                                     cudaStream_t s) {
   const bool tc = h->cfg.attend_impl != RKV_ATTEND_FMA && h->has_map4;
+  const bool want_tc = h->cfg.attend_impl == RKV_ATTEND_TC ||
+                       (h->cfg.attend_impl == RKV_ATTEND_AUTO && p.R >= kTcAutoMinRows);
   cudaError_t e;
   if (tc && p.c == 1 && attend_mma_supported(h->sh, 1)) {
     e = launch_attend_mma(p, h->tmK4, h->tmV4, grid, s);
-  } else if (h->cfg.attend_impl == RKV_ATTEND_TC && h->has_map4 && p.c > 1 &&
-             attend_tc_supported(h->sh, p.c)) {
+  } else if (want_tc && h->has_map4 && p.c > 1 && attend_tc_supported(h->sh, p.c)) {
     e = launch_attend_tc(p, h->tmK4, h->tmV4, grid, s);
   } else if (tc && p.c > 1 && attend_chunk_supported(h->sh, p.c)) {
     e = launch_attend_chunk(p, h->tmK4, h->tmV4, grid, s);
