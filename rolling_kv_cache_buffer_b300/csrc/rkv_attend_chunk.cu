@@ -547,7 +547,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         named_bar_sync(CBAR_CONS, CCONS);
         const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
         if (flag[0] == b1 - b0) {
-          merge_unit_partials<16>(p, u, T, P, ct, CCONS);
+          merge_unit_partials<16>(p, u, T, P, ct, CCONS, slots, CCW * SLOT,
+                                  [] { named_bar_sync(CBAR_CONS, CCONS); });
           if (ct == 0) p.unit_tickets[unit_index(p, u)] = 0;
         }
       }

@@ -287,24 +287,81 @@ __device__ __forceinline__ void zero_empty_units_cached(const AttendParams& p, c
   }
 }
 
-// The last CTA of a split unit combines the unit's partials (m, l and the
+// The last CTA of a split unit combines the unit's np partials (m, l and the
 // unnormalised O of each row, one slot per CTA segment) into its output:
-//   out = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k,   M = max_k m_k.
-// Thread t of nt takes elements t, t + nt, ... Q at a time, so that the loads
-// of one pass over the partials are independent of one another (a few L2
-// round trips in all, not two per element).
-template <int Q>
+//   out = sum_k w_k O_k,  w_k = 2^(m_k - M) / sum_j 2^(m_j - M) l_j,  M = max_k m_k.
+// The np x R weights go to shared scratch `scr` first (one load of every m and
+// l, all in flight together); then thread t of nt sums Q output elements at a
+// time, eight partials per pass, so that 8 Q loads are in flight.  Every thread
+// of the nt calls it; `sync` synchronises them.  Scratch of 2 np R + 2 R
+// floats; with less, the weights are recomputed per element instead.  With
+// `store` false nothing but the scratch is written (a dry run that brings the
+// code into the instruction caches).
+template <int Q, typename Sync>
 __device__ __forceinline__ void merge_unit_partials(const AttendParams& p, const UnitRef& u,
-                                                    int T, int P, int t, int nt) {
+                                                    int T, int P, int t, int nt, float* scr,
+                                                    int scr_floats, Sync sync,
+                                                    bool store = true) {
   const int R = p.R, D = p.sh.D, RD = R * D;
-  const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
+  const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P), np = b1 - b0 + 1;
   const int rs0 = range_start(b0, T, P);
   // CTA b0 holds the unit in its second slot when its range starts before it.
   const float* first =
       p.partials + (size_t)(2 * b0 + (rs0 < u.ustart ? 1 : 0)) * p.slot_floats;
-  auto part = [&](int b) {
-    return b == b0 ? first : p.partials + (size_t)(2 * b) * p.slot_floats;
+  auto part = [&](int k) {
+    return k == 0 ? first : p.partials + (size_t)(2 * (b0 + k)) * p.slot_floats;
   };
+  if (2 * np * R + 2 * R <= scr_floats) {
+    float* wm = scr;                 // [np][R]: m, then the weight
+    float* wl = scr + np * R;        // [np][R]: l
+    float* rowM = wl + np * R;       // [R]: M
+    float* rowI = rowM + R;          // [R]: 1 / sum_j 2^(m_j - M) l_j
+    for (int i = t; i < np * R; i += nt) {
+      const int k = i / R, h = i - k * R;
+      wm[i] = __ldcg(part(k) + h);
+      wl[i] = __ldcg(part(k) + R + h);
+    }
+    sync();
+    for (int h = t; h < R; h += nt) {
+      float M = NEG_BIG;
+      for (int k = 0; k < np; ++k) M = fmaxf(M, wm[k * R + h]);
+      float den = 0.f;
+      for (int k = 0; k < np; ++k) den += exp2f(wm[k * R + h] - M) * wl[k * R + h];
+      rowM[h] = M;
+      rowI[h] = den > 0.f ? 1.f / den : 0.f;
+    }
+    sync();
+    for (int i = t; i < np * R; i += nt) {
+      const int h = i % R;
+      wm[i] = exp2f(wm[i] - rowM[h]) * rowI[h];
+    }
+    sync();
+    for (int i0 = t; i0 < RD; i0 += Q * nt) {
+      float acc[Q];
+      int h[Q], e[Q];
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        e[q] = min(i0 + q * nt, RD - 1);
+        h[q] = e[q] / D;
+        acc[q] = 0.f;
+      }
+      for (int k0 = 0; k0 < np; k0 += 8) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int k = k0 + kk < np ? k0 + kk : np - 1;
+          const float on = k0 + kk < np ? 1.f : 0.f;
+          const float* pp = part(k) + 2 * R;
+#pragma unroll
+          for (int q = 0; q < Q; ++q) acc[q] += on * wm[k * R + h[q]] * __ldcg(pp + e[q]);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < Q; ++q)
+        if (store && i0 + q * nt < RD)
+          p.out[row_offset(p, u, h[q]) + (e[q] - h[q] * D)] = acc[q];
+    }
+    return;
+  }
   for (int i0 = t; i0 < RD; i0 += Q * nt) {
     float M[Q], num[Q], den[Q];
     int h[Q];
@@ -316,14 +373,14 @@ __device__ __forceinline__ void merge_unit_partials(const AttendParams& p, const
       den[q] = 0.f;
     }
 #pragma unroll 4
-    for (int b = b0; b <= b1; ++b) {
-      const float* pp = part(b);
+    for (int k = 0; k < np; ++k) {
+      const float* pp = part(k);
 #pragma unroll
       for (int q = 0; q < Q; ++q) M[q] = fmaxf(M[q], __ldcg(pp + h[q]));
     }
 #pragma unroll 2
-    for (int b = b0; b <= b1; ++b) {
-      const float* pp = part(b);
+    for (int k = 0; k < np; ++k) {
+      const float* pp = part(k);
 #pragma unroll
       for (int q = 0; q < Q; ++q) {
         const int e = min(i0 + q * nt, RD - 1);
@@ -335,7 +392,7 @@ __device__ __forceinline__ void merge_unit_partials(const AttendParams& p, const
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
       const int e = i0 + q * nt;
-      if (e < RD)
+      if (store && e < RD)
         p.out[row_offset(p, u, h[q]) + (e - h[q] * D)] = den[q] > 0.f ? num[q] / den[q] : 0.f;
     }
   }
@@ -390,7 +447,8 @@ __device__ __forceinline__ void finish_segment(const AttendParams& p, const Unit
   const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
   if (*flag != b1 - b0) return;  // another CTA finishes this unit
   __threadfence();
-  merge_unit_partials<16>(p, u, T, P, threadIdx.x, nthr);
+  merge_unit_partials<16>(p, u, T, P, threadIdx.x, nthr, const_cast<float*>(mrg),
+                          NWARP * wstride, [] { __syncthreads(); });
   if (threadIdx.x == 0) p.unit_tickets[unit_index(p, u)] = 0;
 }
 

@@ -70,6 +70,8 @@ constexpr int BAR_PREFIX = 2;                 // the producer warp's block prefi
 
 constexpr int TKH = TK / 2;     // keys of a block each warp of a pair takes
 constexpr int NPAIR = NCW / 2;  // consumer warp pairs
+// Fewest blocks in a CTA's share for the dry run of the merge to pay off.
+constexpr int DRY_MIN_BLOCKS = 32;
 static_assert(NCW % 2 == 0, "consumer warps come in pairs");
 
 template <int D, bool ROTK>
@@ -510,8 +512,10 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
     // producer is filling, nor outputs, partials, tickets, the partner CTA or
     // the merge-done barrier), while the first tiles are still on their way.
     // It brings the merge's code into the instruction caches, so that the
-    // real merge at the end of the stream does not fetch it from memory.
-    bool dry = rb < re;
+    // real merge at the end of the stream does not fetch it from memory.  A
+    // short share (a launch over one layer) has no time to hide it: there the
+    // merge code is fetched when it runs.
+    bool dry = re - rb >= DRY_MIN_BLOCKS;
 #pragma unroll 1
     for (int x = rb; x < re;) {
       const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
@@ -952,20 +956,24 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
           }
         }
       }
-      if (!whole && !CL && !dry) {
+      if (!whole && !CL) {
         // Publish this CTA's partial (one release by one thread after the
-        // barrier); the last CTA of the unit to arrive merges them all.
-        named_bar_sync(BAR_CONS, CONS_THREADS);
-        if (ct == 0) {
-          __threadfence();
-          flag[0] = atomicAdd(&p.unit_tickets[unit_index(p, u)], 1);
-          __threadfence();
-        }
-        named_bar_sync(BAR_CONS, CONS_THREADS);
-        const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
-        if (flag[0] == b1 - b0) {
-          merge_unit_partials<8>(p, u, T, P, ct, CONS_THREADS);
-          if (ct == 0) p.unit_tickets[unit_index(p, u)] = 0;
+        // barrier); the last CTA of the unit to arrive merges them all, with
+        // the raw-query area (free by now) as scratch.
+        if (!dry) {
+          named_bar_sync(BAR_CONS, CONS_THREADS);
+          if (ct == 0) {
+            __threadfence();
+            flag[0] = atomicAdd(&p.unit_tickets[unit_index(p, u)], 1);
+            __threadfence();
+          }
+          named_bar_sync(BAR_CONS, CONS_THREADS);
+          const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
+          if (flag[0] == b1 - b0) {
+            merge_unit_partials<4>(p, u, T, P, ct, CONS_THREADS, reinterpret_cast<float*>(qraw),
+                                   8 * D, [] { named_bar_sync(BAR_CONS, CONS_THREADS); });
+            if (ct == 0) p.unit_tickets[unit_index(p, u)] = 0;
+          }
         }
       }
       // The slots' generic-proxy accesses come before the producer's next

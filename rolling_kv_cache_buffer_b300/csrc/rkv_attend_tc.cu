@@ -782,7 +782,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         named_bar_sync(TBAR_SM, TC_SMT);
         const int b0 = cta_of(u.ustart, T, P), b1 = cta_of(u.uend - 1, T, P);
         if (flag[0] == b1 - b0) {
-          merge_unit_partials<8>(p, u, T, P, st, TC_SMT);
+          merge_unit_partials<8>(p, u, T, P, st, TC_SMT, reinterpret_cast<float*>(qt),
+                                 C::QT / 4, [] { named_bar_sync(TBAR_SM, TC_SMT); });
           if (st == 0) p.unit_tickets[unit_index(p, u)] = 0;
         }
         named_bar_sync(TBAR_SM, TC_SMT);
