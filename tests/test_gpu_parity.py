@@ -12,8 +12,9 @@ import torch
 
 from oracle import rkv_oracle as O
 from rkv_inputs import WORKLOADS, initial_window, random_rows, step_inputs
-from tests.gpu_util import (compare, dev, make_cache, make_oracle, poison_outside,
-                            write_window)
+from rolling_kv_cache_buffer_b300 import RollingKV
+from tests.gpu_util import (MAX_ABS, MEAN_ABS, compare, dev, make_cache, make_oracle,
+                            poison_outside, write_window)
 
 pytestmark = pytest.mark.gpu
 
@@ -442,6 +443,69 @@ def test_reset_stream_with_prefix(layout):
     assert (int(o[1]), int(f[1]), int(st[1])) == (5, 0, 0)
     out, ref = step(71)
     compare(out, ref)
+
+
+@pytest.mark.parametrize("wl_name,layout,style,epoch", [
+    ("qwen3b", "stored_rotated", "split_half", 16),
+    ("qwen3b", "pre_rope", "interleaved", 0),
+    ("qwen3b", "stored_rotated", "interleaved", 0),
+    ("tiny", "pre_rope", "split_half", 0),
+    ("tiny", "stored_rotated", "interleaved", 0)])
+def test_reset_stream_with_prefix_variants(wl_name, layout, style, epoch):
+    """The utterance reset on the paths the base case does not take: stored-
+    rotated keys with a re-basing epoch (the reset clears the lag and stores the
+    prefix keys rotated to their positions from the new origin), the
+    interleaved pairing (both layouts) and float32 pools (the CUDA-core path).
+    Stream 1 restarts with a prefix, then appends run until the prefix is
+    evicted; every few steps the outputs are compared with the oracle whose
+    window was set to the same prefix."""
+    base = WORKLOADS[wl_name]
+    wl = base.replace(n_streams=2, n_layers=min(base.n_layers, 2),
+                      capacity=min(base.capacity, 64))
+    f32 = wl.kv_dtype == "f32"
+    dt = torch.float32 if f32 else torch.bfloat16
+    stored = layout == "stored_rotated"
+    cache = RollingKV(2, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.capacity,
+                      max_chunk=1, kv_dtype=wl.kv_dtype, layout=layout, rope_style=style,
+                      rope_theta=wl.rope_theta, rebase_epoch=epoch)
+    args = (2, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.capacity)
+    if epoch:
+        orc = O.EpochRotatedOracle(*args, theta=wl.rope_theta, style=style, epoch=epoch)
+    elif stored and not f32:
+        orc = O.StoredRotatedOracle(*args, theta=wl.rope_theta, style=style)
+    else:   # float32 keys are kept exact enough for the plain definition
+        orc = O.RollingCacheOracle(*args, theta=wl.rope_theta, style=style)
+    tol = (1e-4, 1e-5) if f32 else (MAX_ABS, MEAN_ABS)
+    rebase_oracle = hasattr(orc, "rebase") and (epoch or (stored and not f32))
+
+    def step(t):
+        q, k, v = step_inputs(wl, t)
+        cache.append(dev(k, dt), dev(v, dt))
+        orc.append(k.double().numpy(), v.double().numpy())
+        if stored:
+            cache.rebase()
+            if rebase_oracle:
+                orc.rebase()
+        return cache.attend(dev(q, dt)), orc.attend(q.double().numpy())
+
+    for t in range(1, 11):
+        step(t)
+    n, origin = 12, 424_242
+    D, Hkv = wl.head_dim, wl.n_kv_heads
+    kp = random_rows((wl.n_layers, n, Hkv, D), 31, dt)
+    vp = random_rows((wl.n_layers, n, Hkv, D), 32, dt)
+    cache.reset_stream(1, origin, dev(kp, dt), dev(vp, dt))
+    orc.set_state(1, origin, n, kp.permute(0, 2, 1, 3).double().numpy(),
+                  vp.permute(0, 2, 1, 3).double().numpy())
+    o, f, st = cache.get_stream_state()
+    assert (int(o[1]), int(f[1]), int(st[1])) == (origin, n, 0)
+    W = wl.capacity
+    for t in range(11, 11 + W + 16):   # past the fill and the prefix's eviction
+        out, ref = step(t)
+        if t % 5 == 0 or t > W + 20:
+            compare(out, ref, *tol)
+    o, f, st = cache.get_stream_state()
+    assert (int(o[1]), int(f[1]), int(st[1])) == (origin + n + W + 16 - W, W, 0)
 
 
 # ----------------------------------------------------------------------------
