@@ -50,7 +50,7 @@
 #include "rkv_rows.cuh"
 
 #ifndef RKV_MMA_NCW
-#define RKV_MMA_NCW 8
+#define RKV_MMA_NCW 10
 #endif
 
 namespace rkv {
@@ -105,7 +105,7 @@ __host__ __device__ constexpr size_t mma_smem_bytes(int stage, int fixed, int ns
 // warps: per consumer thread, m and l of its head and its 4 (D/16) / NCW
 // output elements (see the segment end), stored element-major.
 template <int D>
-constexpr int rx_per_thread() { return 2 + (4 * (D / 16)) / NCW; }
+constexpr int rx_per_thread() { return 2 + (4 * (D / 16) + NCW - 1) / NCW; }
 template <int D>
 constexpr int rx_floats() { return rx_per_thread<D>() * CONS_THREADS; }
 
@@ -880,7 +880,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
       {
         // Thread ct takes fragment elements i = ct/32, ct/32 + NCW, ... of lane
         // lf: head h = 2(lf & 3) + (i & 1) is the same for all of them.
-        constexpr int NE = C::FR / NCW;       // output elements per thread
+        constexpr int NE = (C::FR + NCW - 1) / NCW;   // output elements per thread (at most)
         const int lf = ct & 31, i0 = ct >> 5;
         const int h = 2 * (lf & 3) + (i0 & 1);
         float M = NEG_BIG;
@@ -894,13 +894,17 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
         }
         float v[NE];
         int dd[NE];
+        bool ok[NE];   // element i0 + k NCW exists (NCW need not divide FR)
 #pragma unroll
         for (int k = 0; k < NE; ++k) {
           const int i = i0 + k * NCW;
-          dd[k] = 16 * (i >> 2) + (lf >> 2) + (((i >> 1) & 1) << 3);
+          ok[k] = i < C::FR;
+          dd[k] = ok[k] ? 16 * (i >> 2) + (lf >> 2) + (((i >> 1) & 1) << 3) : 0;
           float a = 0.f;
+          if (ok[k]) {
 #pragma unroll
-          for (int w = 0; w < NCW; ++w) a += sc[w] * slots[w * C::SLOT + 16 + 32 * i + lf];
+            for (int w = 0; w < NCW; ++w) a += sc[w] * slots[w * C::SLOT + 16 + 32 * i + lf];
+          }
           v[k] = a;
         }
         if (ship && !dry) {
@@ -946,12 +950,14 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
               const float inv = L > 0.f ? 1.f / L : 0.f;
               float* out = p.out + row_offset(p, u, h);
 #pragma unroll
-              for (int k = 0; k < NE; ++k) out[dd[k]] = v[k] * inv;
+              for (int k = 0; k < NE; ++k)
+                if (ok[k]) out[dd[k]] = v[k] * inv;
             } else {
               float* part = p.partials + (size_t)(2 * b + (x == rb ? 0 : 1)) * p.slot_floats;
               if (lf < 4 && i0 < 2) { part[h] = M; part[R + h] = L; }
 #pragma unroll
-              for (int k = 0; k < NE; ++k) part[2 * R + h * D + dd[k]] = v[k];
+              for (int k = 0; k < NE; ++k)
+                if (ok[k]) part[2 * R + h * D + dd[k]] = v[k];
             }
           }
         }
