@@ -67,6 +67,7 @@ constexpr int mma_threads() { return (1 + NCW + (FUSED ? 1 : 0)) * 32; }
 constexpr int MMA_MAX_STAGES = 16;
 constexpr int BAR_CONS = 1;                   // named barrier of the consumer warps
 constexpr int BAR_PREFIX = 2;                 // the producer warp's block prefix is ready
+constexpr int BAR_SIDE = 3;                   // the side warp's own barrier in its dry pass
 
 constexpr int TKH = TK / 2;     // keys of a block each warp of a pair takes
 constexpr int NPAIR = NCW / 2;  // consumer warp pairs
@@ -426,16 +427,18 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
                                           sfill, rb, re, abort_flag);
     __syncwarp();
     if constexpr (CL) cluster_wait();
-  } else if (FUSED && warp == NCW + 1) {
-    // ------------------------------------------------------------------ side warp
-    // The step's new pairs into their slots (every unit once over the grid),
-    // then, on the step's last launch, the new stream states.
-    step_prepass<D, !ROTK>(p, sa, sfill, slag, 0, 1, lane);
-    if (p.publish) step_publish(p, lane);
-    if constexpr (CL) cluster_wait();
   } else {
     // ------------------------------------------------------------------ consumers
+    // In a fused step the side warp (warp NCW + 1) runs this code too, as a
+    // dry pass only: one block body and the segment end, with nothing written
+    // but its own scratch and its own barrier instead of the consumers' --
+    // so that the consumers find that code in the instruction caches and need
+    // no dry pass of their own -- and then does its own work (below).
+    const bool side = FUSED && warp == NCW + 1;
     const int cw = warp - 1, ct = tid - 32;
+    auto cbar = [&]() {
+      named_bar_sync(side ? BAR_SIDE : BAR_CONS, side ? 32 : CONS_THREADS);
+    };
     const int g = lane >> 2, cq = lane & 3;   // mma fragment coordinates
     // A unit's query rows (and, in a fused step, its new pair) reach shared
     // memory in two steps: `stage_unit` issues 16-byte asynchronous copies of the
@@ -488,15 +491,17 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
         widen(nraw + (size_t)i * 16, kvn + kv * D + c * (16 / kesz), p.sh.bf16);
       }
     };
-    for (int i = ct; i < (8 - G) * D; i += CONS_THREADS)
-      qs[(G + i / D) * QSTR + i % D] = 0.f;
-    if (rb < re) stage_unit(unit_of_cached(rb, p, pre, sa, sfill));
-    if constexpr (!FUSED) zero_empty_units_cached(p, sa, sfill, ct, CONS_THREADS);
-    if (rb < re) {
-      unstage_q();
-      if constexpr (FUSED) unstage_new();
+    if (!side) {
+      for (int i = ct; i < (8 - G) * D; i += CONS_THREADS)
+        qs[(G + i / D) * QSTR + i % D] = 0.f;
+      if (rb < re) stage_unit(unit_of_cached(rb, p, pre, sa, sfill));
+      if constexpr (!FUSED) zero_empty_units_cached(p, sa, sfill, ct, CONS_THREADS);
+      if (rb < re) {
+        unstage_q();
+        if constexpr (FUSED) unstage_new();
+      }
     }
-    named_bar_sync(BAR_CONS, CONS_THREADS);
+    cbar();
     if constexpr (CL) cluster_wait();   // long after both CTAs arrived
     // Dims of the thread's A-fragment elements: k-block kb, j in {0,1,2,3}:
     //   dim 16kb + (j>>1)*8 + 2cq + (j&1)
@@ -505,7 +510,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
     // Warp pair pi takes blocks pi, pi + NPAIR, ...; warp hh of the pair takes
     // keys 16*hh .. 16*hh+15 of each.
     const int pi = cw >> 1, hh = cw & 1;
-    int jb = pi, stage = pi, round = 0;   // the pair's next block and its stage (NS >= NPAIR)
+    int jb = pi, stage = side ? 0 : pi, round = 0;   // the pair's next block and its stage (NS >= NPAIR)
     bool dead = false;
     // The first pass through the loop is a dry run of the segment end: no
     // block, nothing written (neither the slots, which alias the stages the
@@ -514,8 +519,9 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
     // It brings the merge's code into the instruction caches, so that the
     // real merge at the end of the stream does not fetch it from memory.  A
     // short share (a launch over one layer) has no time to hide it: there the
-    // merge code is fetched when it runs.
-    bool dry = re - rb >= DRY_MIN_BLOCKS;
+    // merge code is fetched when it runs.  In a fused step the side warp
+    // makes this pass instead of the consumers.
+    bool dry = FUSED ? side && rb < re : re - rb >= DRY_MIN_BLOCKS;
 #pragma unroll 1
     for (int x = rb; x < re;) {
       const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
@@ -614,10 +620,13 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
         }
       };
       const int Wg = p.sh.Wring;
-      BlockWalk wk;
+      BlockWalk wk{};
       if (rb + jb < x1 && !dry) wk.init(rb + jb, u, p.sh);
-      for (; !dry && rb + jb < x1; jb += NPAIR) {
-        if (r0 >= 0) {
+      // The side warp's dry pass also runs the block body once, on whatever
+      // stage 0 holds: no wait, no release, no wrap (whose row it would write).
+      bool dry_blk = side && dry;
+      for (; dry_blk || (!dry && rb + jb < x1); jb += NPAIR) {
+        if (r0 >= 0 && !dry_blk) {
           // NPAIR blocks further on: the query base turns by R(-NPAIR*TK), and
           // by R(W_ring) each time the ring's end is passed; where the blocks
           // jump (pinned prefix to ring) it is seeded from the table again.
@@ -640,7 +649,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
         const BlockGeo& bg = wk.g;
         r0 = bg.r0;
         const int wrap_at = bg.wrap_at;  // keys d >= wrap_at sit at r0 + d - W_ring
-        const bool wraps = wrap_at < TK;
+        const bool wraps = wrap_at < TK && !dry_blk;
         const bool allvalid = wraps ? (u.fill == Wg) : (r0 + TK <= bg.lim);
         const bool plain = allvalid && !wraps;   // every key visible, one base
         {
@@ -648,10 +657,11 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
           // A pair only waits on every NPAIR-th stage, so it may reach one
           // before the stage's previous block has even landed.  Waiting first
           // for that block's release makes the full barrier's parity unambiguous.
-          if (!dead && st_r > 0 &&
+          if (!dead && !dry_blk && st_r > 0 &&
               !mbar_wait_or_abort(smem_u32(empty + st_i), (st_r - 1) & 1, abort_flag))
             dead = true;
-          if (!dead && !mbar_wait_or_abort(smem_u32(full + st_i), st_r & 1, abort_flag))
+          if (!dead && !dry_blk &&
+              !mbar_wait_or_abort(smem_u32(full + st_i), st_r & 1, abort_flag))
             dead = true;
           dead = __any_sync(0xffffffffu, dead);   // the warp stays converged
           if (dead && lane == 0 && !*abort_flag) {
@@ -829,8 +839,14 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
             }
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(empty + st_i));   // this warp's half is done
+          if (lane == 0 && !dry_blk) mbar_arrive(smem_u32(empty + st_i));   // this warp's half is done
           }
+        }
+        if (dry_blk) {
+          dry_blk = false;
+          jb -= NPAIR;
+          r0 = -1;
+          continue;
         }
         stage += NPAIR;
         if (stage >= NS) { stage -= NS; ++round; }
@@ -847,7 +863,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
       // barrier) and is done; rank 0 folds it into its own and writes the
       // output.  Otherwise the partial is the output (whole unit) or goes to
       // the unit's ticket merge in global memory.
-      named_bar_sync(BAR_CONS, CONS_THREADS);
+      cbar();
       const bool whole = (x == u.ustart) && (x1 == u.uend);
       const bool ship = CL && !whole && x != u.ustart;      // rank 1: partial goes to rank 0
       const bool receive = CL && !whole && x == u.ustart;   // rank 0: waits for it
@@ -874,7 +890,7 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
           for (int i = 0; i < C::FR; ++i) my[16 + 32 * i + lane] = o[i >> 2][i & 3];
         }
       }
-      named_bar_sync(BAR_CONS, CONS_THREADS);
+      cbar();
       if (has_next && !dry) unstage_q();
       const int R = p.R;   // == G for decode
       {
@@ -985,8 +1001,9 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
       // The slots' generic-proxy accesses come before the producer's next
       // asynchronous copies into the same memory.
       fence_proxy_async();
-      named_bar_sync(BAR_CONS, CONS_THREADS);
+      cbar();
       if (dry) {   // the real pass over the same segment
+        if (side) break;
         dry = false;
         continue;
       }
@@ -995,6 +1012,12 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
         if (has_next) unstage_new();
       }
       x = x1;
+    }
+    if (side) {
+      // The step's new pairs into their slots (every unit once over the grid),
+      // then, on the step's last launch, the new stream states.
+      step_prepass<D, !ROTK>(p, sa, sfill, slag, 0, 1, lane);
+      if (p.publish) step_publish(p, lane);
     }
   }
   __syncthreads();
