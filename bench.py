@@ -133,14 +133,16 @@ def kernel_hash(kernel_key):
     return h.hexdigest()[:16]
 
 
-def _traffic(kernel_key):
+def _traffic(kernel_key, workload):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel's sources changed since the counters were taken."""
+    kernel's sources changed since the counters were taken or the counters
+    were taken on another workload."""
     try:
         with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
             d = json.load(f)
         ent = d.get(kernel_key)
-        if ent and ent.get("source_hash") == kernel_hash(kernel_key):
+        if (ent and ent.get("source_hash") == kernel_hash(kernel_key)
+                and ent.get("workload", "").split(" ")[0] == workload):
             return ent["bytes_per_launch"]
     except Exception:
         pass
@@ -679,7 +681,7 @@ def main():
                             "rkv_append + rkv_rebase + rkv_attend (all layers)")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
-                     "kernel": kernel_key, "traffic": _traffic(kernel_key),
+                     "kernel": kernel_key, "traffic": _traffic(kernel_key, args.workload),
                      "kernel_us": kern_us, "kernel_scope": scope},
         "e2e": ({"value": all_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                  "us_per_step": e2e_ms * 1e3, "us_per_step_mean": res["e2e"]["ms_mean"] * 1e3,
