@@ -532,6 +532,21 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
       // this segment is done with `qs` (and `kvn`).
       const bool has_next = x1 < re;
       if (has_next && !dry) stage_unit(unit_of_cached(x1, p, pre, sa, sfill));
+      // The CTA that finishes the unit adds the fused step's new pair.  It sits
+      // at the query's own position, so its score is <q, k_new> (the rotations
+      // cancel); warp h scores head h -- for the CTA's first segment here,
+      // while the first tiles are on their way (q and k_new are in shared
+      // memory since the barrier above), for a later one at its end.
+      const bool add_new = FUSED && (CL ? x == u.ustart : x1 == u.uend);
+      auto score_new = [&]() {
+        if (add_new && cw < G) {
+          float dot = 0.f;
+          for (int d = lane; d < D; d += 32) dot += qs[cw * QSTR + d] * kvn[d];
+          dot = warp_sum(dot);
+          if (lane == 0) mx[cw] = dot * p.scale_log2;
+        }
+      };
+      if (FUSED && !side && x == rb) score_new();
 
       // The raw query of head g (dims of the thread's A fragments), from `qs`.
       auto load_qf = [&](float (&qr)[NKB][4]) {
@@ -867,21 +882,12 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
       const bool whole = (x == u.ustart) && (x1 == u.uend);
       const bool ship = CL && !whole && x != u.ustart;      // rank 1: partial goes to rank 0
       const bool receive = CL && !whole && x == u.ustart;   // rank 0: waits for it
-      // The CTA that finishes the unit adds the fused step's new pair.
-      const bool add_new = FUSED && (CL ? x == u.ustart : x1 == u.uend);
       {
         float lsum = l_run;
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
         if constexpr (FUSED) {
-          // The new pair sits at the query's own position: its score is <q, k_new>
-          // (the rotations cancel).  Warp h scores head h.
-          if (add_new && cw < G) {
-            float dot = 0.f;
-            for (int d = lane; d < D; d += 32) dot += qs[cw * QSTR + d] * kvn[d];
-            dot = warp_sum(dot);
-            if (lane == 0) mx[cw] = dot * p.scale_log2;
-          }
+          if (x != rb) score_new();
         }
         if (!dry) {
           float* my = slots + cw * C::SLOT;
