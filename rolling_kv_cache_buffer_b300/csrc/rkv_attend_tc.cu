@@ -46,9 +46,18 @@ namespace {
 constexpr int TC_SMW = 4;                       // softmax warps of one group
 constexpr int TC_SMG = 2;                       // softmax groups (one stream of steps each)
 constexpr int TC_RW = 4;                        // staging (rotation) warps
-constexpr int W_SM0 = 1, W_MMA = 1 + TC_SMG * TC_SMW, W_ROT0 = W_MMA + 1;
+// Warps 9.. are the MMA issuer and the staging warps; the issuer takes warp 10
+// (sub-partition 2), off the sub-partitions of the softmax warps that hold
+// rows when a unit has at most 64 (lane quarters 0 and 1: warps 4, 8 and 1, 5).
+constexpr int W_SM0 = 1, W_ROT0 = 1 + TC_SMG * TC_SMW, W_MMA = W_ROT0 + 1;
 constexpr int TC_SMT = TC_SMG * TC_SMW * 32;    // softmax threads
-constexpr int TC_THREADS = (W_ROT0 + TC_RW) * 32;
+constexpr int TC_THREADS = (W_ROT0 + TC_RW + 1) * 32;
+// Staging thread index of a thread of a staging warp (the warps from W_ROT0
+// but the issuer's).
+__device__ __forceinline__ int staging_index(int tid) {
+  const int w = tid >> 5;
+  return (w - W_ROT0 - (w > W_MMA ? 1 : 0)) * 32 + (tid & 31);
+}
 constexpr int TC_MAX_STAGES = 12;
 constexpr int TC_ROWS = 128;                    // M of every product
 constexpr int TBAR_PREFIX = 2;                  // named barrier: block prefix ready
@@ -376,7 +385,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if constexpr (ROTK) {
-    if (warp >= W_ROT0) load_fine_rot<D>(p, fine, tid - 32 * W_ROT0, TC_RW * 32);
+    if (warp >= W_ROT0 && warp != W_MMA) load_fine_rot<D>(p, fine, staging_index(tid), TC_RW * 32);
   }
   prefetch_queries(p, D);
   prefetch_states(p);
@@ -403,10 +412,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       flag[2] = produce<D, ROTK, ROTK ? KEY_BASES : NO_ROWS>(
           p, &tmK, &tmV, stages, full, empty, mdone, pre, sa, sfill, rb, re, abort_flag);
     __syncwarp();
-  } else if (warp >= W_ROT0) {
+  } else if (warp >= W_ROT0 && warp != W_MMA) {
     // ------------------------------------------------------------- staging warps
     stage_tiles<D, STYLE, ROTK>(p, stages, fine, full, rotd, pre, sa, sfill, rb, re, abort_flag,
-                                tid - 32 * W_ROT0);
+                                staging_index(tid));
   } else if (warp == W_MMA) {
     // --------------------------------------------------------------- MMA issuer
     if (lane == 0) {
