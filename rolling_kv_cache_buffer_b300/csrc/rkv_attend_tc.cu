@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(smem_u32(sfree + i), TC_SMW);
       mbar_init(smem_u32(pready + i), TC_SMW);
     }
-    mbar_init(smem_u32(qready), TC_SMW);
+    mbar_init(smem_u32(qready), TC_SMG * TC_SMW);   // every softmax warp
     mbar_init(smem_u32(ofin), 1);
     mbar_init(smem_u32(mdone), 1);
     fence_mbar_init();
@@ -537,64 +537,88 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int rq = row < R ? qbase + row / G : -1;
       // ---- this segment's Q tile: row = (query j, head), rotated to r_j ----
       // (plus the lag of stored-rotated keys that follow a re-basing epoch);
-      // rows >= R are zero.  Eight rotary pairs per pass: split-half pairs
-      // (i, i + D/2) from two 16-byte chunks, interleaved ones from one.
-      // The first group stages it.
-      if (grp == 0) {
-        const size_t qo = row < R ? row_offset(p, u, row) : 0;
-        const float2* t = p.table + (size_t)(row < R ? rq + slag[u.s] : 0) * HALF;
-        auto load8 = [&](int d0, float (&v)[8]) {
-          if (row >= R) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = 0.f;
-          } else if (p.sh.q_bf16) {
+      // rows >= R are zero.  The work is cut into chunks of eight rotary
+      // pairs of one row (split-half pairs (i, i + D/2) from two 16-byte runs
+      // of q, interleaved ones from one) dealt round-robin to every softmax
+      // thread; each thread issues all the loads of a batch of its chunks
+      // before it uses the first, so the tile costs one or two memory round
+      // trips (the memory system is loaded by the stream, and dependent loads
+      // would hold the segment's first product back by microseconds).
+      {
+        constexpr int NCK = STYLE == 0 ? HALF / 8 : D / 8;   // chunks per row
+        constexpr int IB = STYLE == 0 ? 2 : 4;              // chunks per thread and batch
+        auto qtile = [&](int r, int d0) {
+          return reinterpret_cast<uint4*>(qt + (d0 >> 6) * (TC_ROWS * 128) + swz128(r, d0 & 63));
+        };
+        for (int i = st; i < (TC_ROWS - R) * (D / 8); i += TC_SMT)
+          *qtile(R + i / (D / 8), 8 * (i % (D / 8))) = make_uint4(0, 0, 0, 0);
+        auto load8 = [&](size_t off, float (&v)[8]) {
+          if (p.sh.q_bf16) {
             const uint4 w = __ldg(reinterpret_cast<const uint4*>(
-                static_cast<const uint16_t*>(p.q) + qo + d0));
+                static_cast<const uint16_t*>(p.q) + off));
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) { v[2 * i] = bf_lo(ww[i]); v[2 * i + 1] = bf_hi(ww[i]); }
           } else {
-            const float4* f = reinterpret_cast<const float4*>(
-                static_cast<const float*>(p.q) + qo + d0);
-            const float4 a = __ldg(f), bq = __ldg(f + 1);
-            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-            v[4] = bq.x; v[5] = bq.y; v[6] = bq.z; v[7] = bq.w;
+            const float4* f = reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + off);
+            const float4 x0 = __ldg(f), x1v = __ldg(f + 1);
+            v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+            v[4] = x1v.x; v[5] = x1v.y; v[6] = x1v.z; v[7] = x1v.w;
           }
         };
-        auto store8 = [&](int d0, const float (&v)[8]) {
-          const uint4 w = make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]),
+        auto store8 = [&](int r, int d0, const float (&v)[8]) {
+          *qtile(r, d0) = make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]),
                                      pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
-          *reinterpret_cast<uint4*>(qt + (d0 >> 6) * (TC_ROWS * 128) + swz128(row, d0 & 63)) = w;
         };
-        if constexpr (STYLE == 0) {
+        const int items = R * NCK;
 #pragma unroll 1
-          for (int i0 = 0; i0 < HALF; i0 += 8) {
-            float xa[8], xb[8];
-            load8(i0, xa);
-            load8(i0 + HALF, xb);
+        for (int i0 = st; i0 < items; i0 += IB * TC_SMT) {
+          float xa[IB][8], xb[IB][8];
+          float4 cs[IB][4];   // (cos, sin) of pairs 2k and 2k+1 = float4 k of a table row
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float2 cs = row < R ? __ldg(t + i0 + i) : make_float2(1.f, 0.f);
-              const float a = xa[i], bq = xb[i];
-              xa[i] = a * cs.x - bq * cs.y;
-              xb[i] = bq * cs.x + a * cs.y;
+          for (int k = 0; k < IB; ++k) {
+            const int it = min(i0 + k * TC_SMT, items - 1);
+            const int r = it / NCK, d0 = 8 * (it % NCK);
+            const size_t qo = row_offset(p, u, r);
+            const float4* tb = reinterpret_cast<const float4*>(
+                p.table + (size_t)(qbase + r / G + slag[u.s]) * HALF);
+            load8(qo + d0, xa[k]);
+            if constexpr (STYLE == 0) {
+              load8(qo + d0 + HALF, xb[k]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) cs[k][e] = __ldg(tb + d0 / 2 + e);
+            } else {
+              cs[k][0] = __ldg(tb + d0 / 4);
+              cs[k][1] = __ldg(tb + d0 / 4 + 1);
             }
-            store8(i0, xa);
-            store8(i0 + HALF, xb);
           }
-        } else {
-#pragma unroll 1
-          for (int d0 = 0; d0 < D; d0 += 8) {
-            float xv[8];
-            load8(d0, xv);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 cs = row < R ? __ldg(t + d0 / 2 + i) : make_float2(1.f, 0.f);
-              const float a = xv[2 * i], bq = xv[2 * i + 1];
-              xv[2 * i] = a * cs.x - bq * cs.y;
-              xv[2 * i + 1] = bq * cs.x + a * cs.y;
+          for (int k = 0; k < IB; ++k) {
+            const int it = i0 + k * TC_SMT;
+            if (it >= items) break;
+            const int r = it / NCK, d0 = 8 * (it % NCK);
+            if constexpr (STYLE == 0) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {   // pair d0 + i: (x, y) = (q[d0 + i], q[d0 + i + D/2])
+                const float4 c4 = cs[k][i >> 1];
+                const float cv = (i & 1) ? c4.z : c4.x, sv = (i & 1) ? c4.w : c4.y;
+                const float x = xa[k][i], y = xb[k][i];
+                xa[k][i] = x * cv - y * sv;
+                xb[k][i] = y * cv + x * sv;
+              }
+              store8(r, d0, xa[k]);
+              store8(r, d0 + HALF, xb[k]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {   // pair d0/2 + i: (x, y) = (q[d0 + 2i], q[d0 + 2i + 1])
+                const float4 c4 = cs[k][i >> 1];
+                const float cv = (i & 1) ? c4.z : c4.x, sv = (i & 1) ? c4.w : c4.y;
+                const float x = xa[k][2 * i], y = xa[k][2 * i + 1];
+                xa[k][2 * i] = x * cv - y * sv;
+                xa[k][2 * i + 1] = y * cv + x * sv;
+              }
+              store8(r, d0, xa[k]);
             }
-            store8(d0, xv);
           }
         }
         // The tensor cores read the Q tile through the async proxy.
