@@ -46,6 +46,7 @@ namespace {
 constexpr int TC_SMW = 4;                       // softmax warps of one group
 constexpr int TC_SMG = 2;                       // softmax groups (one stream of steps each)
 constexpr int TC_RW = 4;                        // staging (rotation) warps
+constexpr int TC_RG = 2;                        // staging groups (they take alternate blocks)
 // Warps 9.. are the MMA issuer and the staging warps; the issuer takes warp 10
 // (sub-partition 2), off the sub-partitions of the softmax warps that hold
 // rows when a unit has at most 64 (lane quarters 0 and 1: warps 4, 8 and 1, 5).
@@ -84,9 +85,9 @@ struct TcCfg : PipeCfg<D, ROTK> {
 };
 
 __host__ __device__ constexpr size_t tc_smem_bytes(int stage, int fine, int qt, int ns, int S) {
-  // stages, Q tile, R(d) table, 3 barriers per stage, 9 more barriers, the
+  // stages, Q tile, R(d) table, 3 barriers per stage, 10 more barriers, the
   // tensor memory address (16 B), flags (16 B), the per-stream cache.
-  return 1024 + (size_t)ns * stage + (size_t)qt + (size_t)fine + (size_t)ns * 24 + 9 * 8 + 16 +
+  return 1024 + (size_t)ns * stage + (size_t)qt + (size_t)fine + (size_t)ns * 24 + 10 * 8 + 16 +
          16 + (size_t)(4 * S + 1) * 4;
 }
 
@@ -216,8 +217,9 @@ __device__ __forceinline__ void rot2_composed(f2& X, f2& Y, float4 b, float4 f) 
   Y = Yr;
 }
 
-// Staging warps: for every block of the CTA's share, in order, wait for its
-// tiles, zero the V rows of slots outside the window (they may hold anything,
+// Staging warps, in TC_RG groups that take alternate blocks of the CTA's
+// share (so that the load -> turn -> store chains of two blocks overlap): for
+// every block of its group, in order, wait for its tiles, zero the V rows of slots outside the window (they may hold anything,
 // and 0 * NaN would reach the output through P V), turn each key of the K
 // tile in place to its position (pre-RoPE keys) -- slot d of the block at
 // r0 + d, or r0 + d - W_ring past the ring's end -- and hand the stage on.  R(r0 + d) is the block's base row
@@ -234,18 +236,23 @@ __device__ __forceinline__ void stage_tiles(const AttendParams& p, uint8_t* stag
                                              int rb, int re, volatile int* abort_flag, int rt) {
   using C = PipeCfg<D, ROTK>;
   constexpr int HALF = D / 2, NG = D / 16, ITEMS = TK * NG;
-  constexpr int RT = TC_RW * 32;
+  constexpr int RT = TC_RW * 32 / TC_RG;   // threads of a group
   constexpr int VCH = D / 8;   // 16-byte chunks of a V row
   const int NS = p.ns, Wg = p.sh.Wring;
-  const int lane = rt & 31;
-  int stage = 0, round = 0;
+  const int lane = rt & 31, rg = rt / RT;
+  rt -= rg * RT;
+  int stage = 0, round = 0, jx = 0;
   for (int x = rb; x < re;) {
     const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
     const int x1 = min(u.uend, re);
     BlockWalk wk;
     wk.init(x, u, p.sh);
-    for (bool first = true; x < x1; ++x, first = false) {
+    for (bool first = true; x < x1; ++x, ++jx, first = false) {
       if (!first) wk.advance(1, u, p.sh);
+      if (jx % TC_RG != rg) {   // the other group's block
+        if (++stage == NS) { stage = 0; ++round; }
+        continue;
+      }
       // Every block passes through here in order, so the full barrier of a
       // stage is never more than one phase ahead of this wait.
       const bool bad = !mbar_wait_or_abort(smem_u32(full + stage), round & 1, abort_flag);
@@ -325,7 +332,12 @@ __device__ __forceinline__ void stage_tiles(const AttendParams& p, uint8_t* stag
 
 }  // namespace
 
-template <int D, bool ROTK, int STYLE>
+// CL: the grid is one 2-CTA cluster per unit (every unit cut into exactly
+// two CTAs).  Rank 1 leaves its partial (m, l and the unnormalised O rows) in
+// its own stage memory, free once its one segment's products are done, and
+// arrives on an mbarrier of rank 0; rank 0 reads it through distributed
+// shared memory, folds it into its own rows and writes the output.
+template <int D, bool ROTK, int STYLE, bool CL>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     attend_tc_chunk(const __grid_constant__ AttendParams p,
                     const __grid_constant__ CUtensorMap tmK,
@@ -349,7 +361,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* qready = pready + 2;                                 // Q tile of the segment
   uint64_t* ofin = qready + 1;                                   // every product of a segment
   uint64_t* mdone = ofin + 1;                                    // a segment's products issued
-  uint32_t* tm_base = reinterpret_cast<uint32_t*>(mdone + 1);    // tensor memory address
+  uint64_t* rxbar = mdone + 1;                                   // the peer's partial (CL)
+  uint32_t* tm_base = reinterpret_cast<uint32_t*>(rxbar + 1);    // tensor memory address
   int* flag = reinterpret_cast<int*>(tm_base + 4);               // ticket, abort, issued
   int* pre = flag + 4;                                           // [S+1] block prefix
   int* sa = pre + p.sh.S + 1;                                    // [S] ring start | npin
@@ -364,7 +377,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(full + i), 1);
       mbar_init(smem_u32(empty + i), 1);      // the MMA issuer's commit
-      mbar_init(smem_u32(rotd + i), TC_RW);   // every rotation warp
+      mbar_init(smem_u32(rotd + i), TC_RW / TC_RG);   // every warp of the block's group
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(sfull + i), 1);
@@ -374,10 +387,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     mbar_init(smem_u32(qready), TC_SMG * TC_SMW);   // every softmax warp
     mbar_init(smem_u32(ofin), 1);
     mbar_init(smem_u32(mdone), 1);
+    mbar_init(smem_u32(rxbar), TC_SMT);   // every softmax thread of rank 1
     fence_mbar_init();
     flag[1] = 0;
     flag[2] = 0;
   }
+  // Cluster barrier, phase 0: both CTAs have initialised their barriers once
+  // it completes (waited on below, before any access to the peer).
+  if constexpr (CL) cluster_arrive_relaxed();
   if (warp == W_MMA) {
     // The MMA warp owns the tensor memory: TM_COLS columns for the CTA.
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -400,6 +417,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     named_bar_sync(TBAR_PREFIX, TC_THREADS);
   }
   tc_fence_after();
+  if constexpr (CL) cluster_wait();
   const uint32_t tmem = *tm_base;
   const int T = pre[p.sh.S];
   const int P = min(static_cast<int>(gridDim.x), T);
@@ -531,8 +549,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
       const int x1 = min(u.uend, re);
       const bool whole = (x == u.ustart) && (x1 == u.uend);
-      // A split unit's partial goes to slot 0 (the CTA's first segment) or 1.
+      // A split unit's partial goes to slot 0 (the CTA's first segment) or 1;
+      // in a cluster, rank 1 (the unit's second half) ships it to rank 0.
       const int kslot = x == rb ? 0 : 1;
+      const bool ship = CL && !whole && x != u.ustart;
+      const bool receive = CL && !whole && x == u.ustart;
       const int qbase = u.npin + u.fill - c;  // position of the chunk's first query
       const int rq = row < R ? qbase + row / G : -1;
       // ---- this segment's Q tile: row = (query j, head), rotated to r_j ----
@@ -763,13 +784,45 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       xch[grp * 384 + 128 + row] = l;
       xch[grp * 384 + 256 + row] = static_cast<float>(nmine);
       named_bar_sync(TBAR_SM, TC_SMT);
-      if (fin) {
+      // Rank 1's partial, in its stage memory: O rows first (16-byte chunk j
+      // of row r at chunk j ^ (r mod 8), so that eight rows read at once hit
+      // eight bank groups), then m, then l.
+      auto rx_o = [&](int r, int col) {
+        return static_cast<uint32_t>(4 * (r * D + ((((col >> 2) ^ (r & 7))) << 2)));
+      };
+      const uint32_t rx_m = static_cast<uint32_t>(4 * R * D), rx_l = rx_m + 4u * R;
+      bool got = true;
+      float M1 = NEG_BIG, L1 = 0.f;
+      uint32_t peer = 0;
+      if (receive) {
+        got = false;
+        for (uint32_t i = 0; i < WAIT_LIMIT && !got; ++i)
+          got = mbar_try_wait_cluster(smem_u32(rxbar), 0);
+        if (!got && st == 0) {
+          *abort_flag = 1;
+          p.st[u.s].status = STATUS_DEVICE_STATE;
+        }
+        peer = map_to_rank(smem_u32(stages), cluster_rank() ^ 1u);
+        if (got && row < R) {
+          M1 = ld_cluster_f32(peer + rx_m + 4u * row);
+          L1 = ld_cluster_f32(peer + rx_l + 4u * row);
+        }
+      }
+      if (fin && got) {
         const float ma = xch[row], la = xch[128 + row];
         const float mb = xch[384 + row], lb = xch[512 + row];
         const bool ha = xch[256 + row] > 0.f, hb = xch[640 + row] > 0.f;
         const float M = ha && hb ? fmaxf(ma, mb) : (ha ? ma : mb);
         const float wa = ha ? ex2(ma - M) : 0.f, wb = hb ? ex2(mb - M) : 0.f;
-        const float L = wa * la + wb * lb;
+        float L = wa * la + wb * lb;
+        // Rank 0: out = (s0 O + s1 O1) / (s0 L + s1 L1), s = 2^(m - max(M, M1)).
+        float s0 = 1.f, s1 = 0.f;
+        if (receive) {
+          const float Mx = fmaxf(M, M1);
+          s0 = ex2(M - Mx);
+          s1 = ex2(M1 - Mx);
+          L = s0 * L + s1 * L1;
+        }
         constexpr int DH = D / 2;
 #pragma unroll 1
         for (int c0 = grp * DH; c0 < (grp + 1) * DH; c0 += 16) {
@@ -784,13 +837,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             ov[i] = (ha ? wa * __uint_as_float(oa[i]) : 0.f) +
                     (hb ? wb * __uint_as_float(ob[i]) : 0.f);
           if (row < R) {
-            if (whole) {
+            if (whole || receive) {
               const float inv = L > 0.f ? 1.f / L : 0.f;
+              if (receive) {
+#pragma unroll
+                for (int i = 0; i < 16; i += 4) {
+                  const float4 o1 = ld_cluster_f4(peer + rx_o(row, c0 + i));
+                  ov[i] = s0 * ov[i] + s1 * o1.x;
+                  ov[i + 1] = s0 * ov[i + 1] + s1 * o1.y;
+                  ov[i + 2] = s0 * ov[i + 2] + s1 * o1.z;
+                  ov[i + 3] = s0 * ov[i + 3] + s1 * o1.w;
+                }
+              }
               float* o = p.out + row_offset(p, u, row) + c0;
 #pragma unroll
               for (int i = 0; i < 16; i += 4)
                 *reinterpret_cast<float4*>(o + i) =
                     make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv, ov[i + 3] * inv);
+            } else if (ship) {
+              uint8_t* rx = stages;
+              if (c0 == 0) {
+                *reinterpret_cast<float*>(rx + rx_m + 4 * row) = M;
+                *reinterpret_cast<float*>(rx + rx_l + 4 * row) = L;
+              }
+#pragma unroll
+              for (int i = 0; i < 16; i += 4)
+                *reinterpret_cast<float4*>(rx + rx_o(row, c0 + i)) =
+                    make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
             } else {
               // Split unit: this CTA's partial (m, l, unnormalised O) of the row.
               float* pp = p.partials + (size_t)(2 * b + kslot) * p.slot_floats;
@@ -802,9 +875,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         tc_fence_before();
       }
+      // Rank 1: every softmax thread releases its part of the partial.
+      if (ship) mbar_arrive_remote(map_to_rank(smem_u32(rxbar), cluster_rank() ^ 1u));
       // The exchange area is the next segment's Q tile.
       named_bar_sync(TBAR_SM, TC_SMT);
-      if (!whole) {
+      if (!whole && !CL) {
         // The last CTA of the unit to take its ticket merges the partials.
         named_bar_sync(TBAR_SM, TC_SMT);
         if (st == 0) {
@@ -829,7 +904,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  // In a cluster neither CTA leaves while its peer may still read its memory.
+  if constexpr (CL) cluster_sync_all(); else __syncthreads();
   tc_fence_after();
   if (warp == W_MMA) {
     // After an abort: no product may be in flight when the memory is freed.
@@ -868,7 +944,7 @@ bool attend_tc_supported(const Shape& sh, int c) {
   return rotk ? tc_stages<64, true>(sh.S) >= need : tc_stages<64, false>(sh.S) >= need;
 }
 
-template <int D, bool ROTK, int STYLE>
+template <int D, bool ROTK, int STYLE, bool CL>
 static cudaError_t launch_tc_k(const AttendParams& p0, const CUtensorMap& tk,
                                const CUtensorMap& tv, int grid, cudaStream_t s) {
   using C = TcCfg<D, ROTK>;
@@ -876,7 +952,7 @@ static cudaError_t launch_tc_k(const AttendParams& p0, const CUtensorMap& tk,
   p.ns = tc_stages<D, ROTK>(p.sh.S);
   const size_t smem = tc_smem_bytes(C::STAGE, C::FINE, C::QT, p.ns, p.sh.S);
   if (smem > (size_t)SMEM_LIMIT) return cudaErrorNotSupported;
-  auto kern = attend_tc_chunk<D, ROTK, STYLE>;
+  auto kern = attend_tc_chunk<D, ROTK, STYLE, CL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -885,12 +961,33 @@ static cudaError_t launch_tc_k(const AttendParams& p0, const CUtensorMap& tk,
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, p, tk, tv);
+}
+
+// The two CTAs that share a unit merge through distributed shared memory
+// when every unit is cut into exactly two CTAs (one stream, grid = 2 units)
+// and rank 1's partial (R rows of D floats, m and l) fits in its stages.
+template <int D, bool ROTK>
+static bool tc_cluster_merge(const AttendParams& p, int grid) {
+  using C = TcCfg<D, ROTK>;
+  return p.sh.S == 1 && grid == 2 * p.L_att * p.sh.Hkv &&
+         (size_t)tc_stages<D, ROTK>(p.sh.S) * C::STAGE >= (size_t)(p.R * D + 2 * p.R) * 4;
+}
+
+template <int D, bool ROTK, int STYLE>
+static cudaError_t launch_tc_s(const AttendParams& p, const CUtensorMap& tk,
+                               const CUtensorMap& tv, int grid, cudaStream_t s) {
+  return tc_cluster_merge<D, ROTK>(p, grid) ? launch_tc_k<D, ROTK, STYLE, true>(p, tk, tv, grid, s)
+                                            : launch_tc_k<D, ROTK, STYLE, false>(p, tk, tv, grid, s);
 }
 
 template <int D>
@@ -898,10 +995,10 @@ static cudaError_t launch_tc_d(const AttendParams& p, const CUtensorMap& tk,
                                const CUtensorMap& tv, int grid, cudaStream_t s) {
   const bool rotk = !p.sh.stored_rotated;
   if (p.sh.style == 0)
-    return rotk ? launch_tc_k<D, true, 0>(p, tk, tv, grid, s)
-                : launch_tc_k<D, false, 0>(p, tk, tv, grid, s);
-  return rotk ? launch_tc_k<D, true, 1>(p, tk, tv, grid, s)
-              : launch_tc_k<D, false, 1>(p, tk, tv, grid, s);
+    return rotk ? launch_tc_s<D, true, 0>(p, tk, tv, grid, s)
+                : launch_tc_s<D, false, 0>(p, tk, tv, grid, s);
+  return rotk ? launch_tc_s<D, true, 1>(p, tk, tv, grid, s)
+              : launch_tc_s<D, false, 1>(p, tk, tv, grid, s);
 }
 
 cudaError_t launch_attend_tc(const AttendParams& p, const CUtensorMap& tk, const CUtensorMap& tv,

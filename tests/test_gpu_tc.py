@@ -137,3 +137,63 @@ def test_tc_agrees_with_mma_chunk_kernel():
         cache.append(dev(kn, torch.bfloat16), dev(vn, torch.bfloat16))
         outs.append(cache.attend(dev(q, torch.bfloat16)).double().cpu().numpy())
     compare(outs[0], outs[1], 2e-2, 2e-3)
+
+
+@pytest.mark.parametrize("c,style,window", [(6, "split_half", None), (16, "split_half", None),
+                                            (6, "interleaved", 512)])
+def test_tc_pair_merge(c, style, window):
+    """Rings of 16-17 blocks over 2 layers x 2 KV heads: the grid is exactly
+    two CTAs per unit, one 2-CTA cluster each, and rank 1's partial is merged
+    into rank 0's through distributed shared memory.  Windows of 1 block (whole
+    units, no merge), 9 blocks (a 4 + 5 split) and the full window, then
+    steps that evict; 16-token chunks fill the 128-row tile."""
+    from rolling_kv_cache_buffer_b300 import RollingKV
+    W = 512 if window is None else 544
+    wl = WORKLOADS["qwen3b"].replace(n_layers=2, capacity=W, n_new=c, window=window)
+    cache = RollingKV(1, 2, 16, 2, 128, W, max_chunk=c, rope_style=style, attend_impl="tc",
+                      window=window or 0)
+    orc = O.RollingCacheOracle(1, 2, 16, 2, 128, W, style=style, window=window)
+    for i, (fill, origin) in enumerate([(20, 77), (280, 123_457), (window or W, 9_999_999)]):
+        k = random_rows((2, 2, fill, 128), 500 + 2 * i, torch.bfloat16)
+        v = random_rows((2, 2, fill, 128), 501 + 2 * i, torch.bfloat16)
+        write_window(cache, 0, origin, fill, k, v)
+        orc.set_state(0, origin, fill, k.double().numpy(), v.double().numpy())
+        for t in range(1, 4):
+            q, kn, vn = step_inputs(wl, 10 * i + t)
+            cache.append(dev(kn, torch.bfloat16), dev(vn, torch.bfloat16))
+            orc.append(kn.double().numpy(), vn.double().numpy())
+            compare(cache.attend(dev(q, torch.bfloat16)), orc.attend(q.double().numpy()))
+
+
+def test_tc_pair_merge_stored_rotated_and_pinned():
+    """The cluster merge with stored-rotated keys (re-rotated at every
+    eviction) from an empty 512-slot ring through eviction, and with a pinned
+    prefix of 20 pairs in 32 slots in front of a 512-slot ring."""
+    from rolling_kv_cache_buffer_b300 import RollingKV
+    wl = WORKLOADS["qwen3b"].replace(n_layers=2, capacity=512, n_new=6)
+    cache = RollingKV(1, 2, 16, 2, 128, 512, max_chunk=6, layout="stored_rotated",
+                      attend_impl="tc")
+    orc = O.StoredRotatedOracle(1, 2, 16, 2, 128, 512)
+    for t in range(1, 100):
+        q, k, v = step_inputs(wl, t)
+        cache.append(dev(k, torch.bfloat16), dev(v, torch.bfloat16))
+        orc.append(k.double().numpy(), v.double().numpy())
+        cache.rebase()
+        orc.rebase()
+        out = cache.attend(dev(q, torch.bfloat16))
+        if t % 9 == 0 or t > 95:
+            compare(out, orc.attend(q.double().numpy()))
+    wl = WORKLOADS["qwen3b"].replace(n_layers=2, capacity=544, n_new=4)
+    cache = RollingKV(1, 2, 16, 2, 128, 544, max_chunk=4, attend_impl="tc", n_pinned=32)
+    orc = O.RollingCacheOracle(1, 2, 16, 2, 128, 544, n_pinned=32)
+    kp = random_rows((2, 20, 2, 128), 61, torch.bfloat16)
+    vp = random_rows((2, 20, 2, 128), 62, torch.bfloat16)
+    cache.reset_stream(0, 70_000, dev(kp, torch.bfloat16), dev(vp, torch.bfloat16))
+    orc.reset(0, 70_000, kp.permute(0, 2, 1, 3).double().numpy(),
+              vp.permute(0, 2, 1, 3).double().numpy(), 20)
+    for t in range(1, 140):
+        q, k, v = step_inputs(wl, t)
+        cache.append(dev(k, torch.bfloat16), dev(v, torch.bfloat16))
+        orc.append(k.double().numpy(), v.double().numpy())
+        if t % 11 == 0 or t in (1, 2, 128, 129, 130, 139):
+            compare(cache.attend(dev(q, torch.bfloat16)), orc.attend(q.double().numpy()))
