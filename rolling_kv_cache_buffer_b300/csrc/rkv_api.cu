@@ -89,6 +89,8 @@ WsLayout make_layout(const rkv_config* c) {
   size_t off = 0;
   w.table_off = off;
   off = align_up(off + (size_t)2 * s.W * (s.D / 2) * sizeof(float2), 256);
+  w.table_g_off = off;
+  off = align_up(off + (size_t)2 * s.W * (s.D / 2) * sizeof(float2), 256);
   w.append_tk_off = off;
   off = align_up(off + (size_t)s.S * 4, 256);
   w.rerot_tk_off = off;
@@ -168,6 +170,20 @@ std::vector<float2> make_table(const Shape& s, double theta) {
   return t;
 }
 
+// The same rows regrouped: chunk j of a row = (cos, cos, sin, sin) of pairs 2j
+// and 2j+1, so that packed f32x2 arithmetic finds the two cosines (sines) of
+// a chunk in one register pair.
+std::vector<float4> group_table(const std::vector<float2>& t, const Shape& s) {
+  const int half = s.D / 2;
+  std::vector<float4> g(t.size() / 2);
+  for (size_t m = 0; m < (size_t)2 * s.W; ++m)
+    for (int j = 0; j < half / 2; ++j) {
+      const float2 a = t[m * half + 2 * j], b = t[m * half + 2 * j + 1];
+      g[m * (half / 2) + j] = make_float4(a.x, b.x, a.y, b.y);
+    }
+  return g;
+}
+
 }  // namespace
 
 extern "C" {
@@ -243,6 +259,7 @@ rkv_status rkv_create(const rkv_config* cfg, const rkv_buffers* bufs, void* stre
     return RKV_ERR_UNSUPPORTED;
   }
   h->host_table = make_table(h->sh, cfg->rope_theta);
+  h->host_table_g = group_table(h->host_table, h->sh);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(h->state, 0, (size_t)h->sh.S * sizeof(rkv::StreamState), s);
   if (e == cudaSuccess)
@@ -250,6 +267,9 @@ rkv_status rkv_create(const rkv_config* cfg, const rkv_buffers* bufs, void* stre
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(h->workspace + ws.table_off, h->host_table.data(),
                         h->host_table.size() * sizeof(float2), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(h->workspace + ws.table_g_off, h->host_table_g.data(),
+                        h->host_table_g.size() * sizeof(float4), cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) {
     delete h;
     return RKV_ERR_CUDA;
@@ -304,6 +324,7 @@ rkv_status rkv_attend(rkv_handle* h, const void* q, float* out, int32_t layer_be
   p.k_pool = h->k_pool;   // read only through the tensor maps (and L2 prefetches)
   p.v_pool = h->v_pool;
   p.table = reinterpret_cast<const float2*>(h->workspace + h->ws.table_off);
+  p.table_g = reinterpret_cast<const float4*>(h->workspace + h->ws.table_g_off);
   p.partials = reinterpret_cast<float*>(h->workspace + h->ws.part_off);
   p.unit_tickets = reinterpret_cast<int*>(h->workspace + h->ws.unit_tk_off);
   p.layer_begin = layer_begin;
@@ -337,6 +358,7 @@ rkv_status rkv_step_layers(rkv_handle* h, int32_t layer_begin, int32_t n_layers,
   p.q = q;
   p.out = out;
   p.table = reinterpret_cast<const float2*>(h->workspace + h->ws.table_off);
+  p.table_g = reinterpret_cast<const float4*>(h->workspace + h->ws.table_g_off);
   p.partials = reinterpret_cast<float*>(h->workspace + h->ws.part_off);
   p.unit_tickets = reinterpret_cast<int*>(h->workspace + h->ws.unit_tk_off);
   p.layer_begin = layer_begin;

@@ -63,19 +63,20 @@ __device__ __forceinline__ uint32_t fine_chunk_keys(int d, int k) {
 
 // The rotation warps of the tcgen05 chunk kernel read the same table with
 // eight lanes on eight consecutive keys d and one chunk j of pairs (2j, 2j+1)
-// as (cos, sin, cos, sin): chunk j of row d sits at position j ^ (d mod 8) of
-// its row, so those eight reads hit eight different 16-byte bank groups.
+// as (cos, cos, sin, sin) (the grouped table): chunk j of row d sits at
+// position j ^ (d mod 8) of its row, so those eight reads hit eight different
+// 16-byte bank groups.
 __device__ __forceinline__ uint32_t fine_chunk_rot(int d, int j) {
   return static_cast<uint32_t>((j ^ (d & 7)) << 4);
 }
-// Threads t0, t0+nt, ... fill that table from rows 0..TK-1 of the global one.
+// Threads t0, t0+nt, ... fill that table from rows 0..TK-1 of the grouped one.
 template <int D>
 __device__ __forceinline__ void load_fine_rot(const AttendParams& p, uint8_t* fine, int t0,
                                               int nt) {
   constexpr int HALF = D / 2;
   for (int idx = t0; idx < TK * HALF / 2; idx += nt) {
     const int d = idx / (HALF / 2), j = idx % (HALF / 2);
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p.table + (size_t)d * HALF) + j);
+    const float4 v = __ldg(p.table_g + (size_t)d * (HALF / 2) + j);
     *reinterpret_cast<float4*>(fine + d * HALF * 8 + fine_chunk_rot(d, j)) = v;
   }
 }
@@ -117,15 +118,17 @@ __device__ __forceinline__ void prefetch_states(const AttendParams& p) {
 
 // The producer loop, run by lane 0 of warp 0 over blocks [rb, re).  Returns
 // the number of stages it filled.  Stops early (status set, *abort raised) if
-// a wait runs out.
+// a wait runs out.  The (cos, sin) rows come from `rows` (rows of D/2 float2
+// of the global table, or of its grouped copy), p.table when null.
 template <int D, bool ROTK, int ROWS>
 __device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap* tmK,
                                        const CUtensorMap* tmV, uint8_t* stages, uint64_t* full,
                                        uint64_t* empty, uint64_t* mdone, const int* pre,
                                        const int* sa, const int* sfill, int rb, int re,
-                                       volatile int* abort_flag) {
+                                       volatile int* abort_flag, const float2* rows = nullptr) {
   using C = PipeCfg<D, ROTK>;
   const int NS = p.ns;
+  const float2* rtab = rows ? rows : p.table;
   int stage = 0, round = 0, issued = 0, seg = 0;
   bool stop = false;
   const uint64_t pol = l2_evict_first_policy();   // every K/V row is read once
@@ -175,9 +178,9 @@ __device__ __forceinline__ int produce(const AttendParams& p, const CUtensorMap*
       tma_load_4d_hint(dst + C::TILE, tmV, 0, blk * TK, 0, ug, bar, pol);
       if constexpr (ROTK && ROWS != NO_ROWS) {
         const int rowA = r0, rowB = r0 >= Wg ? r0 - Wg : Wg - r0;
-        bulk_load(dst + 2 * C::TILE, p.table + (size_t)rowA * C::HALF, C::TROW, bar);
+        bulk_load(dst + 2 * C::TILE, rtab + (size_t)rowA * C::HALF, C::TROW, bar);
         if (wraps)
-          bulk_load(dst + 2 * C::TILE + C::TROW, p.table + (size_t)rowB * C::HALF, C::TROW, bar);
+          bulk_load(dst + 2 * C::TILE + C::TROW, rtab + (size_t)rowB * C::HALF, C::TROW, bar);
       }
       ++issued;
       if (++stage == NS) { stage = 0; ++round; }

@@ -82,6 +82,7 @@ extern "C" rkv_status rkv_attend_static_scratch(rkv_handle* h, const void* q, fl
   p.k_pool = h->k_pool;   // read only through the tensor maps (and L2 prefetches)
   p.v_pool = h->v_pool;
   p.table = reinterpret_cast<const float2*>(h->workspace + h->ws.table_off);
+  p.table_g = reinterpret_cast<const float4*>(h->workspace + h->ws.table_g_off);
   p.partials = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kTicketBytes);
   p.unit_tickets = static_cast<int*>(base);
   p.layer_begin = layer_begin;

@@ -30,13 +30,19 @@
 // The unit's split partials (m, l, O rows) merge across CTAs through global
 // memory: the last CTA to take the unit's ticket combines them.
 //
-// Roles (one persistent CTA per SM, 10 warps): warp 0 the TMA producer (the
-// stage ring of rkv_attend_pipe.cuh), warps 1-4 the softmax warps (warp w owns
-// tensor-memory lanes 32 (w mod 4) .. +31), warp 5 the MMA issuer (one lane;
-// the warp allocates and frees the tensor memory), warps 6-9 the staging
-// warps (they zero the V rows of slots outside the window and, for pre-RoPE
-// keys, rotate the K tile).  Every wait is bounded and falls back to the
-// stream's status word.
+// Roles (one persistent CTA per SM, 16 warps): warp 0 the TMA producer (the
+// stage ring of rkv_attend_pipe.cuh), warps 1-8 the softmax warps in two
+// groups (warp w owns tensor-memory lanes 32 (w mod 4) .. +31), warps 10, 11,
+// 14 and 15 the staging warps (they zero the V rows of slots outside the
+// window and, for pre-RoPE keys, rotate the K tile), three MMA issuers (one
+// lane each): warp 9 the products O += P V (the warp allocates and frees the
+// tensor memory), warps 12 and 13 the products S = Q K^T of the first and the
+// second key block of every step.  The staging warps sit on sub-partitions 2
+// and 3, away from the softmax warps that hold rows when a unit has at most
+// 64 (lane quarters 0 and 1: sub-partitions 0 and 1).  A tcgen05.mma costs the thread that issues
+// it about a hundred cycles whatever its N (measured on B300), so one thread
+// could not keep up with the twenty products of a 64-key step.  Every wait is
+// bounded and falls back to the stream's status word.
 #include "rkv_attend_pipe.cuh"
 
 namespace rkv {
@@ -47,17 +53,17 @@ constexpr int TC_SMW = 4;                       // softmax warps of one group
 constexpr int TC_SMG = 2;                       // softmax groups (one stream of steps each)
 constexpr int TC_RW = 4;                        // staging (rotation) warps
 constexpr int TC_RG = 2;                        // staging groups (they take alternate blocks)
-// Warps 9.. are the MMA issuer and the staging warps; the issuer takes warp 10
-// (sub-partition 2), off the sub-partitions of the softmax warps that hold
-// rows when a unit has at most 64 (lane quarters 0 and 1: warps 4, 8 and 1, 5).
-constexpr int W_SM0 = 1, W_ROT0 = 1 + TC_SMG * TC_SMW, W_MMA = W_ROT0 + 1;
+constexpr int W_SM0 = 1;
+constexpr int W_MMA = 1 + TC_SMG * TC_SMW;       // P V issuer, owner of the tensor memory
+constexpr int W_QK0 = W_MMA + 3;                 // Q K^T issuers: warps W_QK0, W_QK0 + 1
 constexpr int TC_SMT = TC_SMG * TC_SMW * 32;    // softmax threads
-constexpr int TC_THREADS = (W_ROT0 + TC_RW + 1) * 32;
-// Staging thread index of a thread of a staging warp (the warps from W_ROT0
-// but the issuer's).
+// The staging warps: 10, 11, 14, 15.
+__device__ __forceinline__ bool staging_warp(int w) { return (w & 2) && w > W_MMA; }
+// Staging thread index (0 .. 127) of a thread of a staging warp: warps 10, 11
+// form group 0, warps 14, 15 group 1.
 __device__ __forceinline__ int staging_index(int tid) {
   const int w = tid >> 5;
-  return (w - W_ROT0 - (w > W_MMA ? 1 : 0)) * 32 + (tid & 31);
+  return ((w & 1) | (w >= W_QK0 + 2 ? 2 : 0)) * 32 + (tid & 31);
 }
 constexpr int TC_MAX_STAGES = 12;
 constexpr int TC_ROWS = 128;                    // M of every product
@@ -73,6 +79,8 @@ constexpr float TC_TAU = 8.f;                   // lazy rescale threshold (log2 
 // softmax overlaps the other's; the two are combined row by row at the end
 // of a segment.
 constexpr int TC_KB = 2;
+constexpr int TC_THREADS = 16 * 32;
+static_assert(TC_KB == 2 && W_MMA == 9 && W_QK0 == 12, "warp roles");
 // Tensor memory columns: S[2] (f32, TC_KB * TK each), P[2] (bf16 pairs,
 // TC_KB * TK / 2 each), O[2] (f32, D columns each), one of each per stream.
 constexpr int TM_SW = TC_KB * TK, TM_PW = TC_KB * TK / 2;
@@ -85,9 +93,9 @@ struct TcCfg : PipeCfg<D, ROTK> {
 };
 
 __host__ __device__ constexpr size_t tc_smem_bytes(int stage, int fine, int qt, int ns, int S) {
-  // stages, Q tile, R(d) table, 3 barriers per stage, 10 more barriers, the
+  // stages, Q tile, R(d) table, 3 barriers per stage, 13 more barriers, the
   // tensor memory address (16 B), flags (16 B), the per-stream cache.
-  return 1024 + (size_t)ns * stage + (size_t)qt + (size_t)fine + (size_t)ns * 24 + 10 * 8 + 16 +
+  return 1024 + (size_t)ns * stage + (size_t)qt + (size_t)fine + (size_t)ns * 24 + 13 * 8 + 16 +
          16 + (size_t)(4 * S + 1) * 4;
 }
 
@@ -194,24 +202,24 @@ __device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+__device__ __forceinline__ f2 f2_sub(f2 a, f2 b) {
+  f2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 __device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
   f2 r;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
   return r;
 }
 // Two rotary pairs (x0, y0), (x1, y1) -- X = (x0, x1), Y = (y0, y1) -- turned
-// by R(base + d): the base's (cos, sin) of both pairs b = (c0, s0, c1, s1)
-// composed with R(d)'s f (angle addition), then x' = x c - y s, y' = y c + x s.
-__device__ __forceinline__ void rot2_composed(f2& X, f2& Y, float4 b, float4 f) {
-  const f2 Bc = f2_make(b.x, b.z), Bs = f2_make(b.y, b.w);
-  const f2 Fc = f2_make(f.x, f.z), Fs = f2_make(f.y, f.w);
-  const f2 NBs = f2_make(-b.y, -b.w);
-  const f2 Cc = f2_fma(NBs, Fs, f2_mul(Bc, Fc));
+// by the angle b + f: the cosines Bc and sines Bs of the base b of both pairs
+// composed with those of f (angle addition), then x' = x c - y s,
+// y' = y c + x s; ten packed f32x2 operations.
+__device__ __forceinline__ void rot2_composed(f2& X, f2& Y, f2 Bc, f2 Bs, f2 Fc, f2 Fs) {
+  const f2 Cc = f2_sub(f2_mul(Bc, Fc), f2_mul(Bs, Fs));
   const f2 Ss = f2_fma(Bc, Fs, f2_mul(Bs, Fc));
-  float s0, s1;
-  f2_split(Ss, s0, s1);
-  const f2 NSs = f2_make(-s0, -s1);
-  const f2 Xr = f2_fma(Y, NSs, f2_mul(X, Cc));
+  const f2 Xr = f2_sub(f2_mul(X, Cc), f2_mul(Y, Ss));
   const f2 Yr = f2_fma(X, Ss, f2_mul(Y, Cc));
   X = Xr;
   Y = Yr;
@@ -224,7 +232,8 @@ __device__ __forceinline__ void rot2_composed(f2& X, f2& Y, float4 b, float4 f) 
 // tile in place to its position (pre-RoPE keys) -- slot d of the block at
 // r0 + d, or r0 + d - W_ring past the ring's end -- and hand the stage on.  R(r0 + d) is the block's base row
 // R(r0) (or R(r0 - W_ring): the stage's second row |r0 - W_ring|, its sine
-// negated when r0 < W_ring) composed with R(d) from the resident table.  Item
+// negated when r0 < W_ring) composed with R(d) from the resident table, both
+// in the grouped layout (cosines of two pairs, then their sines).  Item
 // `it` of a block is key d = it mod TK and group g = it / TK of eight rotary
 // pairs: eight consecutive lanes take eight keys of one group, so their
 // 16-byte reads of the swizzled tile and of the table fall in eight
@@ -280,10 +289,10 @@ __device__ __forceinline__ void stage_tiles(const AttendParams& p, uint8_t* stag
       const float4* base = reinterpret_cast<const float4*>(kt + 2 * C::TILE);   // R(r0)
       const float4* basew = base + HALF / 2;                                  // |r0 - W_ring|
       const bool neg = wk.g.r0 < Wg;
+      static_assert(ITEMS % RT == 0, "every thread of a group takes the same number of items");
 #pragma unroll
-      for (int k0 = 0; k0 < (ITEMS + RT - 1) / RT; ++k0) {
+      for (int k0 = 0; k0 < ITEMS / RT; ++k0) {
         const int it = rt + k0 * RT;
-        if (it >= ITEMS) break;
         const int d = it & (TK - 1), g = it / TK;
         const bool wr = d >= wrap_at;
         const float4* bp = (wr ? basew : base) + 4 * g;
@@ -295,17 +304,18 @@ __device__ __forceinline__ void stage_tiles(const AttendParams& p, uint8_t* stag
         uint32_t w[8] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {   // pairs 8g + 2k and 8g + 2k + 1
-          float4 bb = bp[k];
-          if (wr && neg) { bb.y = -bb.y; bb.w = -bb.w; }
+          const float4 bb = bp[k];
           const float4 ff =
               *reinterpret_cast<const float4*>(frow + fine_chunk_rot(d, 4 * g + k));
+          f2 Bs = f2_make(bb.z, bb.w);
+          if (wr && neg) Bs = f2_mul(Bs, f2_make(-1.f, -1.f));
           // Split-half: x of the two pairs in word k of A, y in word k of B.
           // Interleaved: pair 8g + 2k + e is word 2k + e of A|B as (x, y).
           uint32_t& u0 = STYLE == 0 ? w[k] : w[2 * k];
           uint32_t& u1 = STYLE == 0 ? w[4 + k] : w[2 * k + 1];
           f2 X = STYLE == 0 ? f2_make(bf_lo(u0), bf_hi(u0)) : f2_make(bf_lo(u0), bf_lo(u1));
           f2 Y = STYLE == 0 ? f2_make(bf_lo(u1), bf_hi(u1)) : f2_make(bf_hi(u0), bf_hi(u1));
-          rot2_composed(X, Y, bb, ff);
+          rot2_composed(X, Y, f2_make(bb.x, bb.y), Bs, f2_make(ff.x, ff.y), f2_make(ff.z, ff.w));
           float x0, x1v, y0, y1;
           f2_split(X, x0, x1v);
           f2_split(Y, y0, y1);
@@ -362,7 +372,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* ofin = qready + 1;                                   // every product of a segment
   uint64_t* mdone = ofin + 1;                                    // a segment's products issued
   uint64_t* rxbar = mdone + 1;                                   // the peer's partial (CL)
-  uint32_t* tm_base = reinterpret_cast<uint32_t*>(rxbar + 1);    // tensor memory address
+  uint64_t* drain = rxbar + 1;                                   // [1 + TC_KB] issuers done
+  uint32_t* tm_base = reinterpret_cast<uint32_t*>(drain + 1 + TC_KB);   // tensor memory address
   int* flag = reinterpret_cast<int*>(tm_base + 4);               // ticket, abort, issued
   int* pre = flag + 4;                                           // [S+1] block prefix
   int* sa = pre + p.sh.S + 1;                                    // [S] ring start | npin
@@ -380,7 +391,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(smem_u32(rotd + i), TC_RW / TC_RG);   // every warp of the block's group
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(sfull + i), 1);
+      mbar_init(smem_u32(sfull + i), TC_KB);   // every Q K^T issuer's commit
       mbar_init(smem_u32(sfree + i), TC_SMW);
       mbar_init(smem_u32(pready + i), TC_SMW);
     }
@@ -388,6 +399,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     mbar_init(smem_u32(ofin), 1);
     mbar_init(smem_u32(mdone), 1);
     mbar_init(smem_u32(rxbar), TC_SMT);   // every softmax thread of rank 1
+    for (int i = 0; i <= TC_KB; ++i) mbar_init(smem_u32(drain + i), 1);
     fence_mbar_init();
     flag[1] = 0;
     flag[2] = 0;
@@ -402,7 +414,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if constexpr (ROTK) {
-    if (warp >= W_ROT0 && warp != W_MMA) load_fine_rot<D>(p, fine, staging_index(tid), TC_RW * 32);
+    if (staging_warp(warp)) load_fine_rot<D>(p, fine, staging_index(tid), TC_RW * 32);
   }
   prefetch_queries(p, D);
   prefetch_states(p);
@@ -428,15 +440,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ------------------------------------------------------------------ producer
     if (lane == 0)
       flag[2] = produce<D, ROTK, ROTK ? KEY_BASES : NO_ROWS>(
-          p, &tmK, &tmV, stages, full, empty, mdone, pre, sa, sfill, rb, re, abort_flag);
+          p, &tmK, &tmV, stages, full, empty, mdone, pre, sa, sfill, rb, re, abort_flag,
+          reinterpret_cast<const float2*>(p.table_g));
     __syncwarp();
-  } else if (warp >= W_ROT0 && warp != W_MMA) {
+  } else if (staging_warp(warp)) {
     // ------------------------------------------------------------- staging warps
     stage_tiles<D, STYLE, ROTK>(p, stages, fine, full, rotd, pre, sa, sfill, rb, re, abort_flag,
                                 staging_index(tid));
-  } else if (warp == W_MMA) {
-    // --------------------------------------------------------------- MMA issuer
+  } else if (warp == W_MMA || warp == W_QK0 || warp == W_QK0 + 1) {
+    // -------------------------------------------------------------- MMA issuers
+    // role -1: O += P V of every step (P from the step's P buffer, V from the
+    // stages), each block's stage released by the commit after its products;
+    // role i: S = Q K^T of block i of every step, over D in k-steps of 16 (32
+    // bytes of a 128-byte row), into the block's 32 columns of the step's S
+    // buffer.  Both Q K^T issuers commit to the S buffer's barrier (one with
+    // nothing to issue commits all the same).
     if (lane == 0) {
+      const int role = warp == W_MMA ? -1 : warp - W_QK0;
       const uint32_t id_qk = idesc_bf16(TC_ROWS, TK, 0);
       const uint32_t id_pv = idesc_bf16(TC_ROWS, D, 1);
       const uint32_t q_s = smem_u32(qt);
@@ -447,78 +467,68 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (!dead && !mbar_wait_or_abort(smem_u32(bar), parity, abort_flag)) dead = true;
         return !dead;
       };
-      // O += P V over the n blocks of step tp (first block jb), P from the
-      // step's P buffer; each block's stage is released by the commit after
-      // its products.
-      auto issue_pv = [&](int jb, int n, int tp, bool first) {
-        if (!wait(pready + (tp & 1), (tp >> 1) & 1)) return;
-        tc_fence_after();
-        for (int i = 0; i < n; ++i) {
-          const int sp = (jb + i) % NS;
-          const uint32_t v_s = smem_u32(stages + (size_t)sp * C::STAGE + C::TILE);
-#pragma unroll
-          for (int ks = 0; ks < TK / 16; ++ks) {
-            const uint64_t bd = sdesc(v_s + ks * 16 * 128, TK * 128, 1024);
-            tc_mma_ts(tmem + TM_O + (tp & 1) * D, tmem + TM_P + (tp & 1) * TM_PW + i * (TK / 2) +
-                      ks * 8, bd, id_pv, (first && i == 0 && ks == 0) ? 0 : 1);
-          }
-          tc_commit(smem_u32(empty + sp));
-        }
-      };
       for (int x = rb; x < re && !dead; ++seg) {
         const UnitRef u = unit_of_cached(x, p, pre, sa, sfill);
         const int x1 = min(u.uend, re);
-        if (!wait(qready, seg & 1)) break;
-        tc_fence_after();
-        int pj = 0, pn = 0;          // the previous step's first block and block count
+        if (role >= 0) {
+          if (!wait(qready, seg & 1)) break;
+          tc_fence_after();
+        }
         bool first[2] = {true, true};   // each stream's first product into its O
         while (x < x1 && !dead) {
           const int nb = min(TC_KB, x1 - x), bs = t & 1;
-          // The S buffer was read by the softmax of step t - 2.
-          if (t >= 2 && !wait(sfree + bs, ((t >> 1) - 1) & 1)) break;
-          // S = Q K^T of each block over D in k-steps of 16 (32 bytes of a
-          // 128-byte row), into the block's 32 columns of the buffer.
-          for (int i = 0; i < nb; ++i) {
-            const int sb = (jj + i) % NS;
-            if (!wait(ready + sb, ((jj + i) / NS) & 1)) break;
-            tc_fence_after();
-            const uint32_t k_s = smem_u32(stages + (size_t)sb * C::STAGE);
+          if (role >= 0) {
+            // The S buffer was read by the softmax of step t - 2.
+            if (t >= 2 && !wait(sfree + bs, ((t >> 1) - 1) & 1)) break;
+            if (role < nb) {
+              const int sb = (jj + role) % NS;
+              if (!wait(ready + sb, ((jj + role) / NS) & 1)) break;
+              tc_fence_after();
+              const uint32_t k_s = smem_u32(stages + (size_t)sb * C::STAGE);
 #pragma unroll
-            for (int ks = 0; ks < NKS; ++ks) {
-              const uint64_t a = sdesc(q_s + (ks >> 2) * (TC_ROWS * 128) + (ks & 3) * 32, 16, 1024);
-              const uint64_t bd = sdesc(k_s + (ks >> 2) * (TK * 128) + (ks & 3) * 32, 16, 1024);
-              tc_mma_ss(tmem + TM_S + bs * TM_SW + i * TK, a, bd, id_qk, ks > 0);
+              for (int ks = 0; ks < NKS; ++ks) {
+                const uint64_t a = sdesc(q_s + (ks >> 2) * (TC_ROWS * 128) + (ks & 3) * 32, 16, 1024);
+                const uint64_t bd = sdesc(k_s + (ks >> 2) * (TK * 128) + (ks & 3) * 32, 16, 1024);
+                tc_mma_ss(tmem + TM_S + bs * TM_SW + role * TK, a, bd, id_qk, ks > 0);
+              }
             }
+            tc_commit(smem_u32(sfull + bs));
+          } else {
+            if (!wait(pready + bs, (t >> 1) & 1)) break;
+            tc_fence_after();
+            for (int i = 0; i < nb; ++i) {
+              const int sp = (jj + i) % NS;
+              const uint32_t v_s = smem_u32(stages + (size_t)sp * C::STAGE + C::TILE);
+#pragma unroll
+              for (int ks = 0; ks < TK / 16; ++ks) {
+                const uint64_t bd = sdesc(v_s + ks * 16 * 128, TK * 128, 1024);
+                tc_mma_ts(tmem + TM_O + bs * D, tmem + TM_P + bs * TM_PW + i * (TK / 2) + ks * 8,
+                          bd, id_pv, (first[bs] && i == 0 && ks == 0) ? 0 : 1);
+              }
+              tc_commit(smem_u32(empty + sp));
+            }
+            first[bs] = false;
           }
-          if (dead) break;
-          tc_commit(smem_u32(sfull + bs));
-          if (pn > 0) {
-            issue_pv(pj, pn, t - 1, first[(t - 1) & 1]);
-            first[(t - 1) & 1] = false;
-          }
-          pj = jj;
-          pn = nb;
           jj += nb;
           x += nb;
           ++t;
         }
         if (dead) break;
-        if (pn > 0) issue_pv(pj, pn, t - 1, first[(t - 1) & 1]);
-        if (dead) break;
-        tc_commit(smem_u32(ofin));
-        // The producer may go on with the next segment (its epilogue leaves
-        // the stages alone).
-        mbar_arrive(smem_u32(mdone));
-      }
-      if (dead) {
-        if (!*abort_flag) {
-          *abort_flag = 1;
-          if (rb < re) p.st[unit_of_cached(rb, p, pre, sa, sfill).s].status = STATUS_DEVICE_STATE;
+        if (role < 0) {
+          tc_commit(smem_u32(ofin));
+          // The producer may go on with the next segment (its epilogue leaves
+          // the stages alone).
+          mbar_arrive(smem_u32(mdone));
         }
-        // Nothing leaves while products are in flight: one last commit, waited on.
-        tc_commit(smem_u32(ofin));
       }
-      flag[3] = seg;
+      if (dead && !*abort_flag) {
+        *abort_flag = 1;
+        if (rb < re) p.st[unit_of_cached(rb, p, pre, sa, sfill).s].status = STATUS_DEVICE_STATE;
+      }
+      // Nothing leaves while this thread's products are in flight (after an
+      // abort too): one last commit, waited on.
+      tc_commit(smem_u32(drain + role + 1));
+      mbar_wait(smem_u32(drain + role + 1), 0);
     }
     __syncwarp();
   } else {
@@ -908,9 +918,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if constexpr (CL) cluster_sync_all(); else __syncthreads();
   tc_fence_after();
   if (warp == W_MMA) {
-    // After an abort: no product may be in flight when the memory is freed.
-    if (*abort_flag && lane == 0) mbar_wait(smem_u32(ofin), (flag[3]) & 1);
-    __syncwarp();
+    // Every issuer drained its products before the barrier above.
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                  ::"r"(tmem), "r"(TM_COLS));
   }

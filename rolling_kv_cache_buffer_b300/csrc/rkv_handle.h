@@ -22,6 +22,7 @@ struct rkv_handle {
   int last_launches;
   float scale;
   std::vector<float2> host_table;  // kept alive until destroy
+  std::vector<float4> host_table_g;
 };
 
 namespace rkv {

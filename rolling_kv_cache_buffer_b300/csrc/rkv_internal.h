@@ -48,6 +48,8 @@ __device__ __forceinline__ int state_ok(const StreamState& s, const Shape& sh) {
 // Workspace carve-up (byte offsets from the workspace base).
 struct WsLayout {
   size_t table_off;        // float2 [2W][D/2]: (cos, sin)(m * w_i), m in [0, 2W)
+  size_t table_g_off;      // float4 [2W][D/4]: the same, chunk j = (cos, cos, sin, sin) of
+                           // pairs 2j and 2j+1 (the tcgen05 kernel's key rotation)
   size_t append_tk_off;    // int [S]  last-block tickets of the append kernel
   size_t rerot_tk_off;     // int [S]  last-block tickets of the re-rotation kernel
   size_t unit_tk_off;      // int [S*L*H_kv] tickets of split units (attention merge)
@@ -86,6 +88,7 @@ struct AttendParams {
   const void* q;
   float* out;
   const float2* table;
+  const float4* table_g;      // the table with each two pairs' cosines, then sines
   float* partials;
   int* unit_tickets;
   int layer_begin, L_att, c;  // layers of this call, queries per stream
