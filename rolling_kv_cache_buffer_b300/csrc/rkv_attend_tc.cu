@@ -706,6 +706,47 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // A warp without real rows only keeps step with its group (its
         // arrivals below); its lanes of S, P and O are never used.
         if (warp_rows) {
+        // One pass per block while no score exceeds the running maximum by
+        // more than TC_TAU (the common case once a stream has had a step):
+        // P = 2^(s - m) straight from the scores just read.  A block that
+        // would move the maximum sends the whole step down the two-pass path
+        // (maximum first, then P, which overwrites what was stored).
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        bool quiet = t < 2;   // the P buffer and O are free (step t - 2 done)
+        bool slow = false;
+        {
+          BlockWalk w = wk;
+#pragma unroll 1
+          for (int i = 0; i < nb; ++i) {
+            if (i) w.advance(1, u, p.sh);
+            uint32_t sr[32];
+            float sv[32];
+            load_s(TM_S + bs * TM_SW + i * TK, sr);
+            scores(w.g, sr, sv);
+            float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+            for (int d = 4; d < 32; ++d) mx[d & 3] = fmaxf(mx[d & 3], sv[d]);
+            const float bmi = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            if (__any_sync(0xffffffffu, bmi > m + TC_TAU)) { slow = true; break; }
+            if (!quiet) {
+              if (!waited(empty + jl2 % NS, (jl2 / NS) & 1)) break;
+              tc_fence_after();
+              quiet = true;
+            }
+            uint32_t pw[16];
+#pragma unroll
+            for (int d = 0; d < 32; d += 2) {
+              const float p0 = ex2(sv[d] - m);
+              const float p1 = ex2(sv[d + 1] - m);
+              ps[(d >> 1) & 3] += p0 + p1;
+              pw[d >> 1] = pack_bf2(p0, p1);
+            }
+            tc_st16(tmem + lane_addr + TM_P + bs * TM_PW + i * (TK / 2), pw);
+          }
+        }
+        if (dead) { next(); continue; }
+        if (slow) {
+        ps[0] = ps[1] = ps[2] = ps[3] = 0.f;
         // Pass 1: the step's maximum.
         float bm = -INFINITY;
         {
@@ -726,7 +767,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // This stream's previous step (t - 2): its products read the P buffer
         // and wrote O; both are quiet once the commit after its last block
         // has completed.
-        if (t >= 2) {
+        if (!quiet) {
           if (!waited(empty + jl2 % NS, (jl2 / NS) & 1)) { next(); continue; }
           tc_fence_after();
         }
@@ -750,7 +791,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         m = mnew;
         // Pass 2: P = 2^(s - m) (masked scores give 2^-inf = 0; m is always
         // finite), rounded to bf16, two per column of the P buffer.
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
         {
           BlockWalk w = wk;
 #pragma unroll 1
@@ -770,6 +810,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             tc_st16(tmem + lane_addr + TM_P + bs * TM_PW + i * (TK / 2), pw);
           }
+        }
         }
         l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         }
