@@ -74,6 +74,11 @@ __device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+__device__ __forceinline__ f2 f2_sub(f2 a, f2 b) {
+  f2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 __device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
   f2 r;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
@@ -81,24 +86,22 @@ __device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
 }
 
 // Two split-half key pairs (bf16x2 words x = dims (i, i+1), y = their partners
-// (i+D/2, i+D/2+1)) turned by R(base + d): `bs` = (cos, sin, cos, sin) of the
-// base for pairs i, i+1 (sine times sg), `ds` = (cos_i, cos_i+1, sin_i,
-// sin_i+1) of d.  Angles add: c = cb cd - sb sd, s = sb cd + cb sd; then
-// x' = x c - y s, y' = y c + x s, rounded to nearest even.
+// (i+D/2, i+D/2+1)) turned by R(base + d): `bs` = (cos_i, cos_i+1, sin_i,
+// sin_i+1) of the base (a chunk of the grouped table; the sines times sg),
+// `ds` the same of d.  Angles add: c = cb cd - sb sd, s = sb cd + cb sd; then
+// x' = x c - y s, y' = y c + x s, rounded to nearest even: ten packed f32x2
+// operations, the cosines and sines of both pairs each in one register pair.
 __device__ __forceinline__ void rot_pair2_composed(uint32_t& x, uint32_t& y, float4 bs, float sg,
                                                    float4 ds) {
-  const f2 CB = f2_make(bs.x, bs.z), SB = f2_make(sg * bs.y, sg * bs.w);
-  const f2 NSB = f2_make(-sg * bs.y, -sg * bs.w);
+  const f2 CB = f2_make(bs.x, bs.y);
+  f2 SB = f2_make(bs.z, bs.w);
+  if (sg < 0.f) SB = f2_mul(SB, f2_make(-1.f, -1.f));
   const f2 CD = f2_make(ds.x, ds.y), SD = f2_make(ds.z, ds.w);
-  const f2 Cc = f2_fma(NSB, SD, f2_mul(CB, CD));
-  const f2 Ss = f2_fma(SB, CD, f2_mul(CB, SD));
-  float c0, c1, s0, s1;
-  f2_split(Cc, c0, c1);
-  f2_split(Ss, s0, s1);
+  const f2 C = f2_sub(f2_mul(CB, CD), f2_mul(SB, SD));
+  const f2 S = f2_fma(SB, CD, f2_mul(CB, SD));
   const f2 X = f2_make(bf_lo(x), bf_hi(x));
   const f2 Y = f2_make(bf_lo(y), bf_hi(y));
-  const f2 C = f2_make(c0, c1), S = f2_make(s0, s1), NS = f2_make(-s0, -s1);
-  const f2 Xr = f2_fma(Y, NS, f2_mul(X, C));
+  const f2 Xr = f2_sub(f2_mul(X, C), f2_mul(Y, S));
   const f2 Yr = f2_fma(X, S, f2_mul(Y, C));
   float a, b, e, f;
   f2_split(Xr, a, b);
@@ -110,7 +113,8 @@ __device__ __forceinline__ void rot_pair2_composed(uint32_t& x, uint32_t& y, flo
 // Turns key slot d of a block tile in place by R(base + d): the 16-byte chunk
 // m of its first half (dims 8m..8m+7) with its partners (dims D/2+8m..), i.e.
 // split-half pairs 8m..8m+7; or, interleaved, the 4 pairs of chunk m.  `tb` is
-// the base's (cos, sin) row (sine times sg), `frow` the R(d) row of the fine
+// the base's row (sine times sg): of the grouped table for split-half pairs,
+// (cos, sin) per pair for interleaved ones; `frow` the R(d) row of the fine
 // table.
 template <int D, int STYLE>
 __device__ __forceinline__ void rotate_unit(uint8_t* kt, int d, int m, const float2* tb, float sg,
@@ -217,8 +221,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0)
-      flag[2] = produce<D, ROTK, KEY_BASES>(p, &tmK, &tmV, stages, full, empty, mdone, pre, sa,
-                                            sfill, rb, re, abort_flag);
+      flag[2] = produce<D, ROTK, KEY_BASES>(
+          p, &tmK, &tmV, stages, full, empty, mdone, pre, sa, sfill, rb, re, abort_flag,
+          STYLE == 0 ? reinterpret_cast<const float2*>(p.table_g) : nullptr);
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ consumers
