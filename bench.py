@@ -369,7 +369,7 @@ def run_gpu(args, rank, world):
     return res
 
 
-TC_AUTO_MIN_ROWS = 32   # the library's choice under "auto": chunks of c*G >= 32 rows
+TC_AUTO_MIN_ROWS = 16   # the library's choice under "auto": chunks of c*G >= 16 rows
 
 
 def chunk_on_tc(attend_impl, rows):

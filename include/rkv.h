@@ -84,8 +84,8 @@ typedef enum { RKV_PRE_ROPE = 0, RKV_STORED_ROTATED = 1 } rkv_layout;
 typedef enum { RKV_ROPE_SPLIT_HALF = 0, RKV_ROPE_INTERLEAVED = 1 } rkv_rope_style;
 
 /* Attention kernel family: AUTO picks the tensor-core kernels for bf16
- * caches -- single queries and chunks of fewer than 32 rows (c*G < 32) on
- * mma.sync, chunks of 32..128 rows on the fifth-generation tensor cores
+ * caches -- single queries and chunks of fewer than 16 rows (c*G < 16) on
+ * mma.sync, chunks of 16..128 rows on the fifth-generation tensor cores
  * (tcgen05, accumulators in tensor memory) -- and the CUDA-core kernel
  * otherwise; MMA keeps chunks on mma.sync (c*G <= 96); TC runs every chunk
  * with c*G <= 128 on tcgen05, single queries as AUTO. */

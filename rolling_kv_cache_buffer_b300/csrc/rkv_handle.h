@@ -54,9 +54,10 @@ inline int attend_grid(const rkv_handle* h, int n_layers) {
 
 // Chunks of at least this many rows (c*G) run on tcgen05 under RKV_ATTEND_AUTO:
 // below it most of the 128-row tile is padding and the mma.sync kernel wins
-// (measured on B300: 6 x 8 rows 113 us against 130 us; 4 x 1 rows 145 us
-// against 98 us).
-constexpr int kTcAutoMinRows = 32;
+// (attention alone, measured on B300: 2 x 8 rows 59 us against 64 us, 3 x 8
+// rows 61 against 86; 4 x 1 and 8 x 1 rows of the encoder shape 117 against
+// 92-96).
+constexpr int kTcAutoMinRows = 16;
 
 // Picks and launches the attention kernel for p.c queries per stream: the
 // tensor-core kernels for bf16 caches (single query on mma.sync; a chunk on

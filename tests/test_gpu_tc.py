@@ -197,3 +197,23 @@ def test_tc_pair_merge_stored_rotated_and_pinned():
         orc.append(k.double().numpy(), v.double().numpy())
         if t % 11 == 0 or t in (1, 2, 128, 129, 130, 139):
             compare(cache.attend(dev(q, torch.bfloat16)), orc.attend(q.double().numpy()))
+
+
+def test_tc_pair_merge_head_dim_64():
+    """The cluster merge with D = 64 (8 KV heads of one query head each, 8
+    queries per step: 8 rows per unit) over a 512-slot ring: two CTAs per
+    unit, windows of 9 blocks and the full ring, then steps that evict."""
+    from rolling_kv_cache_buffer_b300 import RollingKV
+    wl = WORKLOADS["audio8"].replace(n_layers=2, capacity=512, n_new=8)
+    cache = RollingKV(1, 2, 8, 8, 64, 512, max_chunk=8, attend_impl="tc")
+    orc = O.RollingCacheOracle(1, 2, 8, 8, 64, 512)
+    for i, (fill, origin) in enumerate([(280, 4_321), (512, 77_777)]):
+        k = random_rows((2, 8, fill, 64), 700 + 2 * i, torch.bfloat16)
+        v = random_rows((2, 8, fill, 64), 701 + 2 * i, torch.bfloat16)
+        write_window(cache, 0, origin, fill, k, v)
+        orc.set_state(0, origin, fill, k.double().numpy(), v.double().numpy())
+        for t in range(1, 4):
+            q, kn, vn = step_inputs(wl, 20 * i + t)
+            cache.append(dev(kn, torch.bfloat16), dev(vn, torch.bfloat16))
+            orc.append(kn.double().numpy(), vn.double().numpy())
+            compare(cache.attend(dev(q, torch.bfloat16)), orc.attend(q.double().numpy()))
