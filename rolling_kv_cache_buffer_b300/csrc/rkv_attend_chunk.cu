@@ -48,11 +48,14 @@ struct ChunkCfg : PipeCfg<D, ROTK> {
   static constexpr int SLOT = 32 + 16 * OSTR; // warp partial: m[16] l[16] o[16][OSTR]
 };
 
+// `slots`: bytes of merge slots of their own (0: they alias the stages).
 __host__ __device__ constexpr size_t chunk_smem_bytes(int stage, int fine, int qstr, int rows16,
-                                                      int ns, int S) {
-  return 1024 + (size_t)ns * stage + (size_t)fine + (size_t)rows16 * qstr * 4 + 16 + 16 +
-         (size_t)ns * 16 + (size_t)(3 * S + 1) * 4;
+                                                      int ns, int S, int slots = 0) {
+  return 1024 + (size_t)ns * stage + (size_t)fine + (size_t)rows16 * qstr * 4 + (size_t)slots +
+         16 + 16 + (size_t)ns * 16 + (size_t)(3 * S + 1) * 4;
 }
+// Stages a launch must keep for the merge slots to get memory of their own.
+constexpr int CH_OWN_SLOTS_MIN_STAGES = 10;
 
 __device__ __forceinline__ void rotc(float& x, float& y, float c, float s) {
   const float a = x * c - y * s;
@@ -157,7 +160,11 @@ __device__ __forceinline__ void rotate_unit(uint8_t* kt, int d, int m, const flo
 
 }  // namespace
 
-template <int D, bool ROTK, int STYLE>
+// OWN: the merge slots have shared memory of their own, so the producer goes
+// on into the next unit segment as soon as the consumers are done with the
+// stages (otherwise the slots alias the stages and the producer waits for
+// the merge; the ring then drains at every segment boundary).
+template <int D, bool ROTK, int STYLE, bool OWN>
 __global__ void __launch_bounds__(CH_THREADS, 1)
     attend_mma_chunk(const __grid_constant__ AttendParams p,
                      const __grid_constant__ CUtensorMap tmK,
@@ -174,10 +181,12 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   uint8_t* stages = smem;                                          // [NS][STAGE]
-  float* slots = reinterpret_cast<float*>(smem);                   // [CCW][SLOT], between segments
   uint8_t* fine = stages + (size_t)NS * C::STAGE;                  // [TK][D/2] (cos, sin)
   float* qs = reinterpret_cast<float*>(fine + C::FINE);            // [R16][QSTR] raw queries
-  int* flag = reinterpret_cast<int*>(qs + R16 * QSTR);             // ticket, abort, issued
+  // [CCW][SLOT] merge slots, used between segments: after the raw queries
+  // (OWN) or over the stages.
+  float* slots = OWN ? qs + R16 * QSTR : reinterpret_cast<float*>(smem);
+  int* flag = reinterpret_cast<int*>(qs + R16 * QSTR + (OWN ? CCW * SLOT : 0));   // ticket, abort, issued
   uint64_t* mdone = reinterpret_cast<uint64_t*>(flag + 4);         // segment merged
   uint64_t* full = mdone + 2;                                      // [NS]
   uint64_t* empty = full + NS;                                     // [NS]
@@ -491,6 +500,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 
       // ---- segment end: merge the teams (rows of each row group) ----
       named_bar_sync(CBAR_CONS, CCONS);      // nobody reads the stages any more
+      // With slots of their own the producer may fill the stages again now.
+      if (OWN && ct == 0) mbar_arrive(smem_u32(mdone));
       {
         float lsum[2];
 #pragma unroll
@@ -558,11 +569,13 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         }
       }
       if (has_next) load_query(unit_of_cached(x1, p, pre, sa, sfill));
-      // The slots' generic-proxy accesses come before the producer's next
-      // asynchronous copies into the same memory.
-      fence_proxy_async();
+      if constexpr (!OWN) {
+        // The slots' generic-proxy accesses come before the producer's next
+        // asynchronous copies into the same memory.
+        fence_proxy_async();
+      }
       named_bar_sync(CBAR_CONS, CCONS);
-      if (ct == 0) mbar_arrive(smem_u32(mdone));
+      if (!OWN && ct == 0) mbar_arrive(smem_u32(mdone));
       x = x1;
     }
   }
@@ -588,6 +601,20 @@ static int chunk_stages(const Shape& sh, int R) {
   // The merge slots live in the stage memory.
   if ((size_t)ns * C::STAGE < (size_t)CCW * C::SLOT * 4) return 0;
   return ns;
+}
+
+// Stages with merge slots of their own, or 0 when fewer than
+// CH_OWN_SLOTS_MIN_STAGES fit.
+template <int D, bool ROTK>
+static int chunk_stages_own(const Shape& sh, int R) {
+  using C = ChunkCfg<D, ROTK>;
+  const int rows16 = ((R + 15) / 16) * 16;
+  int ns = CH_MAX_STAGES;
+  while (ns >= CH_OWN_SLOTS_MIN_STAGES &&
+         chunk_smem_bytes(C::STAGE, C::FINE, C::QSTR, rows16, ns, sh.S, CCW * C::SLOT * 4) >
+             (size_t)SMEM_LIMIT)
+    --ns;
+  return ns >= CH_OWN_SLOTS_MIN_STAGES ? ns : 0;
 }
 
 template <int D, bool ROTK>
@@ -616,10 +643,14 @@ bool attend_chunk_supported(const Shape& sh, int c) {
 template <int D, bool ROTK, int STYLE>
 static cudaError_t launch_chunk_t(const AttendParams& p0, const CUtensorMap& tk,
                                   const CUtensorMap& tv, int grid, cudaStream_t s) {
+  using C = ChunkCfg<D, ROTK>;
   AttendParams p = p0;
-  p.ns = chunk_stages<D, ROTK>(p.sh, p.R);
-  const size_t smem = chunk_smem<D, ROTK>(p.sh, p.R);
-  auto kern = attend_mma_chunk<D, ROTK, STYLE>;
+  const int own = chunk_stages_own<D, ROTK>(p.sh, p.R);
+  p.ns = own ? own : chunk_stages<D, ROTK>(p.sh, p.R);
+  const size_t smem = own ? chunk_smem_bytes(C::STAGE, C::FINE, C::QSTR, ((p.R + 15) / 16) * 16,
+                                             own, p.sh.S, CCW * C::SLOT * 4)
+                          : chunk_smem<D, ROTK>(p.sh, p.R);
+  auto kern = own ? attend_mma_chunk<D, ROTK, STYLE, true> : attend_mma_chunk<D, ROTK, STYLE, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
