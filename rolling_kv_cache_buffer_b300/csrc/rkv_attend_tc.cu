@@ -27,8 +27,10 @@
 //    tensor memory (two bf16 per column);
 //  * O += P V takes P from tensor memory and the V tile from shared memory as
 //    an MN-major operand (dims contiguous per key).
-// The unit's split partials (m, l, O rows) merge across CTAs through global
-// memory: the last CTA to take the unit's ticket combines them.
+// A unit cut across CTAs is finished from their partials (m, l, O rows):
+// when every unit is cut into exactly two CTAs, launched as a 2-CTA cluster,
+// through distributed shared memory (rank 0 reads rank 1's); otherwise
+// through global memory, by the last CTA to take the unit's ticket.
 //
 // Roles (one persistent CTA per SM, 16 warps): warp 0 the TMA producer (the
 // stage ring of rkv_attend_pipe.cuh), warps 1-8 the softmax warps in two
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tma_prefetch_desc(&tmV);
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(full + i), 1);
-      mbar_init(smem_u32(empty + i), 1);      // the MMA issuer's commit
+      mbar_init(smem_u32(empty + i), 1);      // the P V issuer's commit
       mbar_init(smem_u32(rotd + i), TC_RW / TC_RG);   // every warp of the block's group
     }
     for (int i = 0; i < 2; ++i) {
