@@ -131,7 +131,7 @@ typedef struct {
   void* k_pool;           /* device, [S][L][H_kv][W][D] of kv_dtype           */
   void* v_pool;           /* device, same shape                               */
   void* state;            /* device, state_bytes (per-stream origin/fill/...) */
-  void* workspace;        /* device, workspace_bytes (RoPE table, partials)   */
+  void* workspace;        /* device, workspace_bytes (RoPE tables, partials)  */
   size_t workspace_bytes; /* size of workspace, >= rkv_required_bytes value   */
 } rkv_buffers;
 
