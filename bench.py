@@ -133,16 +133,22 @@ def kernel_hash(kernel_key):
     return h.hexdigest()[:16]
 
 
-def _traffic(kernel_key, workload):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel's sources changed since the counters were taken or the counters
-    were taken on another workload."""
+def _traffic(kernel_key, workload, alg_bytes_per_launch):
+    """DRAM bytes per launch from the committed ncu summary (the record
+    "<kernel>@<workload>" when there is one, else "<kernel>"), or None when
+    the kernel's sources changed since the counters were taken or the counters
+    were taken on another workload.  A record that states the algorithmic bytes
+    of the launch it captured (a workload whose fills grow from step to step)
+    is scaled to this line's algorithmic bytes per launch."""
     try:
         with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
             d = json.load(f)
-        ent = d.get(kernel_key)
+        ent = d.get(f"{kernel_key}@{workload}") or d.get(kernel_key)
         if (ent and ent.get("source_hash") == kernel_hash(kernel_key)
                 and ent.get("workload", "").split(" ")[0] == workload):
+            if ent.get("algorithmic_bytes"):
+                return round(ent["bytes_per_launch"] * alg_bytes_per_launch
+                             / ent["algorithmic_bytes"])
             return ent["bytes_per_launch"]
     except Exception:
         pass
@@ -652,8 +658,8 @@ def main():
                  "programmatic dependent launch (its prologue overlaps the append); the "
                  "attention's own share of the device time is in the committed launch list")
         kern_us = ms_local * 1e3
-    achieved = bytes_local / (kern_us * (wl.n_layers if res["fused"] and
-                                         (args.per_layer or args.graph) else 1) * 1e-6) / 1e9
+    kern_launches = wl.n_layers if res["fused"] and (args.per_layer or args.graph) else 1
+    achieved = bytes_local / (kern_us * kern_launches * 1e-6) / 1e9
     assert kern_us <= ms_local * 1e3 * (1 + 1e-9)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -681,7 +687,9 @@ def main():
                             "rkv_append + rkv_rebase + rkv_attend (all layers)")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
-                     "kernel": kernel_key, "traffic": _traffic(kernel_key, args.workload),
+                     "kernel": kernel_key,
+                     "traffic": _traffic(kernel_key, args.workload,
+                                         bytes_local / kern_launches),
                      "kernel_us": kern_us, "kernel_scope": scope},
         "e2e": ({"value": all_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                  "us_per_step": e2e_ms * 1e3, "us_per_step_mean": res["e2e"]["ms_mean"] * 1e3,

@@ -69,3 +69,23 @@ def test_pack_lays_out_aligned_views():
         assert torch.equal(view, t) and view.is_contiguous()
         assert (view.data_ptr() - flat.data_ptr()) % 16 == 0
     assert flat.numel() == q.numel() + 8 + k.numel()
+
+
+def test_traffic_record_per_workload_and_scaling(tmp_path, monkeypatch):
+    """`<kernel>@<workload>` wins over the plain kernel record; a record that
+    names another workload or another source hash gives None; a record with
+    the captured launch's algorithmic bytes scales to the line's bytes."""
+    import json
+    (tmp_path / "profiles").mkdir()
+    d = {"k": {"bytes_per_launch": 100, "source_hash": "h", "workload": "qwen3b (--x)"},
+         "k@grow": {"bytes_per_launch": 110, "algorithmic_bytes": 100, "source_hash": "h",
+                    "workload": "grow"},
+         "k@old": {"bytes_per_launch": 7, "source_hash": "stale", "workload": "old"}}
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps(d))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_hash", lambda key: "h")
+    assert bench._traffic("k", "qwen3b", 1) == 100
+    assert bench._traffic("k", "audio8", 1) is None
+    assert bench._traffic("k", "grow", 200) == 220
+    assert bench._traffic("k", "old", 1) is None
+    assert bench._traffic("other", "qwen3b", 1) is None
