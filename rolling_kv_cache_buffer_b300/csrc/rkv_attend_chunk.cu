@@ -196,6 +196,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   volatile int* abort_flag = flag + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The producer's first read after the dependency wait is the stream state:
+  // bring it into L2 before anything else.
+  prefetch_states(p);
   // Prologue: nothing here reads what the previous kernel of the stream writes.
   if (tid == 0) {
     tma_prefetch_desc(&tmK);
@@ -212,8 +215,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
   if constexpr (ROTK) {
     if (warp > 0) load_fine<D, STYLE, true>(p, fine, tid - 32, CCONS);
   }
-  prefetch_queries(p, D);
-  prefetch_states(p);
+  if (warp > 0) prefetch_queries(p, D, tid - 32, CH_THREADS - 32);
   pdl_wait();   // from here on: stream state, pools, queries, outputs
   pdl_trigger();   // a kernel launched next may start its own prologue
   if (warp == 0) {

@@ -347,6 +347,9 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
 
   constexpr int NTHR = mma_threads<FUSED>();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The producer's first read after the dependency wait is the stream state:
+  // bring it into L2 before anything else.
+  prefetch_states(p);
   // Prologue that reads nothing the previous kernel of the stream writes: the
   // barriers and the R(d) table (written once when the handle was created).
   if (tid == 0) {
@@ -386,21 +389,25 @@ __global__ void __launch_bounds__(mma_threads<FUSED>(), 1)
       }
     }
   }
-  prefetch_queries(p, D);
+  // The other warps bring this CTA's share of the queries (and of the step's
+  // new pairs, which no earlier kernel of the step writes) into L2; warp 0
+  // goes on to the stream state and its first copies.
+  if (warp > 0) {
+    prefetch_queries(p, D, tid - 32, NTHR - 32);
+    if constexpr (FUSED) {
+      const size_t nbytes = (size_t)p.L_att * p.sh.S * p.sh.Hkv * D * (p.sh.bf16 ? 2 : 4);
+      const size_t lines = (nbytes + 127) / 128;
+      const size_t l0 = lines * blockIdx.x / gridDim.x;
+      const size_t l1 = lines * (blockIdx.x + 1) / gridDim.x;
+      for (size_t l = l0 + tid - 32; l < l1; l += NTHR - 32) {
+        prefetch_l2(static_cast<const uint8_t*>(p.k_new) + l * 128);
+        prefetch_l2(static_cast<const uint8_t*>(p.v_new) + l * 128);
+      }
+    }
+  }
   // Cluster merge: the partner's barrier must exist before this CTA touches
   // it; every thread arrives here and waits once it has work under way.
   if constexpr (CL) cluster_arrive_relaxed();
-  if constexpr (FUSED) {
-    // The step's new pairs (not written by any earlier kernel of the step).
-    const size_t nbytes = (size_t)p.L_att * p.sh.S * p.sh.Hkv * D * (p.sh.bf16 ? 2 : 4);
-    const size_t lines = (nbytes + 127) / 128;
-    const size_t l0 = lines * blockIdx.x / gridDim.x, l1 = lines * (blockIdx.x + 1) / gridDim.x;
-    for (size_t l = l0 + tid; l < l1; l += blockDim.x) {
-      prefetch_l2(static_cast<const uint8_t*>(p.k_new) + l * 128);
-      prefetch_l2(static_cast<const uint8_t*>(p.v_new) + l * 128);
-    }
-  }
-  prefetch_states(p);
   pdl_wait();   // from here on: stream state, pools, queries, outputs
   pdl_trigger();   // a kernel launched next may start its own prologue
   // Warp 0 builds the block prefix and starts streaming at once; the

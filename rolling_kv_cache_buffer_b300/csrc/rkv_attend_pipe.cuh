@@ -97,13 +97,16 @@ __device__ __forceinline__ void load_fine(const AttendParams& p, uint8_t* fine, 
   }
 }
 
-// Threads of the CTA bring its share of the queries into L2 (the queries are
-// not written by the append kernel that may still be running).
-__device__ __forceinline__ void prefetch_queries(const AttendParams& p, int D) {
+// Threads t0, t0 + nt, ... of the CTA (all of them by default) bring its share
+// of the queries into L2 (the queries are not written by the append kernel
+// that may still be running).
+__device__ __forceinline__ void prefetch_queries(const AttendParams& p, int D, int t0 = -1,
+                                                 int nt = 0) {
+  if (t0 < 0) { t0 = threadIdx.x; nt = blockDim.x; }
   const size_t qbytes = (size_t)p.L_att * p.sh.S * p.c * p.sh.Hq * D * (p.sh.q_bf16 ? 2 : 4);
   const size_t lines = (qbytes + 127) / 128;
   const size_t l0 = lines * blockIdx.x / gridDim.x, l1 = lines * (blockIdx.x + 1) / gridDim.x;
-  for (size_t l = l0 + threadIdx.x; l < l1; l += blockDim.x)
+  for (size_t l = l0 + t0; l < l1; l += nt)
     prefetch_l2(static_cast<const uint8_t*>(p.q) + l * 128);
 }
 

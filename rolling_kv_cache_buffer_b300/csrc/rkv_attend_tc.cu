@@ -384,6 +384,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   volatile int* abort_flag = flag + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The producer's first read after the dependency wait is the stream state:
+  // bring it into L2 before anything else.
+  prefetch_states(p);
   if (tid == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -418,8 +421,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if constexpr (ROTK) {
     if (staging_warp(warp)) load_fine_rot<D>(p, fine, staging_index(tid), TC_RW * 32);
   }
-  prefetch_queries(p, D);
-  prefetch_states(p);
+  if (warp > 0) prefetch_queries(p, D, tid - 32, TC_THREADS - 32);
   pdl_wait();      // from here on: stream state, pools, queries, outputs
   pdl_trigger();   // a kernel launched next may start its own prologue
   tc_fence_before();
