@@ -35,8 +35,12 @@ constexpr int kMinBlocksPerCta = 8;
 // is cut into equal shares, CTA b taking [b*T/P, (b+1)*T/P).  With one stream
 // every unit (layer, KV head) has the same number of blocks, so a grid of
 // U*k CTAs (U units, k = #SMs / U) cuts each unit into exactly k equal parts:
-// no CTA crosses a unit boundary and nothing is merged mid-stream.  Several
-// streams (fills unknown to the host) use one CTA per SM.
+// no CTA crosses a unit boundary and nothing is merged mid-stream.  With more
+// units than SMs, a grid between 3/4 of the SMs and all of them that divides
+// U gives every CTA whole units, again with nothing merged across CTAs (on
+// B300 the encoder shape, 640 units of 24 blocks: 128 CTAs of 5 whole units
+// take the step from 93.3 to 79.2 us against 148 CTAs that merge split
+// units).  Several streams (fills unknown to the host) use one CTA per SM.
 inline int attend_grid(const rkv_handle* h, int n_layers) {
   const int sms = h->num_sms < kMaxCtas ? h->num_sms : kMaxCtas;
   const int units = n_layers * h->sh.Hkv;
@@ -49,6 +53,9 @@ inline int attend_grid(const rkv_handle* h, int n_layers) {
     if (per > cap) per = cap > 1 ? cap : 1;
     return units * per;
   }
+  if (h->sh.S == 1)
+    for (int g = sms; g >= sms * 3 / 4; --g)
+      if (units % g == 0) return g;
   return sms;
 }
 
