@@ -63,7 +63,8 @@ inline int attend_grid(const rkv_handle* h, int n_layers) {
 // below it most of the 128-row tile is padding and the mma.sync kernel wins
 // (attention alone, measured on B300: 2 x 8 rows 59 us against 64 us, 3 x 8
 // rows 61 against 86; 4 x 1 and 8 x 1 rows of the encoder shape 117 against
-// 92-96).
+// 92-96 with split units, and the encoder's whole step 101 against 79 with
+// whole units per CTA).
 constexpr int kTcAutoMinRows = 16;
 
 // Picks and launches the attention kernel for p.c queries per stream: the
