@@ -89,3 +89,25 @@ def test_traffic_record_per_workload_and_scaling(tmp_path, monkeypatch):
     assert bench._traffic("k", "grow", 200) == 220
     assert bench._traffic("k", "old", 1) is None
     assert bench._traffic("other", "qwen3b", 1) is None
+
+
+def test_committed_traffic_records_are_well_formed():
+    """Every record in profiles/dram_traffic.json names a timed kernel and a
+    workload that bench.py runs, and its bytes add up; a record keyed
+    <kernel>@<workload> names that workload."""
+    import json
+    import os
+    with open(os.path.join(bench.ROOT, "profiles", "dram_traffic.json")) as f:
+        d = json.load(f)
+    assert d
+    for key, e in d.items():
+        kernel = key.split("@")[0]
+        assert kernel in bench.KERNEL_SOURCE, key
+        assert e["source"] == bench.KERNEL_SOURCE[kernel]
+        assert e["bytes_per_launch"] == e["dram_read"] + e["dram_write"] > 0
+        wl = e["workload"].split(" ")[0]
+        assert wl in bench.WORKLOAD_TEXT, key
+        if "@" in key:
+            assert key.split("@")[1] == wl
+        if "algorithmic_bytes" in e:
+            assert 1.0 <= e["bytes_per_launch"] / e["algorithmic_bytes"] < 1.1, key
